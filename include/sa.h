@@ -1,0 +1,190 @@
+/*
+ * sa.h -- C ABI of libsa27: DeepSeek-V4 style hybrid compressed attention
+ * (CSA + HCA) on one NVIDIA B300 (sm_103a).
+ *
+ * The operations follow these web pages (cited by title and section):
+ *  [P2]  "오픈소스 LLM의 새 이정표: DeepSeek-V4 시리즈" -- section
+ *        "압축 희소 어텐션(CSA)과 극압축 어텐션(HCA)": CSA compresses every m
+ *        consecutive KV entries into one, each query attends only its top-k
+ *        compressed entries, and a sliding-window branch keeps local detail;
+ *        HCA compresses m' (>> m) entries into one and attends densely.
+ *  [P2q] same page, section "오픈소스 MoE 인프라: MegaMoE와 TileLang": the
+ *        indexer QK path is stored as MXFP4 and dequantised to FP8 losslessly.
+ *  [P3]  "DeepSeek-V4 논문 읽기: 백만 토큰 컨텍스트를 저렴하게" -- sections
+ *        "Compressed Sparse Attention (CSA)" (1 compress blocks, 2 the indexer
+ *        finds relevant blocks, 3 only the top candidates are attended, 4 recent
+ *        tokens kept by a sliding window), "Heavily Compressed Attention (HCA)"
+ *        and "KV Cache 관리: 저장 구조까지 변경" (compressed cache, sliding-window
+ *        cache, tail of tokens not yet compressed).
+ *  [P1]  "EP 95. DeepSeek-V4 논문 읽기 — 노정석" -- section IDEAS: KV cache
+ *        compressed to 1/4, a lightning indexer selects the top-k, multi-query
+ *        attention (one shared KV head).
+ * Readings where the pages are silent: pooling = softmax over one fp32 logit
+ * per raw token; indexer score s = sum_h w_h * ReLU(q_h . k); block j is
+ * visible to a query at position t iff j < floor((t+1)/m); ties in top-k go
+ * to the lower index; the CSA softmax runs over selected rows and window rows
+ * together; HCA also attends the window.
+ *
+ * Conventions for every call
+ *  - All tensor pointers are DEVICE pointers owned by the caller; dense,
+ *    row-major, in the layouts given per call.  Bulk arrays must be 16-byte
+ *    aligned.  Nothing is allocated, freed or synchronised inside a call;
+ *    work is enqueued on `stream` (a cudaStream_t; NULL = legacy default).
+ *  - Scratch memory is the caller's `ws` of `ws_bytes` bytes, at least the
+ *    size the matching *_workspace_bytes() query returns (256-byte aligned).
+ *  - Return value: SA_OK, or an sa_status for a host-side rejection (bad
+ *    argument, unsupported shape) or a CUDA launch error.  Problems found on
+ *    the device (an index out of range, a NaN score, a wait that timed out) are
+ *    OR-ed as (1 << status) into the optional device word `err` (may be NULL);
+ *    the kernels never trap and leave the context usable.
+ *  - Positions are 0-based.  q_pos[b*T + t] is the position of query t of
+ *    sequence b; L = q_pos + 1 tokens are visible to it, including itself.
+ *  - Raw (uncompressed) per-token arrays are rings of R rows: raw position p
+ *    lives in row p mod R (R = sequence length gives the identity layout).
+ *  - Calls are stateless and may be issued from several host threads.
+ */
+#ifndef SA27_H
+#define SA27_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SA_OK = 0,
+  SA_ERR_INVALID_ARG = 1,    /* null pointer, bad size, misaligned array  */
+  SA_ERR_UNSUPPORTED = 2,    /* valid but not implemented for this shape  */
+  SA_ERR_CUDA = 3,           /* CUDA runtime/driver error at launch       */
+  SA_ERR_DEVICE_TIMEOUT = 4, /* device: a bounded wait gave up            */
+  SA_ERR_BOUNDS = 5,         /* device: index/position outside its range  */
+  SA_ERR_NAN = 6             /* device: NaN candidate score in top-k      */
+} sa_status;
+
+typedef enum {
+  SA_F32 = 0,   /* float32                                                  */
+  SA_BF16 = 1,  /* bfloat16                                                 */
+  SA_MXFP4 = 2  /* indexer path only: e2m1 codes, two per byte (element 2i in
+                   the low nibble), plus one e8m0 scale byte per 32 elements */
+} sa_dtype;
+
+/* Text for a status code (static string). */
+const char* sa_status_string(int status);
+
+/* ---------------------------------------------------------------------------
+ * csa_compress -- block compression ([P2], [P3] CSA step 1; KV cache layout
+ * of [P3] "KV Cache 관리").
+ * For each sequence b and each block j in [blk_lo[b], blk_hi[b]):
+ *     a_i = softmax(z[p_i] : i < m)_i,   p_i = j*m + i,
+ *     X_c[b, j, :] = sum_i a_i * X_raw[b, p_i mod R, :]
+ * for X in {K, V} (width d) and, if ik_raw != NULL, the indexer keys
+ * (width dI).  Results are rounded to the storage type (bf16: nearest-even).
+ * The same call with m = m' builds the HCA cache (ik_raw = NULL).
+ *  dtype     SA_F32 or SA_BF16: storage type of k_raw, v_raw, k_c, v_c
+ *  ik_dtype  SA_F32 / SA_BF16 (ik_raw and ik_c share it) or SA_MXFP4
+ *            (ik_raw bf16; ik_c receives codes [B,N_cap,dI/2] u8 and
+ *            ik_c_scales [B,N_cap,dI/32] u8, quantised from the bf16-rounded
+ *            pooled values by the OCP MX v1.0 rule)
+ *  k_raw, v_raw [B,R,d]; ik_raw [B,R,dI] or NULL; z [B,R] f32 pooling logits
+ *  blk_lo, blk_hi [B] int32 device; max_blocks = host bound on
+ *            blk_hi[b]-blk_lo[b] (sizes the grid; larger ranges -> SA_ERR_BOUNDS)
+ *  k_c, v_c [B,N_cap,d]; ik_c as above (NULL iff ik_raw is NULL)
+ * Device errors: block outside [0, N_cap) -> SA_ERR_BOUNDS (block skipped).
+ */
+int csa_compress(int dtype, int ik_dtype, int B, int d, int dI, int m, const void* k_raw,
+                 const void* v_raw, const void* ik_raw, const float* z, int R,
+                 const int32_t* blk_lo, const int32_t* blk_hi, int max_blocks, void* k_c,
+                 void* v_c, void* ik_c, void* ik_c_scales, int N_cap, int32_t* err,
+                 void* stream);
+
+/* ---------------------------------------------------------------------------
+ * csa_index_topk -- lightning-indexer scores and per-query top-k ([P1] IDEAS;
+ * [P3] CSA steps 2-3; [P2] "top-k compressed entries").
+ * For query row r = b*T + t at position p = q_pos[r], n = floor((p+1)/m):
+ *     s[r, j] = sum_h w[r,h] * max(0, q_I[r,h,:] . Ik_c[b,j,:]),  0 <= j < n
+ * idx[r, :] = the min(k, n) indices j with the highest s (equal scores: lower
+ * j first), written in ascending order, padded with -1.
+ *  q_dtype   SA_F32, SA_BF16 or SA_MXFP4; ik_c has the same dtype
+ *  q_idx     [B,T,HI,dI] (MXFP4: codes [B,T,HI,dI/2] + q_scales [B,T,HI,dI/32])
+ *  w         [B,T,HI] f32 indexer head weights
+ *  ik_c      [B,N_cap,dI] (MXFP4: codes + ik_scales as in csa_compress)
+ *  q_pos     [B,T] int32
+ *  idx       [B,T,k] int32 output
+ *  scores_out  optional [B,T,N_cap] f32: receives s (entries j >= n untouched)
+ *  scores_in   optional [B,T,N_cap] f32: if given, scoring is skipped and the
+ *              top-k selects from these values (same n per row)
+ * Supported: dI = 64 and HI in {1..64} multiple of ... (see sa_status);
+ * bf16 / MXFP4 with HI = 64 run on the tensor cores; f32 on CUDA cores.
+ * N_cap <= 786432.  Device errors: NaN score -> SA_ERR_NAN (row written as
+ * all -1); n > N_cap -> SA_ERR_BOUNDS (n clamped).
+ */
+int csa_index_topk(int q_dtype, int B, int T, int HI, int dI, int m, int k, const void* q_idx,
+                   const void* q_scales, const float* w, const void* ik_c,
+                   const void* ik_scales, int N_cap, const int32_t* q_pos, int32_t* idx,
+                   float* scores_out, const float* scores_in, void* ws, size_t ws_bytes,
+                   int32_t* err, void* stream);
+size_t csa_index_topk_workspace_bytes(int B, int T, int N_cap, int k);
+
+/* ---------------------------------------------------------------------------
+ * csa_attend -- sparse multi-query attention over the selected compressed
+ * rows plus the sliding window, in one softmax ([P2]; [P3] CSA steps 3-4).
+ * For query row r (sequence b, position p), n = floor((p+1)/m),
+ * S = { idx[r,i] : i < min(k,n), idx[r,i] >= 0 },  Wn = min(W, p+1):
+ *     keys   = { K_c[b,j] : j in S }  (+)  { K_raw[b, u mod R] : p-Wn < u <= p }
+ *     l      = sm_scale * q[r,h,:] . key
+ *     lse[r,h] = log sum exp(l),   o[r,h,:] = sum softmax(l) * value
+ * An empty key set gives o = 0, lse = -inf.
+ *  dtype     SA_F32 or SA_BF16 for q, k_c, v_c, k_raw, v_raw
+ *  q [B,T,H,d]; k_c, v_c [B,N_cap,d]; idx [B,T,k]; k_raw, v_raw [B,R,d]
+ *  o [B,T,H,d] f32; lse [B,T,H] f32 (natural log)
+ * bf16 with H <= 64, d = 128 runs on the tensor cores; other shapes on CUDA
+ * cores (d <= 256).  Requires R >= W.
+ * Device errors: idx entry >= n or < -1 -> SA_ERR_BOUNDS (entry ignored).
+ */
+int csa_attend(int dtype, int B, int T, int H, int d, int m, int k, int W, float sm_scale,
+               const void* q, const int32_t* q_pos, const void* k_c, const void* v_c,
+               int N_cap, const int32_t* idx, const void* k_raw, const void* v_raw, int R,
+               float* o, float* lse, void* ws, size_t ws_bytes, int32_t* err, void* stream);
+size_t csa_attend_workspace_bytes(int dtype, int B, int T, int H, int d, int k, int W);
+
+/* ---------------------------------------------------------------------------
+ * hca_compress_attend -- heavy compression then dense attention ([P2] HCA;
+ * [P3] "Heavily Compressed Attention (HCA)").
+ * First compresses blocks [blk_lo[b], blk_hi[b]) of m2 raw rows into
+ * hk_c/hv_c exactly as csa_compress does (no indexer keys); then, for query
+ * row r at position p, n2 = floor((p+1)/m2), Wn = min(W, p+1):
+ *     keys = { hK_c[b,j] : j < n2 }  (+)  { K_raw[b, u mod R] : p-Wn < u <= p }
+ * with the same softmax, o and lse definitions as csa_attend.
+ *  q [B,T,H,d]; k_raw, v_raw [B,R,d]; z_hca [B,R] f32; hk_c, hv_c [B,N2_cap,d]
+ *  o [B,T,H,d] f32; lse [B,T,H] f32
+ * Requires R >= W and, when compressing, R >= m2.
+ */
+int hca_compress_attend(int dtype, int B, int T, int H, int d, int m2, int W, float sm_scale,
+                        const void* q, const int32_t* q_pos, const void* k_raw,
+                        const void* v_raw, const float* z_hca, int R, const int32_t* blk_lo,
+                        const int32_t* blk_hi, int max_blocks, void* hk_c, void* hv_c,
+                        int N2_cap, float* o, float* lse, void* ws, size_t ws_bytes,
+                        int32_t* err, void* stream);
+size_t hca_compress_attend_workspace_bytes(int dtype, int B, int T, int H, int d, int N2_cap,
+                                           int W);
+
+/* ---------------------------------------------------------------------------
+ * attn_merge -- exact log-sum-exp merge of attention partials computed over
+ * disjoint key sets (the branches of the multi-branch design, [P2] and [P1]
+ * IDEAS; also split-K partials):
+ *     lse = log sum_i exp(lse_i),   o = sum_i exp(lse_i - lse) * o_i
+ * Parts with lse_i = -inf contribute nothing; all -inf gives o = 0, lse = -inf.
+ *  n         number of parts, 1..8
+ *  o_parts   HOST array of n device pointers, each [rows, d] f32
+ *  lse_parts HOST array of n device pointers, each [rows] f32
+ *  o         [rows, d] in o_dtype (SA_F32 or SA_BF16); lse [rows] f32
+ */
+int attn_merge(int n, const float* const* o_parts, const float* const* lse_parts, int64_t rows,
+               int d, void* o, int o_dtype, float* lse, int32_t* err, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SA27_H */

@@ -1,0 +1,152 @@
+"""Python binding of libsa27 (hybrid compressed attention, CSA + HCA, on B300).
+
+Argument marshalling only: every function below has the name of the C entry
+point it calls (declared in ``include/sa.h``), passes device pointers of
+torch tensors (``data_ptr()``), sizes and the current CUDA stream, and turns
+a non-zero status into ``SaError``.  All computation happens in the library's
+CUDA kernels; there is no other implementation behind these names.  If the
+library is missing, importing this package raises: there is no fallback.
+
+Build the library with ``python -m sparse_attention_27_b300.build``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsa27.so")
+
+SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA = 0, 1, 2, 3
+SA_ERR_DEVICE_TIMEOUT, SA_ERR_BOUNDS, SA_ERR_NAN = 4, 5, 6
+SA_F32, SA_BF16, SA_MXFP4 = 0, 1, 2
+
+EXPORTS = (
+    "sa_status_string", "csa_compress", "csa_index_topk", "csa_index_topk_workspace_bytes",
+    "csa_attend", "csa_attend_workspace_bytes", "hca_compress_attend",
+    "hca_compress_attend_workspace_bytes", "attn_merge",
+)
+
+
+class SaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libsa27.so not built at {LIB_PATH}; run python -m sparse_attention_27_b300.build")
+
+_lib = C.CDLL(LIB_PATH)
+_vp, _i, _i64, _f, _sz = C.c_void_p, C.c_int, C.c_int64, C.c_float, C.c_size_t
+
+_lib.sa_status_string.argtypes = [_i]
+_lib.sa_status_string.restype = C.c_char_p
+_lib.csa_compress.argtypes = [_i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp,
+                              _vp, _vp, _vp, _i, _vp, _vp]
+_lib.csa_index_topk.argtypes = [_i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp,
+                                _vp, _vp, _vp, _vp, _sz, _vp, _vp]
+_lib.csa_index_topk_workspace_bytes.argtypes = [_i, _i, _i, _i]
+_lib.csa_index_topk_workspace_bytes.restype = _sz
+_lib.csa_attend.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _i, _vp, _vp,
+                            _vp, _i, _vp, _vp, _vp, _sz, _vp, _vp]
+_lib.csa_attend_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+_lib.csa_attend_workspace_bytes.restype = _sz
+_lib.hca_compress_attend.argtypes = [_i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _i,
+                                     _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp, _vp]
+_lib.hca_compress_attend_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+_lib.hca_compress_attend_workspace_bytes.restype = _sz
+_lib.attn_merge.argtypes = [_i, _vp, _vp, _i64, _i, _vp, _i, _vp, _vp, _vp]
+
+
+def library() -> C.CDLL:
+    return _lib
+
+
+def status_string(s: int) -> str:
+    return _lib.sa_status_string(int(s)).decode()
+
+
+def _p(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(s: int, where: str) -> None:
+    if s != SA_OK:
+        raise SaError(s, where)
+
+
+def dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SA_F32
+    if t.dtype == torch.bfloat16:
+        return SA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def csa_compress(dtype, ik_dtype, B, d, dI, m, k_raw, v_raw, ik_raw, z, R, blk_lo, blk_hi,
+                 max_blocks, k_c, v_c, ik_c, ik_c_scales, N_cap, err=None, stream=None):
+    _check(_lib.csa_compress(dtype, ik_dtype, B, d, dI, m, _p(k_raw), _p(v_raw), _p(ik_raw), _p(z),
+                             R, _p(blk_lo), _p(blk_hi), max_blocks, _p(k_c), _p(v_c), _p(ik_c),
+                             _p(ik_c_scales), N_cap, _p(err), _stream(stream)), "csa_compress")
+
+
+def csa_index_topk_workspace_bytes(B, T, N_cap, k) -> int:
+    return int(_lib.csa_index_topk_workspace_bytes(B, T, N_cap, k))
+
+
+def csa_index_topk(q_dtype, B, T, HI, dI, m, k, q_idx, q_scales, w, ik_c, ik_scales, N_cap, q_pos,
+                   idx, scores_out=None, scores_in=None, ws=None, ws_bytes=0, err=None,
+                   stream=None):
+    _check(_lib.csa_index_topk(q_dtype, B, T, HI, dI, m, k, _p(q_idx), _p(q_scales), _p(w),
+                               _p(ik_c), _p(ik_scales), N_cap, _p(q_pos), _p(idx),
+                               _p(scores_out), _p(scores_in), _p(ws), ws_bytes, _p(err),
+                               _stream(stream)), "csa_index_topk")
+
+
+def csa_attend_workspace_bytes(dtype, B, T, H, d, k, W) -> int:
+    return int(_lib.csa_attend_workspace_bytes(dtype, B, T, H, d, k, W))
+
+
+def csa_attend(dtype, B, T, H, d, m, k, W, sm_scale, q, q_pos, k_c, v_c, N_cap, idx, k_raw, v_raw,
+               R, o, lse, ws=None, ws_bytes=0, err=None, stream=None):
+    _check(_lib.csa_attend(dtype, B, T, H, d, m, k, W, sm_scale, _p(q), _p(q_pos), _p(k_c),
+                           _p(v_c), N_cap, _p(idx), _p(k_raw), _p(v_raw), R, _p(o), _p(lse),
+                           _p(ws), ws_bytes, _p(err), _stream(stream)), "csa_attend")
+
+
+def hca_compress_attend_workspace_bytes(dtype, B, T, H, d, N2_cap, W) -> int:
+    return int(_lib.hca_compress_attend_workspace_bytes(dtype, B, T, H, d, N2_cap, W))
+
+
+def hca_compress_attend(dtype, B, T, H, d, m2, W, sm_scale, q, q_pos, k_raw, v_raw, z_hca, R,
+                        blk_lo, blk_hi, max_blocks, hk_c, hv_c, N2_cap, o, lse, ws=None,
+                        ws_bytes=0, err=None, stream=None):
+    _check(_lib.hca_compress_attend(dtype, B, T, H, d, m2, W, sm_scale, _p(q), _p(q_pos),
+                                    _p(k_raw), _p(v_raw), _p(z_hca), R, _p(blk_lo), _p(blk_hi),
+                                    max_blocks, _p(hk_c), _p(hv_c), N2_cap, _p(o), _p(lse), _p(ws),
+                                    ws_bytes, _p(err), _stream(stream)), "hca_compress_attend")
+
+
+def attn_merge(o_parts, lse_parts, o, lse, err=None, stream=None):
+    """o_parts: list of [rows, d] f32 tensors; lse_parts: list of [rows] f32."""
+    n = len(o_parts)
+    rows, d = o_parts[0].shape[0], o_parts[0].shape[-1]
+    op = (C.c_void_p * n)(*[t.data_ptr() for t in o_parts])
+    lp = (C.c_void_p * n)(*[t.data_ptr() for t in lse_parts])
+    _check(_lib.attn_merge(n, C.cast(op, C.c_void_p), C.cast(lp, C.c_void_p), rows, d, _p(o),
+                           dtype_code(o), _p(lse), _p(err), _stream(stream)), "attn_merge")

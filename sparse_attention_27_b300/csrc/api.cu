@@ -1,0 +1,257 @@
+// extern "C" entry points of libsa27 (declared and documented in include/sa.h):
+// host-side argument validation, kernel choice by dtype and shape, workspace
+// carving and launches.  Nothing here allocates, frees or synchronises.
+#include <mutex>
+
+#include "kernels.cuh"
+
+using namespace sa;
+
+namespace {
+
+int device_sms() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int elem_bytes(int dt) { return dt == SA_F32 ? 4 : 2; }
+bool plain_dtype(int dt) { return dt == SA_F32 || dt == SA_BF16; }
+int status_of(cudaError_t e) {
+  if (e == cudaSuccess) return SA_OK;
+  cudaGetLastError();  // clear a sticky launch error for the caller's next call
+  return SA_ERR_CUDA;
+}
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Key-tile split of each query row's key list for the attention kernels.
+struct Split {
+  int nsplit, split_tiles;
+};
+Split choose_split(int64_t rows, int max_tiles) {
+  Split s{1, max_tiles > 0 ? max_tiles : 1};
+  if (rows <= 0 || max_tiles <= 1) return s;
+  const int64_t want = (2LL * device_sms() + rows - 1) / rows;   // CTAs per row
+  int ns = (int)std::min<int64_t>(want, max_tiles);
+  if (ns < 1) ns = 1;
+  s.split_tiles = (max_tiles + ns - 1) / ns;
+  s.nsplit = (max_tiles + s.split_tiles - 1) / s.split_tiles;
+  return s;
+}
+size_t split_bytes(int64_t rows, int H, int d, const Split& s) {
+  if (s.nsplit <= 1) return 0;
+  return round256(sizeof(float) * (size_t)rows * s.nsplit * H * d) +
+         round256(sizeof(float) * (size_t)rows * s.nsplit * H);
+}
+int attn_tiles(int64_t n_comp_max, int W) {
+  return (int)((n_comp_max + kAttnTile - 1) / kAttnTile + (W + kAttnTile - 1) / kAttnTile);
+}
+
+int run_attention(AttnArgs& a, void* ws, size_t ws_bytes, int max_tiles, cudaStream_t st) {
+  const int64_t rows = (int64_t)a.B * a.T;
+  const Split s = choose_split(rows, max_tiles);
+  a.nsplit = s.nsplit;
+  a.split_tiles = s.split_tiles;
+  a.part_o = nullptr;
+  a.part_lse = nullptr;
+  if (s.nsplit > 1) {
+    const size_t need = split_bytes(rows, a.H, a.d, s);
+    if (ws == nullptr || ws_bytes < need || !al16(ws)) return SA_ERR_INVALID_ARG;
+    a.part_o = static_cast<float*>(ws);
+    a.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                          round256(sizeof(float) * (size_t)rows * s.nsplit * a.H * a.d));
+  }
+  cudaError_t e = attend_tc_supported(a) ? launch_attend_tc(a, st) : launch_attend_simt(a, st);
+  if (e != cudaSuccess) return status_of(e);
+  return status_of(launch_merge_splits(a, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sa_status_string(int s) {
+  switch (s) {
+    case SA_OK: return "ok";
+    case SA_ERR_INVALID_ARG: return "invalid argument";
+    case SA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case SA_ERR_CUDA: return "CUDA error";
+    case SA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case SA_ERR_BOUNDS: return "index or position out of range";
+    case SA_ERR_NAN: return "NaN score";
+    default: return "unknown status";
+  }
+}
+
+int csa_compress(int dtype, int ik_dtype, int B, int d, int dI, int m, const void* k_raw,
+                 const void* v_raw, const void* ik_raw, const float* z, int R,
+                 const int32_t* blk_lo, const int32_t* blk_hi, int max_blocks, void* k_c,
+                 void* v_c, void* ik_c, void* ik_c_scales, int N_cap, int32_t* err,
+                 void* stream) {
+  if (!plain_dtype(dtype) || B < 0 || d <= 0 || m < 1 || R < m || max_blocks < 0 || N_cap < 0)
+    return SA_ERR_INVALID_ARG;
+  const int vec = 16 / elem_bytes(dtype);
+  if (d % vec) return SA_ERR_UNSUPPORTED;
+  if (!k_raw || !v_raw || !z || !blk_lo || !blk_hi || !k_c || !v_c) return SA_ERR_INVALID_ARG;
+  if (!al16(k_raw) || !al16(v_raw) || !al16(k_c) || !al16(v_c)) return SA_ERR_INVALID_ARG;
+  if (ik_raw) {
+    if (!ik_c || !al16(ik_raw) || !al16(ik_c) || dI <= 0) return SA_ERR_INVALID_ARG;
+    if (ik_dtype == SA_MXFP4) {
+      if (dtype != SA_BF16 || dI % 32 || !ik_c_scales) return SA_ERR_UNSUPPORTED;
+    } else if (ik_dtype != dtype || dI % vec) {
+      return SA_ERR_UNSUPPORTED;
+    }
+  }
+  if (B == 0 || max_blocks == 0) return SA_OK;
+  CompressArgs a{dtype, ik_dtype, B, d, dI, m, k_raw, v_raw, ik_raw, z, R, blk_lo, blk_hi,
+                 max_blocks, k_c, v_c, ik_c, ik_c_scales, N_cap, err};
+  return status_of(launch_compress(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t csa_index_topk_workspace_bytes(int B, int T, int N_cap, int k) {
+  (void)k;
+  if (B <= 0 || T <= 0 || N_cap <= 0) return 0;
+  return round256(sizeof(float) * (size_t)B * T * N_cap);
+}
+
+int csa_index_topk(int q_dtype, int B, int T, int HI, int dI, int m, int k, const void* q_idx,
+                   const void* q_scales, const float* w, const void* ik_c,
+                   const void* ik_scales, int N_cap, const int32_t* q_pos, int32_t* idx,
+                   float* scores_out, const float* scores_in, void* ws, size_t ws_bytes,
+                   int32_t* err, void* stream) {
+  if (B < 0 || T < 0 || m < 1 || k < 0 || N_cap < 0 || !q_pos || (k > 0 && !idx))
+    return SA_ERR_INVALID_ARG;
+  if (!topk_supported(N_cap)) return SA_ERR_UNSUPPORTED;
+  const int64_t rows = (int64_t)B * T;
+  if (rows == 0 || k == 0) return SA_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float* sc = scores_in;
+  if (!scores_in) {
+    if (q_dtype != SA_F32 && q_dtype != SA_BF16 && q_dtype != SA_MXFP4) return SA_ERR_INVALID_ARG;
+    if (HI <= 0 || dI <= 0 || !q_idx || !w || !ik_c) return SA_ERR_INVALID_ARG;
+    if (!al16(q_idx) || !al16(w) || !al16(ik_c)) return SA_ERR_INVALID_ARG;
+    float* dst = scores_out;
+    if (!dst) {
+      if (!ws || ws_bytes < csa_index_topk_workspace_bytes(B, T, N_cap, k) || !al16(ws))
+        return SA_ERR_INVALID_ARG;
+      dst = static_cast<float*>(ws);
+    }
+    ScoreArgs sa_{q_dtype, B, T, HI, dI, m, q_idx, q_scales, w, ik_c, ik_scales, N_cap,
+                  q_pos, dst, (int64_t)N_cap, err};
+    cudaError_t e;
+    if (q_dtype == SA_MXFP4) {
+      return SA_ERR_UNSUPPORTED;
+    } else if (score_tc_supported(sa_)) {
+      e = launch_score_tc(sa_, device_sms(), st);
+    } else {
+      if ((size_t)HI * dI + HI > 12 * 1024) return SA_ERR_UNSUPPORTED;
+      e = launch_score_simt(sa_, st);
+    }
+    if (e != cudaSuccess) return status_of(e);
+    sc = dst;
+  }
+  TopkArgs ta{sc, (int64_t)N_cap, q_pos, (int)rows, m, N_cap, k, idx, err};
+  return status_of(launch_topk(ta, device_sms(), st));
+}
+
+size_t csa_attend_workspace_bytes(int dtype, int B, int T, int H, int d, int k, int W) {
+  (void)dtype;
+  const int64_t rows = (int64_t)B * T;
+  if (rows <= 0 || H <= 0 || d <= 0) return 0;
+  return split_bytes(rows, H, d, choose_split(rows, attn_tiles(k, W)));
+}
+
+int csa_attend(int dtype, int B, int T, int H, int d, int m, int k, int W, float sm_scale,
+               const void* q, const int32_t* q_pos, const void* k_c, const void* v_c,
+               int N_cap, const int32_t* idx, const void* k_raw, const void* v_raw, int R,
+               float* o, float* lse, void* ws, size_t ws_bytes, int32_t* err, void* stream) {
+  if (!plain_dtype(dtype) || B < 0 || T < 0 || H <= 0 || d <= 0 || d > 256 || m < 1 || k < 0 ||
+      W < 0 || N_cap < 0 || R < W || R < 1)
+    return SA_ERR_INVALID_ARG;
+  if (!q || !q_pos || !o || !lse || !k_raw || !v_raw || (k > 0 && (!idx || !k_c || !v_c)))
+    return SA_ERR_INVALID_ARG;
+  if (!al16(q) || !al16(o) || !al16(k_raw) || !al16(v_raw) || (k_c && !al16(k_c)) ||
+      (v_c && !al16(v_c)))
+    return SA_ERR_INVALID_ARG;
+  if ((size_t)H * d > 16384) return SA_ERR_UNSUPPORTED;
+  if ((int64_t)B * T == 0) return SA_OK;
+  AttnArgs a{};
+  a.dtype = dtype; a.B = B; a.T = T; a.H = H; a.d = d; a.sm_scale = sm_scale;
+  a.q = q; a.q_pos = q_pos; a.kc = k_c; a.vc = v_c; a.N_cap = N_cap; a.idx = idx;
+  a.k = k; a.m = m; a.kr = k_raw; a.vr = v_raw; a.R = R; a.W = W; a.o = o; a.lse = lse;
+  a.err = err;
+  a.gather = 1;
+  return run_attention(a, ws, ws_bytes, attn_tiles(k, W), static_cast<cudaStream_t>(stream));
+}
+
+size_t hca_compress_attend_workspace_bytes(int dtype, int B, int T, int H, int d, int N2_cap,
+                                           int W) {
+  (void)dtype;
+  const int64_t rows = (int64_t)B * T;
+  if (rows <= 0 || H <= 0 || d <= 0) return 0;
+  return split_bytes(rows, H, d, choose_split(rows, attn_tiles(N2_cap, W)));
+}
+
+int hca_compress_attend(int dtype, int B, int T, int H, int d, int m2, int W, float sm_scale,
+                        const void* q, const int32_t* q_pos, const void* k_raw,
+                        const void* v_raw, const float* z_hca, int R, const int32_t* blk_lo,
+                        const int32_t* blk_hi, int max_blocks, void* hk_c, void* hv_c,
+                        int N2_cap, float* o, float* lse, void* ws, size_t ws_bytes,
+                        int32_t* err, void* stream) {
+  if (!plain_dtype(dtype) || B < 0 || T < 0 || H <= 0 || d <= 0 || d > 256 || m2 < 1 || W < 0 ||
+      N2_cap < 0 || R < W || R < 1 || max_blocks < 0)
+    return SA_ERR_INVALID_ARG;
+  if (!q || !q_pos || !o || !lse || !k_raw || !v_raw || (N2_cap > 0 && (!hk_c || !hv_c)))
+    return SA_ERR_INVALID_ARG;
+  if (!al16(q) || !al16(o) || !al16(k_raw) || !al16(v_raw) || (hk_c && !al16(hk_c)) ||
+      (hv_c && !al16(hv_c)))
+    return SA_ERR_INVALID_ARG;
+  if ((size_t)H * d > 16384) return SA_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (max_blocks > 0 && B > 0) {
+    if (!z_hca || !blk_lo || !blk_hi || R < m2) return SA_ERR_INVALID_ARG;
+    const int vec = 16 / elem_bytes(dtype);
+    if (d % vec) return SA_ERR_UNSUPPORTED;
+    CompressArgs c{dtype, dtype, B, d, 0, m2, k_raw, v_raw, nullptr, z_hca, R, blk_lo, blk_hi,
+                   max_blocks, hk_c, hv_c, nullptr, nullptr, N2_cap, err};
+    const int s = status_of(launch_compress(c, st));
+    if (s != SA_OK) return s;
+  }
+  if ((int64_t)B * T == 0) return SA_OK;
+  AttnArgs a{};
+  a.dtype = dtype; a.B = B; a.T = T; a.H = H; a.d = d; a.sm_scale = sm_scale;
+  a.q = q; a.q_pos = q_pos; a.kc = hk_c; a.vc = hv_c; a.N_cap = N2_cap; a.idx = nullptr;
+  a.gather = 0;
+  a.k = 0; a.m = m2; a.kr = k_raw; a.vr = v_raw; a.R = R; a.W = W; a.o = o; a.lse = lse;
+  a.err = err;
+  return run_attention(a, ws, ws_bytes, attn_tiles(N2_cap, W), st);
+}
+
+int attn_merge(int n, const float* const* o_parts, const float* const* lse_parts, int64_t rows,
+               int d, void* o, int o_dtype, float* lse, int32_t* err, void* stream) {
+  (void)err;
+  if (n < 1 || n > 8 || rows < 0 || d <= 0 || !o_parts || !lse_parts || !o || !lse ||
+      !plain_dtype(o_dtype))
+    return SA_ERR_INVALID_ARG;
+  MergeArgs a{};
+  a.n = n;
+  for (int i = 0; i < n; ++i) {
+    if (!o_parts[i] || !lse_parts[i]) return SA_ERR_INVALID_ARG;
+    a.o_parts[i] = o_parts[i];
+    a.lse_parts[i] = lse_parts[i];
+  }
+  a.rows = rows; a.d = d; a.o = o; a.o_dtype = o_dtype; a.lse = lse;
+  return status_of(launch_merge(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,186 @@
+// Block compression (CSA with m = 4, HCA with m' = 128): softmax pooling of m
+// consecutive raw rows into one cache row.
+//
+// Source: "오픈소스 LLM의 새 이정표: DeepSeek-V4 시리즈", section
+// "압축 희소 어텐션(CSA)과 극압축 어텐션(HCA)" (m consecutive KV entries merged
+// into one; HCA with m' >> m), and "DeepSeek-V4 논문 읽기: 백만 토큰 컨텍스트를
+// 저렴하게", section "Compressed Sparse Attention (CSA)" step 1.  The pooling
+// rule (softmax over one logit per raw token) is the reading taken where the
+// pages give none.
+//
+// One CTA per (sequence, block).  The CTA first turns the block's m logits
+// into weights in shared memory, then every thread owns one 16-byte chunk of
+// an output row (8 bf16 or 4 f32 channels of K, V or the indexer key) and
+// accumulates the m weighted raw chunks in fp32.  Memory-bound: each raw byte
+// is read once, each output byte written once.
+#include "kernels.cuh"
+
+namespace sa {
+
+constexpr int kCompressThreads = 128;
+
+// Nearest e2m1 magnitude code for |v| (v already divided by the block
+// scale), ties to the even code, saturating at 6 (OCP MX v1.0 FP4 E2M1 grid
+// 0, 0.5, 1, 1.5, 2, 3, 4, 6).
+__device__ __forceinline__ uint32_t e2m1_code(float av) {
+  if (av <= 0.25f) return 0;
+  if (av < 0.75f) return 1;
+  if (av <= 1.25f) return 2;
+  if (av < 1.75f) return 3;
+  if (av <= 2.5f) return 4;
+  if (av < 3.5f) return 5;
+  if (av <= 5.0f) return 6;
+  return 7;
+}
+
+// Quantise one 32-element block held one element per lane (MXFP4, OCP MX
+// v1.0): scale exponent e = floor(log2(amax)) - 2 clamped to [-127, 127]
+// (all-zero block: -127); element code = nearest e2m1 of x / 2^e; a negative
+// element whose magnitude rounds to zero is stored as +0.  Lane 0 writes the
+// scale byte, even lanes write one code byte each (low nibble = even element).
+__device__ __forceinline__ void mxfp4_quantize_warp(float x, uint8_t* codes16, uint8_t* scale) {
+  const int lane = threadIdx.x & 31;
+  float amax = fabsf(x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  int e = (amax > 0.f) ? ilogbf(amax) - 2 : -127;
+  e = max(-127, min(127, e));
+  float v = ldexpf(x, -e);
+  uint32_t mag = e2m1_code(fabsf(v));
+  uint32_t nib = (v < 0.f && mag != 0) ? (8u | mag) : mag;
+  uint32_t hi = __shfl_down_sync(0xffffffffu, nib, 1);
+  if ((lane & 1) == 0) codes16[lane >> 1] = static_cast<uint8_t>(nib | (hi << 4));
+  if (lane == 0) *scale = static_cast<uint8_t>(e + 127);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressArgs a) {
+  using S = Store<DT>;
+  constexpr int kVec = 16 / S::kBytes;               // channels per 16-byte chunk
+  extern __shared__ float s_w[];                     // [m] pooling weights
+  const int b = blockIdx.y;
+  const int lo = __ldg(a.blk_lo + b), hi = __ldg(a.blk_hi + b);
+  const int64_t j = (int64_t)lo + blockIdx.x;
+  if (j >= hi) return;
+  if (hi - lo > a.max_blocks || j < 0 || j >= a.N_cap) {
+    if (threadIdx.x == 0) set_err(a.err, SA_ERR_BOUNDS);
+    return;
+  }
+  const int m = a.m, R = a.R;
+  const int64_t p0 = j * m;
+  // ---- pooling weights: softmax of the block's logits
+  for (int i = threadIdx.x; i < m; i += blockDim.x)
+    s_w[i] = __ldg(a.z + (int64_t)b * R + (p0 + i) % R);
+  __syncthreads();
+  __shared__ float s_mu, s_sum;
+  if (threadIdx.x < 32) {
+    float mu = -INFINITY;
+    for (int i = threadIdx.x; i < m; i += 32) mu = fmaxf(mu, s_w[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, o));
+    float sum = 0.f;
+    for (int i = threadIdx.x; i < m; i += 32) sum += expf(s_w[i] - mu);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (threadIdx.x == 0) { s_mu = mu; s_sum = sum; }
+  }
+  __syncthreads();
+  const float mu = s_mu, inv = 1.f / s_sum;
+  for (int i = threadIdx.x; i < m; i += blockDim.x) s_w[i] = expf(s_w[i] - mu) * inv;
+  __syncthreads();
+
+  // ---- weighted sums, one 16-byte output chunk per thread
+  const int ckv = a.d / kVec;                         // chunks per K or V row
+  const bool ik_plain = a.ik_raw != nullptr && a.ik_dtype != SA_MXFP4;
+  const int cik = ik_plain ? a.dI / kVec : 0;
+  const int nchunks = 2 * ckv + cik;
+  for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {
+    const void* src;
+    void* dst;
+    int width, off;
+    if (c < ckv) { src = a.k_raw; dst = a.k_c; width = a.d; off = c * kVec; }
+    else if (c < 2 * ckv) { src = a.v_raw; dst = a.v_c; width = a.d; off = (c - ckv) * kVec; }
+    else { src = a.ik_raw; dst = a.ik_c; width = a.dI; off = (c - 2 * ckv) * kVec; }
+    float acc[kVec];
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) acc[e] = 0.f;
+    const char* base = static_cast<const char*>(src) + (int64_t)b * R * width * S::kBytes;
+    for (int i = 0; i < m; ++i) {
+      const int64_t slot = (p0 + i) % R;
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(base + (slot * width + off) * S::kBytes));
+      float f[kVec];
+      if constexpr (DT == SA_BF16) {
+        bf16x8_to_f32(u, f);
+      } else {
+        f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+      }
+      const float wi = s_w[i];
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) acc[e] = fmaf(wi, f[e], acc[e]);
+    }
+    char* out = static_cast<char*>(dst) + (((int64_t)b * a.N_cap + j) * width + off) * S::kBytes;
+    if constexpr (DT == SA_BF16) {
+      uint32_t w4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+        w4[e] = *reinterpret_cast<uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint4*>(out) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    } else {
+      *reinterpret_cast<float4*>(out) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    }
+  }
+
+  // ---- indexer key stored as MXFP4: one warp per 32-element block
+  if (a.ik_raw != nullptr && a.ik_dtype == SA_MXFP4) {
+    const int nblk32 = a.dI / 32;
+    for (int q = warp_id(); q < nblk32; q += blockDim.x / 32) {
+      const int ch = q * 32 + lane_id();
+      float acc = 0.f;
+      for (int i = 0; i < m; ++i) {
+        const int64_t slot = (p0 + i) % R;
+        acc = fmaf(s_w[i], Store<SA_BF16>::ld(a.ik_raw, ((int64_t)b * R + slot) * a.dI + ch), acc);
+      }
+      const float rounded = __bfloat162float(__float2bfloat16_rn(acc));
+      uint8_t* codes = static_cast<uint8_t*>(a.ik_c) + ((int64_t)b * a.N_cap + j) * (a.dI / 2) + q * 16;
+      uint8_t* sc = static_cast<uint8_t*>(a.ik_c_scales) + ((int64_t)b * a.N_cap + j) * nblk32 + q;
+      mxfp4_quantize_warp(rounded, codes, sc);
+    }
+  }
+}
+
+// Stand-alone MXFP4 quantiser for rows of bf16 values (the indexer queries
+// and the indexer key cache): one warp per 32-element block.
+__global__ void mxfp4_quantize_kernel(const __nv_bfloat16* x, int64_t nblk, uint8_t* codes,
+                                      uint8_t* scales) {
+  const int64_t blk = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (blk >= nblk) return;
+  const float v = __bfloat162float(x[blk * 32 + lane_id()]);
+  mxfp4_quantize_warp(v, codes + blk * 16, scales + blk);
+}
+
+cudaError_t launch_compress(const CompressArgs& a, cudaStream_t st) {
+  if (a.max_blocks <= 0) return cudaSuccess;
+  dim3 grid(a.max_blocks, a.B);
+  size_t smem = sizeof(float) * a.m;
+  if (a.dtype == SA_BF16)
+    compress_kernel<SA_BF16><<<grid, kCompressThreads, smem, st>>>(a);
+  else
+    compress_kernel<SA_F32><<<grid, kCompressThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mxfp4_quantize(const void* x_bf16, int64_t nblk, void* codes, void* scales,
+                                  cudaStream_t st) {
+  if (nblk <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (nblk * 32 + threads - 1) / threads;
+  mxfp4_quantize_kernel<<<(unsigned)blocks, threads, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(x_bf16), nblk, static_cast<uint8_t*>(codes),
+      static_cast<uint8_t*>(scales));
+  return cudaGetLastError();
+}
+
+}  // namespace sa

@@ -1,0 +1,103 @@
+// Argument blocks and launchers of the libsa27 kernels (internal header).
+#pragma once
+#include "common.cuh"
+
+namespace sa {
+
+struct CompressArgs {
+  int dtype, ik_dtype, B, d, dI, m;
+  const void* k_raw;
+  const void* v_raw;
+  const void* ik_raw;
+  const float* z;
+  int R;
+  const int32_t* blk_lo;
+  const int32_t* blk_hi;
+  int max_blocks;
+  void* k_c;
+  void* v_c;
+  void* ik_c;
+  void* ik_c_scales;
+  int N_cap;
+  int32_t* err;
+};
+cudaError_t launch_compress(const CompressArgs& a, cudaStream_t st);
+cudaError_t launch_mxfp4_quantize(const void* x_bf16, int64_t nblk, void* codes, void* scales,
+                                  cudaStream_t st);
+
+// Indexer scoring: scores[r*ld + j] for j < n(r) = min(N_cap, (q_pos[r]+1)/m).
+struct ScoreArgs {
+  int dtype, B, T, HI, dI, m;
+  const void* q;        // [B*T, HI, dI] (MXFP4: codes [.., dI/2])
+  const void* q_scales; // MXFP4 only: [B*T, HI, dI/32]
+  const float* w;       // [B*T, HI]
+  const void* ik;       // [B, N_cap, dI] (MXFP4: codes)
+  const void* ik_scales;
+  int N_cap;
+  const int32_t* q_pos;
+  float* scores;
+  int64_t ld;
+  int32_t* err;
+};
+cudaError_t launch_score_simt(const ScoreArgs& a, cudaStream_t st);
+cudaError_t launch_score_tc(const ScoreArgs& a, int num_sms, cudaStream_t st);
+bool score_tc_supported(const ScoreArgs& a);
+
+// Per-row top-k over scores (see csa_index_topk).
+struct TopkArgs {
+  const float* scores;
+  int64_t ld;
+  const int32_t* q_pos;
+  int rows, m, N_cap, k;
+  int32_t* idx;
+  int32_t* err;
+};
+cudaError_t launch_topk(const TopkArgs& a, int num_sms, cudaStream_t st);
+bool topk_supported(int N_cap);
+
+// Attention over (compressed part) + (window part) per query row.
+//  Compressed part: gathered (gather = 1: idx slots [0, min(k, n)), n = (p+1)/m,
+//  entries -1 skipped) or dense (gather = 0: rows [0, n)).
+//  Window part: raw positions p-Wn+1 .. p in ring rows (u mod R).
+struct AttnArgs {
+  int dtype, B, T, H, d;
+  float sm_scale;
+  const void* q;        // [B*T, H, d]
+  const int32_t* q_pos;
+  const void* kc;       // [B, N_cap, d]
+  const void* vc;
+  int N_cap;
+  const int32_t* idx;   // [B*T, k] when gather
+  int gather;           // 1: CSA (idx slots), 0: dense compressed rows (HCA)
+  int k, m;
+  const void* kr;       // [B, R, d]
+  const void* vr;
+  int R, W;
+  float* o;             // [B*T, H, d]
+  float* lse;           // [B*T, H]
+  int nsplit;           // key-tile splits per row (1: write o/lse directly)
+  int split_tiles;      // key tiles (of kAttnTile keys) per split
+  float* part_o;        // [B*T, nsplit, H, d] when nsplit > 1
+  float* part_lse;      // [B*T, nsplit, H]
+  int32_t* err;
+};
+constexpr int kAttnTile = 128;
+cudaError_t launch_attend_simt(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_attend_tc(const AttnArgs& a, cudaStream_t st);
+bool attend_tc_supported(const AttnArgs& a);
+// Merge nsplit partials per (row, head) into o/lse.
+cudaError_t launch_merge_splits(const AttnArgs& a, cudaStream_t st);
+
+struct MergeArgs {
+  int n;
+  const float* o_parts[8];
+  const float* lse_parts[8];
+  int64_t rows;
+  int d;
+  void* o;
+  int o_dtype;
+  float* lse;
+};
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t st);
+
+}  // namespace sa

@@ -1,0 +1,330 @@
+// Lightning-indexer scores on the 5th-generation tensor cores (bf16 inputs,
+// fp32 accumulation in TMEM, fp32 ReLU-weighted head sum in the epilogue):
+//     s[r, j] = sum_h w[r,h] * max(0, q_I[r,h,:] . Ik_c[b,j,:]),  j < n(r)
+// Source: "EP 95. DeepSeek-V4 논문 읽기 — 노정석", section IDEAS (lightning indexer
+// over the compressed cache) and "DeepSeek-V4 논문 읽기: 백만 토큰 컨텍스트를
+// 저렴하게", section "Compressed Sparse Attention (CSA)" step 2.  The weighted ReLU
+// head sum is the reading taken where the pages give no formula.
+//
+// The contraction is D[j, (q,h)] = Ik_c[j,:] . q_I[q,h,:] with M = 128 cache
+// entries (A, streamed by TMA), N = QG*64 (the 64 indexer heads of QG queries;
+// B, resident per query group) and K = 64.  Putting the heads on N keeps the
+// head sum inside one TMEM lane: epilogue thread j reads its row of D and
+// folds w and ReLU in fp32 -- no cross-thread reduction and no rounding of w
+// into bf16 operands.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and
+// TMEM owner, warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
+// A ring of shared-memory stages holds the streamed Ik_c tiles; two TMEM
+// accumulators let the epilogue of tile i overlap the MMA of tile i+1.
+// Persistent grid: CTA c takes jobs c, c+G, ...; a job is (query group,
+// chunk of entry tiles), tiles past the group's causal limit are never loaded.
+// Every wait is bounded; on a timeout the CTA records SA_ERR_DEVICE_TIMEOUT,
+// drops its remaining work and still frees its TMEM.
+#include <cudaTypedefs.h>
+
+#include "kernels.cuh"
+
+namespace sa {
+
+constexpr int kScoreTcThreads = 192;
+constexpr int kTileEntries = 128;
+constexpr int kDI = 64;
+constexpr int kHI = 64;
+
+template <int QG>
+struct ScoreTcCfg {
+  static constexpr int kStages = QG == 1 ? 8 : 6;
+  static constexpr int kAccCols = QG * kHI;
+  static constexpr int kTmemCols = 2 * kAccCols;              // 128 or 512
+  static constexpr int kABytes = kTileEntries * kDI * 2;      // 16 KB
+  static constexpr int kBBytes = QG * kHI * kDI * 2;          // 8 KB per query
+  static constexpr size_t kSmem = 1024 /*align slack*/ + kStages * kABytes + 2 * kBBytes + 256;
+};
+
+struct ScoreTcParams {
+  const float* w;
+  const int32_t* q_pos;
+  int B, T, m, N_cap;
+  int chunk_tiles, max_chunks;
+  int64_t njobs;
+  float* scores;
+  int64_t ld;
+  int32_t* err;
+};
+
+template <int QG>
+struct JobInfo {
+  int b, t0, nq, t_lo, t_hi;
+  int64_t g;
+};
+
+template <int QG>
+__device__ __forceinline__ JobInfo<QG> job_info(const ScoreTcParams& p, int64_t job) {
+  JobInfo<QG> J;
+  J.g = job / p.max_chunks;
+  const int c = (int)(job % p.max_chunks);
+  const int gpb = (p.T + QG - 1) / QG;
+  J.b = (int)(J.g / gpb);
+  J.t0 = (int)(J.g % gpb) * QG;
+  J.nq = min(QG, p.T - J.t0);
+  int64_t nmax = 0;
+  for (int q = 0; q < J.nq; ++q) {
+    const int pos = __ldg(p.q_pos + (int64_t)J.b * p.T + J.t0 + q);
+    int64_t n = pos < 0 ? 0 : ((int64_t)pos + 1) / p.m;
+    nmax = max64(nmax, min64(n, p.N_cap));
+  }
+  const int ntiles = (int)((nmax + kTileEntries - 1) / kTileEntries);
+  J.t_lo = c * p.chunk_tiles;
+  J.t_hi = min(ntiles, J.t_lo + p.chunk_tiles);
+  return J;
+}
+
+template <int QG>
+__global__ void __launch_bounds__(kScoreTcThreads, 1)
+    score_tc_kernel(const __grid_constant__ CUtensorMap tm_ik,
+                    const __grid_constant__ CUtensorMap tm_q, ScoreTcParams p) {
+  using Cfg = ScoreTcCfg<QG>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sA = smem;
+  unsigned char* sB = sA + Cfg::kStages * Cfg::kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + 2 * Cfg::kBBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = full + Cfg::kStages;
+  uint64_t* bfull = empty + Cfg::kStages;
+  uint64_t* bempty = bfull + 2;
+  uint64_t* tfull = bempty + 2;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+
+  const int warp = (int)warp_id(), lane = (int)lane_id();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bfull[s], 1);
+      mbar_init(&bempty[s], 1);
+      mbar_init(&tfull[s], 1);
+      mbar_init(&tempty[s], 128);
+    }
+    *s_abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_ik);
+    tma_prefetch_desc(&tm_q);
+  }
+  if (warp == 1) tmem_alloc(s_tmem, Cfg::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t ph = 0;
+      int nsw = 0;
+      int64_t prev_g = -1;
+      for (int64_t job = blockIdx.x; job < p.njobs && !*s_abort; job += gridDim.x) {
+        const JobInfo<QG> J = job_info<QG>(p, job);
+        if (J.t_lo >= J.t_hi) continue;
+        if (J.g != prev_g) {
+          const int slot = nsw & 1, u = nsw >> 1;
+          if (!mbar_wait(&bempty[slot], (u & 1) ^ 1, p.err)) { *s_abort = 1; break; }
+          mbar_arrive_expect_tx(&bfull[slot], Cfg::kBBytes);
+          tma_load_2d(&tm_q, &bfull[slot], sB + slot * Cfg::kBBytes, 0,
+                      (int32_t)(((int64_t)J.b * p.T + J.t0) * kHI));
+          prev_g = J.g;
+          ++nsw;
+        }
+        for (int t = J.t_lo; t < J.t_hi; ++t) {
+          if (!mbar_wait(&empty[stage], ph ^ 1, p.err)) { *s_abort = 1; break; }
+          mbar_arrive_expect_tx(&full[stage], Cfg::kABytes);
+          tma_load_2d(&tm_ik, &full[stage], sA + stage * Cfg::kABytes, 0,
+                      (int32_t)((int64_t)J.b * p.N_cap + (int64_t)t * kTileEntries));
+          if (++stage == Cfg::kStages) { stage = 0; ph ^= 1; }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(128, Cfg::kAccCols);
+      int stage = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      int nsw = 0, slot = -1;
+      int64_t prev_g = -1;
+      for (int64_t job = blockIdx.x; job < p.njobs && !*s_abort; job += gridDim.x) {
+        const JobInfo<QG> J = job_info<QG>(p, job);
+        if (J.t_lo >= J.t_hi) continue;
+        if (J.g != prev_g) {
+          if (slot >= 0) tc_commit(&bempty[slot]);
+          slot = nsw & 1;
+          const int u = nsw >> 1;
+          if (!mbar_wait(&bfull[slot], u & 1, p.err)) { *s_abort = 1; break; }
+          prev_g = J.g;
+          ++nsw;
+        }
+        const uint32_t b_base = smem_u32(sB + slot * Cfg::kBBytes);
+        for (int t = J.t_lo; t < J.t_hi; ++t) {
+          if (!mbar_wait(&full[stage], ph, p.err)) { *s_abort = 1; break; }
+          if (!mbar_wait(&tempty[acc], acc_ph ^ 1, p.err)) { *s_abort = 1; break; }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * Cfg::kABytes);
+#pragma unroll
+          for (int kk = 0; kk < kDI / 16; ++kk)
+            tc_mma_f16(tmem + acc * Cfg::kAccCols, sdesc_kmajor_sw128(a_base + kk * 32),
+                       sdesc_kmajor_sw128(b_base + kk * 32), idesc, kk > 0 ? 1u : 0u);
+          tc_commit(&empty[stage]);
+          tc_commit(&tfull[acc]);
+          if (++stage == Cfg::kStages) { stage = 0; ph ^= 1; }
+          acc ^= 1;
+          if (acc == 0) acc_ph ^= 1;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int row_in_tile = quad * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    for (int64_t job = blockIdx.x; job < p.njobs && !*s_abort; job += gridDim.x) {
+      const JobInfo<QG> J = job_info<QG>(p, job);
+      if (J.t_lo >= J.t_hi) continue;
+      int64_t nq_vis[QG];
+#pragma unroll
+      for (int q = 0; q < QG; ++q) {
+        nq_vis[q] = 0;
+        if (q < J.nq) {
+          const int pos = __ldg(p.q_pos + (int64_t)J.b * p.T + J.t0 + q);
+          const int64_t n = pos < 0 ? 0 : ((int64_t)pos + 1) / p.m;
+          nq_vis[q] = min64(n, p.N_cap);
+        }
+      }
+      bool stop = false;
+      for (int t = J.t_lo; t < J.t_hi; ++t) {
+        if (!mbar_wait(&tfull[acc], acc_ph, p.err)) { *s_abort = 1; stop = true; break; }
+        tc_fence_after();
+        const int64_t j = (int64_t)t * kTileEntries + row_in_tile;
+#pragma unroll 1
+        for (int q = 0; q < J.nq; ++q) {
+          const int64_t r = (int64_t)J.b * p.T + J.t0 + q;
+          const float4* w4 = reinterpret_cast<const float4*>(p.w + r * kHI);
+          float s = 0.f;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float v[32];
+            tmem_ld32(tmem + lane_base + acc * Cfg::kAccCols + q * kHI + half * 32, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 ww = __ldg(w4 + half * 8 + i);
+              s = fmaf(ww.x, fmaxf(v[4 * i + 0], 0.f), s);
+              s = fmaf(ww.y, fmaxf(v[4 * i + 1], 0.f), s);
+              s = fmaf(ww.z, fmaxf(v[4 * i + 2], 0.f), s);
+              s = fmaf(ww.w, fmaxf(v[4 * i + 3], 0.f), s);
+            }
+          }
+          if (j < nq_vis[q]) p.scores[r * p.ld + j] = s;
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_ph ^= 1;
+      }
+      if (stop) break;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, 64] (128-byte rows) with a {64, box_rows} box and the
+// 128-byte swizzle expected by the K-major shared-memory descriptors.
+bool make_tmap_bf16_rows64(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {64, rows};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool score_tc_supported(const ScoreArgs& a) {
+  return a.dtype == SA_BF16 && a.HI == kHI && a.dI == kDI;
+}
+
+template <int QG>
+static cudaError_t launch_qg(const ScoreArgs& a, int num_sms, cudaStream_t st) {
+  using Cfg = ScoreTcCfg<QG>;
+  CUtensorMap tm_ik, tm_q;
+  if (!make_tmap_bf16_rows64(&tm_ik, a.ik, (uint64_t)a.B * a.N_cap, kTileEntries) ||
+      !make_tmap_bf16_rows64(&tm_q, a.q, (uint64_t)a.B * a.T * kHI, QG * kHI))
+    return cudaErrorInvalidValue;
+  ScoreTcParams p;
+  p.w = a.w;
+  p.q_pos = a.q_pos;
+  p.B = a.B;
+  p.T = a.T;
+  p.m = a.m;
+  p.N_cap = a.N_cap;
+  p.scores = a.scores;
+  p.ld = a.ld;
+  p.err = a.err;
+  const int64_t ngroups = (int64_t)a.B * ((a.T + QG - 1) / QG);
+  const int ntiles_max = (a.N_cap + kTileEntries - 1) / kTileEntries;
+  if (ngroups == 0 || ntiles_max == 0) return cudaSuccess;
+  // chunk so that there are >= ~16 jobs per CTA
+  int64_t ct = (ngroups * ntiles_max) / (16LL * num_sms);
+  if (ct < 1) ct = 1;
+  if (ct > ntiles_max) ct = ntiles_max;
+  p.chunk_tiles = (int)ct;
+  p.max_chunks = (int)((ntiles_max + ct - 1) / ct);
+  p.njobs = ngroups * p.max_chunks;
+  const int grid = (int)min64(num_sms, p.njobs);
+  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<QG>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)Cfg::kSmem);
+  if (e != cudaSuccess) return e;
+  score_tc_kernel<QG><<<grid, kScoreTcThreads, Cfg::kSmem, st>>>(tm_ik, tm_q, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_score_tc(const ScoreArgs& a, int num_sms, cudaStream_t st) {
+  if (a.T >= 4) return launch_qg<4>(a, num_sms, st);
+  return launch_qg<1>(a, num_sms, st);
+}
+
+}  // namespace sa

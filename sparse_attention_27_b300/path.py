@@ -1,0 +1,138 @@
+"""One pass of the hybrid compressed attention hot path through the C ABI.
+
+``HybridStep`` owns the output buffers and scratch of one decode step (or
+prefill chunk) and issues, in order, the library calls of the two layer
+kinds:
+
+  CSA layer:  csa_compress -> csa_index_topk -> csa_attend
+  HCA layer:  hca_compress_attend
+
+(CSA and HCA are different layers, interleaved in the model -- "오픈소스 LLM의
+새 이정표: DeepSeek-V4 시리즈", section "기존의 벽을 허문 아키텍처: 하이브리드 압축
+어텐션" -- so their outputs are not merged with each other; each layer has its
+own caches and sliding window.)  torch is used only to allocate device memory
+and to provide streams; all arithmetic runs in libsa27's kernels.
+
+Tensor names (device tensors, layouts row-major):
+  q, q_hca [B,T,H,d]; q_idx [B,T,HI,dI] (MXFP4: q_idx codes + q_idx_scales);
+  w_idx [B,T,HI] f32; q_pos [B,T] int32;
+  k_raw, v_raw [B,R,d]; ik_raw [B,R,dI]; z [B,R] f32 (CSA layer ring);
+  hk_raw, hv_raw [B,R,d]; hz [B,R] f32 (HCA layer ring);
+  k_c, v_c [B,ncap,d]; ik_c [B,ncap,dI] (MXFP4: ik_c codes + ik_c_scales);
+  hk_c, hv_c [B,ncap2,d];
+  blk_lo, blk_hi, hblk_lo, hblk_hi [B] int32 (blocks compressed this pass).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import (SA_BF16, SA_F32, SA_MXFP4, csa_attend, csa_attend_workspace_bytes, csa_compress,
+               csa_index_topk, csa_index_topk_workspace_bytes, hca_compress_attend,
+               hca_compress_attend_workspace_bytes)
+
+_CODES = {"f32": SA_F32, "bf16": SA_BF16, "mxfp4": SA_MXFP4}
+
+
+@dataclass
+class Dims:
+    B: int
+    T: int
+    H: int
+    d: int
+    HI: int
+    dI: int
+    m: int
+    k: int
+    W: int
+    m2: int
+    R: int
+    ncap: int
+    ncap2: int
+    dtype: str          # "bf16" or "f32" (K/V/q storage)
+    indexer: str        # "bf16", "f32" or "mxfp4"
+    sm_scale: float
+    max_blocks: int     # bound on CSA blocks compressed per sequence this pass
+    max_blocks2: int    # bound on HCA blocks compressed per sequence this pass
+
+
+class HybridStep:
+    def __init__(self, dims: Dims, x: dict, device="cuda"):
+        self.D, self.x = dims, x
+        D = dims
+        rows = D.B * D.T
+        dev = torch.device(device)
+        self.idx = torch.empty((D.B, D.T, D.k), dtype=torch.int32, device=dev)
+        self.o = torch.empty((D.B, D.T, D.H, D.d), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((D.B, D.T, D.H), dtype=torch.float32, device=dev)
+        self.ho = torch.empty_like(self.o)
+        self.hlse = torch.empty_like(self.lse)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        dt = _CODES[D.dtype]
+        self.ws_index = csa_index_topk_workspace_bytes(D.B, D.T, D.ncap, D.k)
+        self.ws_attend = csa_attend_workspace_bytes(dt, D.B, D.T, D.H, D.d, D.k, D.W)
+        self.ws_hca = hca_compress_attend_workspace_bytes(dt, D.B, D.T, D.H, D.d, D.ncap2, D.W)
+        self.ws_a = torch.empty(max(self.ws_index, 256), dtype=torch.uint8, device=dev)
+        self.ws_b = torch.empty(max(self.ws_attend, 256), dtype=torch.uint8, device=dev)
+        self.ws_c = torch.empty(max(self.ws_hca, 256), dtype=torch.uint8, device=dev)
+        self.scores = None
+        assert rows > 0
+
+    # -------------------------------------------------------------- layers
+    def compress_csa(self, stream=None):
+        D, x = self.D, self.x
+        csa_compress(_CODES[D.dtype], _CODES[D.indexer], D.B, D.d, D.dI, D.m, x["k_raw"],
+                     x["v_raw"], x["ik_raw"], x["z"], D.R, x["blk_lo"], x["blk_hi"], D.max_blocks,
+                     x["k_c"], x["v_c"], x["ik_c"], x.get("ik_c_scales"), D.ncap, err=self.err,
+                     stream=stream)
+
+    def index_topk(self, stream=None, scores_out=None, scores_in=None):
+        D, x = self.D, self.x
+        csa_index_topk(_CODES[D.indexer], D.B, D.T, D.HI, D.dI, D.m, D.k, x["q_idx"],
+                       x.get("q_idx_scales"), x["w_idx"], x["ik_c"], x.get("ik_c_scales"), D.ncap,
+                       x["q_pos"], self.idx, scores_out=scores_out, scores_in=scores_in,
+                       ws=self.ws_a, ws_bytes=self.ws_a.numel(), err=self.err, stream=stream)
+
+    def attend_csa(self, stream=None, idx=None):
+        D, x = self.D, self.x
+        csa_attend(_CODES[D.dtype], D.B, D.T, D.H, D.d, D.m, D.k, D.W, D.sm_scale, x["q"],
+                   x["q_pos"], x["k_c"], x["v_c"], D.ncap, self.idx if idx is None else idx,
+                   x["k_raw"], x["v_raw"], D.R, self.o, self.lse, ws=self.ws_b,
+                   ws_bytes=self.ws_b.numel(), err=self.err, stream=stream)
+
+    def hca(self, stream=None):
+        D, x = self.D, self.x
+        hca_compress_attend(_CODES[D.dtype], D.B, D.T, D.H, D.d, D.m2, D.W, D.sm_scale, x["q_hca"],
+                            x["q_pos"], x["hk_raw"], x["hv_raw"], x["hz"], D.R, x["hblk_lo"],
+                            x["hblk_hi"], D.max_blocks2, x["hk_c"], x["hv_c"], D.ncap2, self.ho,
+                            self.hlse, ws=self.ws_c, ws_bytes=self.ws_c.numel(), err=self.err,
+                            stream=stream)
+
+    def csa(self, stream=None):
+        self.compress_csa(stream)
+        self.index_topk(stream)
+        self.attend_csa(stream)
+
+    def run(self, stream=None):
+        """The whole pass on one stream."""
+        self.csa(stream)
+        self.hca(stream)
+
+    def run_two_streams(self, s_csa: torch.cuda.Stream, s_hca: torch.cuda.Stream):
+        """The CSA and HCA layers on two streams (they share no buffer)."""
+        cur = torch.cuda.current_stream()
+        ev = torch.cuda.Event()
+        ev.record(cur)
+        s_csa.wait_event(ev)
+        s_hca.wait_event(ev)
+        self.csa(s_csa)
+        self.hca(s_hca)
+        e1, e2 = torch.cuda.Event(), torch.cuda.Event()
+        e1.record(s_csa)
+        e2.record(s_hca)
+        cur.wait_event(e1)
+        cur.wait_event(e2)
+
+    def device_errors(self) -> int:
+        return int(self.err.item())

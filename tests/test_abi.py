@@ -1,0 +1,54 @@
+"""CPU-side checks of the C ABI: the library loads, exports every entry point
+that include/sa.h declares, and rejects bad arguments on the host before any
+CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "sa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                                 src, flags=re.M)))
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for n in ("csa_compress", "csa_index_topk", "csa_attend", "hca_compress_attend", "attn_merge"):
+        assert n in names, names
+
+
+def test_library_exports_every_declared_symbol():
+    import sparse_attention_27_b300 as m
+    lib = ctypes.CDLL(m.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert set(declared_functions()) == set(m.EXPORTS)
+
+
+def test_status_strings_and_host_validation():
+    import sparse_attention_27_b300 as m
+    assert m.status_string(0) == "ok"
+    assert "range" in m.status_string(m.SA_ERR_BOUNDS)
+    # bad dtype / null pointers / R < W: rejected before any CUDA call
+    with pytest.raises(m.SaError) as e:
+        m.csa_compress(9, 9, 1, 128, 64, 4, None, None, None, None, 128, None, None, 1, None,
+                       None, None, None, 10, stream=0)
+    assert e.value.status == m.SA_ERR_INVALID_ARG
+    with pytest.raises(m.SaError) as e:
+        m.csa_attend(m.SA_BF16, 1, 1, 64, 128, 4, 8, 16, 0.1, None, None, None, None, 4, None,
+                     None, None, 8, None, None, stream=0)
+    assert e.value.status == m.SA_ERR_INVALID_ARG
+    assert m.library().attn_merge(0, None, None, 1, 1, None, 0, None, None, None) == \
+        m.SA_ERR_INVALID_ARG
+
+
+def test_workspace_queries_are_host_only():
+    import sparse_attention_27_b300 as m
+    assert m.csa_index_topk_workspace_bytes(32, 1, 32768, 2048) == 32 * 32768 * 4
+    assert m.csa_index_topk_workspace_bytes(0, 1, 10, 1) == 0
