@@ -1,0 +1,307 @@
+"""Benchmark: CSA + HCA decode query-tokens/s at 128K context on B300.
+
+One step = one decode token for each of the 32 sequences through one CSA
+layer (compress the block the token closes, indexer scores, top-k 2048,
+sparse attention over the selected rows + a 128-token window) and one HCA
+layer (compress the closing 128-token block, dense attention over all 1024
+HCA rows + the window), on synthetic seeded inputs of the 128K decode shape.
+The two layers run on two streams (they share no data) inside one captured
+CUDA graph.  L2 is flushed (a 512 MiB write) before every timed step, outside
+the timed interval; each step is timed with CUDA events on the launching
+stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  Multi-GPU (torchrun): every rank runs its own batch of
+32 sequences (weak scaling, no data-path collective); time = max over ranks.
+``--impl reference`` times the float64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA+HCA decode query-tokens/s at 128K and 1M ctx; HBM GB/s vs peak"
+UNIT = "query-tokens/s"
+WORKLOAD = "decode128k"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+def algorithmic_bytes(w) -> dict:
+    """Minimum bytes one decode step must move (each needed row read once)."""
+    e = 2  # bf16
+    per_seq_index = w.ncap * w.dI * e + w.HI * w.dI * e + w.HI * 4
+    per_seq_csa = (per_seq_index + w.k * 2 * w.d * e + w.W * 2 * w.d * e + w.H * w.d * e
+                   + w.k * 4 + w.H * w.d * 4 + w.H * 4)
+    per_seq_hca = (w.ncap2 * 2 * w.d * e + w.W * 2 * w.d * e + w.H * w.d * e
+                   + w.H * w.d * 4 + w.H * 4)
+    return dict(index=per_seq_index * w.B, step=(per_seq_csa + per_seq_hca) * w.B)
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        import torch
+        try:
+            u = str(torch.cuda.get_device_properties(device).uuid)
+            self.id = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            self.id = str(device)
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.id}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        if self.p:
+            self.p.terminate()
+            try:
+                out, _ = self.p.communicate(timeout=5)
+            except Exception:
+                self.p.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        else:
+            self.lines = []
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+                for n, v in zip(names, f[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w, x, seqs: int) -> dict:
+    """The float64 oracle, as it stands, on ``seqs`` sequences of the same step."""
+    import numpy as np
+    import oracle
+    import synth
+    sub = synth.Workload(w.name, w.mode, B=seqs, L=w.L, T=w.T, R=w.R, k=w.k, x8=w.x8)
+    xs = {k: (v[:seqs] if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == w.B else v)
+          for k, v in x.items()}
+    t0 = time.perf_counter()
+    oracle.reference(sub, xs)
+    dt = time.perf_counter() - t0
+    return {"value": seqs * sub.T / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{seqs} of {w.B} sequences of one {w.name} step (full CSA+HCA path, "
+                      f"float64, OpenMP over query rows), {dt:.2f} s"}
+
+
+def run_reference(args) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    x = synth.make_inputs(w)
+    seqs = 4
+    for _ in range(args.warmup):
+        cpu_baseline(w, x, seqs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cpu_baseline(w, x, seqs)
+    dt = time.perf_counter() - t0
+    v = seqs * args.steps / dt
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sequences_per_step": seqs},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{seqs} of {w.B} sequences per step"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    assert args.warmup >= 3
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from gpu_util import dev, make_step
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    w = synth.WORKLOADS[WORKLOAD]
+    x = synth.make_inputs(w)
+    step = make_step(w, x)
+    launches = step.kernel_launches()
+    s_csa, s_hca = torch.cuda.Stream(), torch.cuda.Stream()
+    main_s = torch.cuda.current_stream()
+    # warm-up outside the graph (sets kernel attributes, loads modules)
+    for _ in range(2):
+        step.run_two_streams(s_csa, s_hca)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=cap):
+        step.run_two_streams(s_csa, s_hca)
+    torch.cuda.synchronize()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a, b in evs:
+            flush.zero_()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        ms = timed(g.replay, args.steps)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    total_ms = sum(ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    errs = step.device_errors()
+    value = world * w.B * w.T * args.steps / (total_ms / 1e3)
+
+    # ---- dominant kernel: indexer scoring alone (csa_index_topk with k = 0)
+    import sparse_attention_27_b300 as sa
+    D = step.D
+    sc = torch.empty((w.B, w.T, w.ncap), dtype=torch.float32, device="cuda")
+
+    def score_only():
+        sa.csa_index_topk(sa.SA_BF16, D.B, D.T, D.HI, D.dI, D.m, 0, step.x["q_idx"], None,
+                          step.x["w_idx"], step.x["ik_c"], None, D.ncap, step.x["q_pos"], None,
+                          scores_out=sc)
+    for _ in range(3):
+        score_only()
+    k_ms = timed(score_only, args.steps)
+    k_avg = sum(k_ms) / len(k_ms)
+    ab = algorithmic_bytes(w)
+    peak, peak_kind = peaks()
+    achieved = ab["index"] / (k_avg / 1e3) / 1e9
+    step_gbs = ab["step"] / (total_ms / args.steps / 1e3) / 1e9
+
+    # ---- end to end: host (pinned) inputs of the new token in, outputs out
+    e2e = None
+    if rank == 0 or world > 1:
+        new_names = ["q", "q_hca", "q_idx", "w_idx", "q_pos"]
+        host_in = {n: torch.from_numpy(np.ascontiguousarray(x[n]).view(
+            np.int16 if x[n].dtype == np.uint16 else x[n].dtype)).pin_memory() for n in new_names}
+        # the new token's raw rows (ring slot t mod R) of every ring
+        slot = (w.L - 1) % w.ring
+        ring_names = ["k_raw", "v_raw", "ik_raw", "z", "hk_raw", "hv_raw", "hz"]
+        host_ring = {n: torch.from_numpy(np.ascontiguousarray(x[n][:, slot]).view(
+            np.int16 if x[n].dtype == np.uint16 else x[n].dtype)).pin_memory() for n in ring_names}
+        outs = [step.o, step.lse, step.ho, step.hlse]
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + \
+            sum(t.numel() * t.element_size() for t in host_ring.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs)
+
+        def e2e_step():
+            for n, t in host_in.items():
+                step.x[n].view(t.dtype).copy_(t, non_blocking=True)
+            for n, t in host_ring.items():
+                step.x[n][:, slot].view(t.dtype).copy_(t, non_blocking=True)
+            g.replay()
+            for hd, dv in zip(host_out, outs):
+                hd.copy_(dv, non_blocking=True)
+        for _ in range(3):
+            e2e_step()
+        e_ms = timed(e2e_step, args.steps)
+        e2e = {"value": world * w.B * w.T * args.steps / (sum(e_ms) / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, x, seqs=w.B)
+
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": w.B, "context": w.L, "heads": w.H,
+                       "head_dim": w.d, "m": w.m, "top_k": w.k, "window": w.W, "m2": w.m2,
+                       "indexer_heads": w.HI, "parallelism": f"replicas x{world}",
+                       "l2": "flushed (512 MiB write) before every timed step",
+                       "graph": "one CUDA graph per step, CSA and HCA on two streams"},
+            "step_algorithmic_bytes": ab["step"], "step_gbs": step_gbs,
+            "step_frac_of_hbm": step_gbs / peak,
+            "roofline": {"kernel": "score_tc_kernel (csa_index_topk scores, k=0)",
+                         "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "traffic": None, "avg_launch_ms": k_avg,
+                         "algorithmic_bytes_per_launch": ab["index"]},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * args.steps,
+            "device_errors": errs, "clocks": clk.summary(),
+        }), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -115,10 +115,13 @@ int csa_compress(int dtype, int ik_dtype, int B, int d, int dI, int m, const voi
  *  scores_out  optional [B,T,N_cap] f32: receives s (entries j >= n untouched)
  *  scores_in   optional [B,T,N_cap] f32: if given, scoring is skipped and the
  *              top-k selects from these values (same n per row)
- * Supported: dI = 64 and HI in {1..64} multiple of ... (see sa_status);
- * bf16 / MXFP4 with HI = 64 run on the tensor cores; f32 on CUDA cores.
- * N_cap <= 786432.  Device errors: NaN score -> SA_ERR_NAN (row written as
- * all -1); n > N_cap -> SA_ERR_BOUNDS (n clamped).
+ *  k = 0 with scores_out given computes the scores only (idx untouched).
+ *  ws          scratch of csa_index_topk_workspace_bytes() bytes when
+ *              scores_out and scores_in are both NULL (holds the scores)
+ * Kernels: bf16 with HI = 64, dI = 64 scores on the tensor cores (tcgen05);
+ * other f32/bf16 shapes (HI*dI <= 12K) on CUDA cores.  N_cap <= 393216.
+ * Device errors: NaN score -> SA_ERR_NAN (row written as all -1);
+ * n > N_cap -> SA_ERR_BOUNDS (n clamped).
  */
 int csa_index_topk(int q_dtype, int B, int T, int HI, int dI, int m, int k, const void* q_idx,
                    const void* q_scales, const float* w, const void* ik_c,

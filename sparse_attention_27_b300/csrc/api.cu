@@ -41,7 +41,8 @@ struct Split {
 Split choose_split(int64_t rows, int max_tiles) {
   Split s{1, max_tiles > 0 ? max_tiles : 1};
   if (rows <= 0 || max_tiles <= 1) return s;
-  const int64_t want = (2LL * device_sms() + rows - 1) / rows;   // CTAs per row
+  // one resident CTA per SM: at most one wave of row splits
+  const int64_t want = std::max<int64_t>(1, device_sms() / rows);
   int ns = (int)std::min<int64_t>(want, max_tiles);
   if (ns < 1) ns = 1;
   s.split_tiles = (max_tiles + ns - 1) / ns;
@@ -101,7 +102,8 @@ int csa_compress(int dtype, int ik_dtype, int B, int d, int dI, int m, const voi
   if (!plain_dtype(dtype) || B < 0 || d <= 0 || m < 1 || R < m || max_blocks < 0 || N_cap < 0)
     return SA_ERR_INVALID_ARG;
   const int vec = 16 / elem_bytes(dtype);
-  if (d % vec) return SA_ERR_UNSUPPORTED;
+  if (d % vec || 2 * d / vec + (ik_raw && ik_dtype != SA_MXFP4 ? dI / vec : 0) > 256)
+    return SA_ERR_UNSUPPORTED;
   if (!k_raw || !v_raw || !z || !blk_lo || !blk_hi || !k_c || !v_c) return SA_ERR_INVALID_ARG;
   if (!al16(k_raw) || !al16(v_raw) || !al16(k_c) || !al16(v_c)) return SA_ERR_INVALID_ARG;
   if (ik_raw) {
@@ -133,7 +135,7 @@ int csa_index_topk(int q_dtype, int B, int T, int HI, int dI, int m, int k, cons
     return SA_ERR_INVALID_ARG;
   if (!topk_supported(N_cap)) return SA_ERR_UNSUPPORTED;
   const int64_t rows = (int64_t)B * T;
-  if (rows == 0 || k == 0) return SA_OK;
+  if (rows == 0 || (k == 0 && (scores_in || !scores_out))) return SA_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const float* sc = scores_in;
   if (!scores_in) {
@@ -160,6 +162,7 @@ int csa_index_topk(int q_dtype, int B, int T, int HI, int dI, int m, int k, cons
     if (e != cudaSuccess) return status_of(e);
     sc = dst;
   }
+  if (k == 0) return SA_OK;   // scores only
   TopkArgs ta{sc, (int64_t)N_cap, q_pos, (int)rows, m, N_cap, k, idx, err};
   return status_of(launch_topk(ta, device_sms(), st));
 }
@@ -221,7 +224,7 @@ int hca_compress_attend(int dtype, int B, int T, int H, int d, int m2, int W, fl
   if (max_blocks > 0 && B > 0) {
     if (!z_hca || !blk_lo || !blk_hi || R < m2) return SA_ERR_INVALID_ARG;
     const int vec = 16 / elem_bytes(dtype);
-    if (d % vec) return SA_ERR_UNSUPPORTED;
+    if (d % vec || 2 * d / vec > 256) return SA_ERR_UNSUPPORTED;
     CompressArgs c{dtype, dtype, B, d, 0, m2, k_raw, v_raw, nullptr, z_hca, R, blk_lo, blk_hi,
                    max_blocks, hk_c, hv_c, nullptr, nullptr, N2_cap, err};
     const int s = status_of(launch_compress(c, st));

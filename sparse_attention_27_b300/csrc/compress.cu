@@ -9,15 +9,17 @@
 // pages give none.
 //
 // One CTA per (sequence, block).  The CTA first turns the block's m logits
-// into weights in shared memory, then every thread owns one 16-byte chunk of
-// an output row (8 bf16 or 4 f32 channels of K, V or the indexer key) and
-// accumulates the m weighted raw chunks in fp32.  Memory-bound: each raw byte
-// is read once, each output byte written once.
+// into weights in shared memory.  Each output row is cut into 16-byte chunks
+// (8 bf16 or 4 f32 channels of K, V or the indexer key); a thread owns one
+// chunk and one group of rows (all m rows for m = 4, m/8 rows for m' = 128),
+// accumulates in fp32 with 16-byte loads, and the row groups are added in
+// shared memory.  Memory-bound: each raw byte is read once, each output byte
+// written once.
 #include "kernels.cuh"
 
 namespace sa {
 
-constexpr int kCompressThreads = 128;
+constexpr int kCompressThreads = 256;
 
 // Nearest e2m1 magnitude code for |v| (v already divided by the block
 // scale), ties to the even code, saturating at 6 (OCP MX v1.0 FP4 E2M1 grid
@@ -89,23 +91,30 @@ __global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressArgs
   for (int i = threadIdx.x; i < m; i += blockDim.x) s_w[i] = expf(s_w[i] - mu) * inv;
   __syncthreads();
 
-  // ---- weighted sums, one 16-byte output chunk per thread
+  // ---- weighted sums.  Thread (chunk c, row group g) accumulates rows
+  // i = g, g+RG, ... of one 16-byte output chunk; the RG partial sums are then
+  // added in shared memory in a fixed order.
   const int ckv = a.d / kVec;                         // chunks per K or V row
   const bool ik_plain = a.ik_raw != nullptr && a.ik_dtype != SA_MXFP4;
   const int cik = ik_plain ? a.dI / kVec : 0;
   const int nchunks = 2 * ckv + cik;
-  for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {
-    const void* src;
-    void* dst;
-    int width, off;
-    if (c < ckv) { src = a.k_raw; dst = a.k_c; width = a.d; off = c * kVec; }
-    else if (c < 2 * ckv) { src = a.v_raw; dst = a.v_c; width = a.d; off = (c - ckv) * kVec; }
-    else { src = a.ik_raw; dst = a.ik_c; width = a.dI; off = (c - 2 * ckv) * kVec; }
+  int RG = 1;
+  while (RG * 2 <= m && RG * 2 * nchunks <= (int)blockDim.x) RG *= 2;
+  float* s_part = s_w + m;                            // [RG][nchunks][kVec]
+  const int c = threadIdx.x % nchunks, g = threadIdx.x / nchunks;
+  const void* src = nullptr;
+  void* dst = nullptr;
+  int width = 0, off = 0;
+  if (c < ckv) { src = a.k_raw; dst = a.k_c; width = a.d; off = c * kVec; }
+  else if (c < 2 * ckv) { src = a.v_raw; dst = a.v_c; width = a.d; off = (c - ckv) * kVec; }
+  else { src = a.ik_raw; dst = a.ik_c; width = a.dI; off = (c - 2 * ckv) * kVec; }
+  if (g < RG && nchunks > 0) {
     float acc[kVec];
 #pragma unroll
     for (int e = 0; e < kVec; ++e) acc[e] = 0.f;
     const char* base = static_cast<const char*>(src) + (int64_t)b * R * width * S::kBytes;
-    for (int i = 0; i < m; ++i) {
+#pragma unroll 4
+    for (int i = g; i < m; i += RG) {
       const int64_t slot = (p0 + i) % R;
       const uint4 u = __ldg(reinterpret_cast<const uint4*>(base + (slot * width + off) * S::kBytes));
       float f[kVec];
@@ -119,6 +128,17 @@ __global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressArgs
 #pragma unroll
       for (int e = 0; e < kVec; ++e) acc[e] = fmaf(wi, f[e], acc[e]);
     }
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) s_part[(g * nchunks + c) * kVec + e] = acc[e];
+  }
+  __syncthreads();
+  if (g == 0 && nchunks > 0) {
+    float acc[kVec];
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) acc[e] = s_part[c * kVec + e];
+    for (int q = 1; q < RG; ++q)
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) acc[e] += s_part[(q * nchunks + c) * kVec + e];
     char* out = static_cast<char*>(dst) + (((int64_t)b * a.N_cap + j) * width + off) * S::kBytes;
     if constexpr (DT == SA_BF16) {
       uint32_t w4[4];
@@ -164,7 +184,8 @@ __global__ void mxfp4_quantize_kernel(const __nv_bfloat16* x, int64_t nblk, uint
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t st) {
   if (a.max_blocks <= 0) return cudaSuccess;
   dim3 grid(a.max_blocks, a.B);
-  size_t smem = sizeof(float) * a.m;
+  // weights [m] + partial sums [RG <= 256/nchunks][nchunks][4 or 8 floats]
+  size_t smem = sizeof(float) * (a.m + 2 * kCompressThreads * 8);
   if (a.dtype == SA_BF16)
     compress_kernel<SA_BF16><<<grid, kCompressThreads, smem, st>>>(a);
   else

@@ -81,7 +81,7 @@ struct AttnArgs {
   float* part_lse;      // [B*T, nsplit, H]
   int32_t* err;
 };
-constexpr int kAttnTile = 128;
+constexpr int kAttnTile = 64;     // keys per attention tile (split granularity)
 cudaError_t launch_attend_simt(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_attend_tc(const AttnArgs& a, cudaStream_t st);
 bool attend_tc_supported(const AttnArgs& a);

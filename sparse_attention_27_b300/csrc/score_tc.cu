@@ -32,14 +32,24 @@ constexpr int kTileEntries = 128;
 constexpr int kDI = 64;
 constexpr int kHI = 64;
 
+constexpr int kMaxJobsPerCta = 256;
+
+template <int QG>
+struct JobRec {
+  int b, t0, nq, t_lo, t_hi, g;
+  int n[QG];            // visible entries of each query of the group
+};
+
 template <int QG>
 struct ScoreTcCfg {
   static constexpr int kStages = QG == 1 ? 8 : 6;
   static constexpr int kAccCols = QG * kHI;
-  static constexpr int kTmemCols = 2 * kAccCols;              // 128 or 512
+  static constexpr int kAccBufs = QG == 1 ? 4 : 2;
+  static constexpr int kTmemCols = kAccBufs * kAccCols;       // 256 or 512
   static constexpr int kABytes = kTileEntries * kDI * 2;      // 16 KB
   static constexpr int kBBytes = QG * kHI * kDI * 2;          // 8 KB per query
-  static constexpr size_t kSmem = 1024 /*align slack*/ + kStages * kABytes + 2 * kBBytes + 256;
+  static constexpr size_t kSmem = 1024 /*align slack*/ + kStages * kABytes + 2 * kBBytes + 512 +
+                                  kMaxJobsPerCta * sizeof(JobRec<QG>);
 };
 
 struct ScoreTcParams {
@@ -54,25 +64,25 @@ struct ScoreTcParams {
 };
 
 template <int QG>
-struct JobInfo {
-  int b, t0, nq, t_lo, t_hi;
-  int64_t g;
-};
-
-template <int QG>
-__device__ __forceinline__ JobInfo<QG> job_info(const ScoreTcParams& p, int64_t job) {
-  JobInfo<QG> J;
-  J.g = job / p.max_chunks;
+__device__ __forceinline__ JobRec<QG> make_job(const ScoreTcParams& p, int64_t job) {
+  JobRec<QG> J;
+  const int64_t g = job / p.max_chunks;
   const int c = (int)(job % p.max_chunks);
   const int gpb = (p.T + QG - 1) / QG;
-  J.b = (int)(J.g / gpb);
-  J.t0 = (int)(J.g % gpb) * QG;
+  J.g = (int)g;
+  J.b = (int)(g / gpb);
+  J.t0 = (int)(g % gpb) * QG;
   J.nq = min(QG, p.T - J.t0);
   int64_t nmax = 0;
-  for (int q = 0; q < J.nq; ++q) {
-    const int pos = __ldg(p.q_pos + (int64_t)J.b * p.T + J.t0 + q);
-    int64_t n = pos < 0 ? 0 : ((int64_t)pos + 1) / p.m;
-    nmax = max64(nmax, min64(n, p.N_cap));
+#pragma unroll
+  for (int q = 0; q < QG; ++q) {
+    int64_t n = 0;
+    if (q < J.nq) {
+      const int pos = __ldg(p.q_pos + (int64_t)J.b * p.T + J.t0 + q);
+      n = pos < 0 ? 0 : min64(((int64_t)pos + 1) / p.m, p.N_cap);
+    }
+    J.n[q] = (int)n;
+    nmax = max64(nmax, n);
   }
   const int ntiles = (int)((nmax + kTileEntries - 1) / kTileEntries);
   J.t_lo = c * p.chunk_tiles;
@@ -96,9 +106,14 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
   uint64_t* bfull = empty + Cfg::kStages;
   uint64_t* bempty = bfull + 2;
   uint64_t* tfull = bempty + 2;
-  uint64_t* tempty = tfull + 2;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* tempty = tfull + Cfg::kAccBufs;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + Cfg::kAccBufs);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  JobRec<QG>* jobs = reinterpret_cast<JobRec<QG>*>(
+      reinterpret_cast<unsigned char*>(bars) + 512);
+  const int n_my = (int)((p.njobs - blockIdx.x + gridDim.x - 1) / gridDim.x);
+  for (int i = threadIdx.x; i < n_my; i += blockDim.x)
+    jobs[i] = make_job<QG>(p, blockIdx.x + (int64_t)i * gridDim.x);
 
   const int warp = (int)warp_id(), lane = (int)lane_id();
   if (threadIdx.x == 0) {
@@ -106,6 +121,8 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bfull[s], 1);
       mbar_init(&bempty[s], 1);
+    }
+    for (int s = 0; s < Cfg::kAccBufs; ++s) {
       mbar_init(&tfull[s], 1);
       mbar_init(&tempty[s], 128);
     }
@@ -129,8 +146,8 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
       uint32_t ph = 0;
       int nsw = 0;
       int64_t prev_g = -1;
-      for (int64_t job = blockIdx.x; job < p.njobs && !*s_abort; job += gridDim.x) {
-        const JobInfo<QG> J = job_info<QG>(p, job);
+      for (int ji = 0; ji < n_my && !*s_abort; ++ji) {
+        const JobRec<QG>& J = jobs[ji];
         if (J.t_lo >= J.t_hi) continue;
         if (J.g != prev_g) {
           const int slot = nsw & 1, u = nsw >> 1;
@@ -161,8 +178,8 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
       uint32_t acc_ph = 0;
       int nsw = 0, slot = -1;
       int64_t prev_g = -1;
-      for (int64_t job = blockIdx.x; job < p.njobs && !*s_abort; job += gridDim.x) {
-        const JobInfo<QG> J = job_info<QG>(p, job);
+      for (int ji = 0; ji < n_my && !*s_abort; ++ji) {
+        const JobRec<QG>& J = jobs[ji];
         if (J.t_lo >= J.t_hi) continue;
         if (J.g != prev_g) {
           if (slot >= 0) tc_commit(&bempty[slot]);
@@ -185,8 +202,7 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
           tc_commit(&empty[stage]);
           tc_commit(&tfull[acc]);
           if (++stage == Cfg::kStages) { stage = 0; ph ^= 1; }
-          acc ^= 1;
-          if (acc == 0) acc_ph ^= 1;
+          if (++acc == Cfg::kAccBufs) { acc = 0; acc_ph ^= 1; }
         }
       }
     }
@@ -198,19 +214,9 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     int acc = 0;
     uint32_t acc_ph = 0;
-    for (int64_t job = blockIdx.x; job < p.njobs && !*s_abort; job += gridDim.x) {
-      const JobInfo<QG> J = job_info<QG>(p, job);
+    for (int ji = 0; ji < n_my && !*s_abort; ++ji) {
+      const JobRec<QG>& J = jobs[ji];
       if (J.t_lo >= J.t_hi) continue;
-      int64_t nq_vis[QG];
-#pragma unroll
-      for (int q = 0; q < QG; ++q) {
-        nq_vis[q] = 0;
-        if (q < J.nq) {
-          const int pos = __ldg(p.q_pos + (int64_t)J.b * p.T + J.t0 + q);
-          const int64_t n = pos < 0 ? 0 : ((int64_t)pos + 1) / p.m;
-          nq_vis[q] = min64(n, p.N_cap);
-        }
-      }
       bool stop = false;
       for (int t = J.t_lo; t < J.t_hi; ++t) {
         if (!mbar_wait(&tfull[acc], acc_ph, p.err)) { *s_abort = 1; stop = true; break; }
@@ -220,26 +226,26 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
         for (int q = 0; q < J.nq; ++q) {
           const int64_t r = (int64_t)J.b * p.T + J.t0 + q;
           const float4* w4 = reinterpret_cast<const float4*>(p.w + r * kHI);
-          float s = 0.f;
+          float4 wv[16];
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float v[32];
-            tmem_ld32(tmem + lane_base + acc * Cfg::kAccCols + q * kHI + half * 32, v);
+          for (int i = 0; i < 16; ++i) wv[i] = __ldg(w4 + i);
+          uint32_t v[64];
+          tmem_ld32_async(tmem + lane_base + acc * Cfg::kAccCols + q * kHI, v);
+          tmem_ld32_async(tmem + lane_base + acc * Cfg::kAccCols + q * kHI + 32, v + 32);
+          tmem_wait_ld();
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 ww = __ldg(w4 + half * 8 + i);
-              s = fmaf(ww.x, fmaxf(v[4 * i + 0], 0.f), s);
-              s = fmaf(ww.y, fmaxf(v[4 * i + 1], 0.f), s);
-              s = fmaf(ww.z, fmaxf(v[4 * i + 2], 0.f), s);
-              s = fmaf(ww.w, fmaxf(v[4 * i + 3], 0.f), s);
-            }
+          for (int i = 0; i < 16; ++i) {
+            s0 = fmaf(wv[i].x, fmaxf(__uint_as_float(v[4 * i + 0]), 0.f), s0);
+            s1 = fmaf(wv[i].y, fmaxf(__uint_as_float(v[4 * i + 1]), 0.f), s1);
+            s2 = fmaf(wv[i].z, fmaxf(__uint_as_float(v[4 * i + 2]), 0.f), s2);
+            s3 = fmaf(wv[i].w, fmaxf(__uint_as_float(v[4 * i + 3]), 0.f), s3);
           }
-          if (j < nq_vis[q]) p.scores[r * p.ld + j] = s;
+          if (j < J.n[q]) p.scores[r * p.ld + j] = (s0 + s1) + (s2 + s3);
         }
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_ph ^= 1;
+        if (++acc == Cfg::kAccBufs) { acc = 0; acc_ph ^= 1; }
       }
       if (stop) break;
     }
@@ -306,10 +312,17 @@ static cudaError_t launch_qg(const ScoreArgs& a, int num_sms, cudaStream_t st) {
   const int64_t ngroups = (int64_t)a.B * ((a.T + QG - 1) / QG);
   const int ntiles_max = (a.N_cap + kTileEntries - 1) / kTileEntries;
   if (ngroups == 0 || ntiles_max == 0) return cudaSuccess;
-  // chunk so that there are >= ~16 jobs per CTA
+  // chunk so that there are ~16 jobs per CTA, and never more jobs than a
+  // CTA's job table holds
   int64_t ct = (ngroups * ntiles_max) / (16LL * num_sms);
   if (ct < 1) ct = 1;
   if (ct > ntiles_max) ct = ntiles_max;
+  while (ct < ntiles_max &&
+         ngroups * ((ntiles_max + ct - 1) / ct) > (int64_t)kMaxJobsPerCta * num_sms)
+    ct *= 2;
+  if (ct > ntiles_max) ct = ntiles_max;
+  if (ngroups * ((ntiles_max + ct - 1) / ct) > (int64_t)kMaxJobsPerCta * num_sms)
+    return cudaErrorInvalidValue;
   p.chunk_tiles = (int)ct;
   p.max_chunks = (int)((ntiles_max + ct - 1) / ct);
   p.njobs = ngroups * p.max_chunks;
