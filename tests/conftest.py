@@ -11,9 +11,23 @@ if HERE not in sys.path:
     sys.path.insert(0, HERE)
 
 
+def _ensure_built():
+    """Compile libsa27.so (nvcc cross-compiles without a GPU) and the oracle's
+    C code when they are missing or older than their sources."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "sa27_build", os.path.join(ROOT, "sparse_attention_27_b300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+    import oracle
+    oracle.build()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (B300, sm_103a)")
     config.addinivalue_line("markers", "slow: full-size workload")
+    _ensure_built()
 
 
 def pytest_collection_modifyitems(config, items):
