@@ -22,7 +22,6 @@ import argparse
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -43,6 +42,38 @@ def peaks():
         return 6400.0, "fallback"
 
 
+# Sources of the dominant kernel; the ncu DRAM traffic recorded in
+# profiles/traffic.txt is reported only while these files hash to the value
+# recorded with it (a changed kernel has no valid traffic figure).
+SCORE_SOURCES = ["sparse_attention_27_b300/csrc/score_tc.cu", "sparse_attention_27_b300/csrc/common.cuh",
+                 "sparse_attention_27_b300/csrc/kernels.cuh"]
+
+
+def source_hash(files) -> str:
+    import hashlib
+    h = hashlib.sha1()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, files):
+    """(bytes per launch, capture note) from profiles/traffic.txt, or (None, why)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    cur = source_hash(files)
+    try:
+        for line in open(path):
+            f = line.split()
+            if len(f) >= 3 and not line.startswith("#") and f[0] == kernel:
+                if f[1] == cur:
+                    return int(f[2]), " ".join(f[3:])
+                return None, "kernel changed since the ncu capture"
+    except OSError:
+        pass
+    return None, "no ncu capture recorded"
+
+
 def algorithmic_bytes(w) -> dict:
     """Minimum bytes one decode step must move (each needed row read once)."""
     e = 2  # bf16
@@ -55,56 +86,59 @@ def algorithmic_bytes(w) -> dict:
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons sampled through NVML every ~2 ms by a
+    background thread while the timed region runs."""
 
     def __init__(self, device: int):
         import torch
+        self.samples = []
+        self.max_mhz = None
+        self.h = None
         try:
+            import pynvml
+            pynvml.nvmlInit()
             u = str(torch.cuda.get_device_properties(device).uuid)
-            self.id = u if u.startswith("GPU-") else "GPU-" + u
+            u = u if u.startswith("GPU-") else "GPU-" + u
+            self.h = pynvml.nvmlDeviceGetHandleByUUID(u.encode())
+            self.nv = pynvml
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
         except Exception:
-            self.id = str(device)
-        self.p = None
+            self.h = None
+
+    def _loop(self):
+        nv = self.nv
+        names = {"hw_slowdown": nv.nvmlClocksEventReasonHwSlowdown,
+                 "hw_thermal_slowdown": nv.nvmlClocksEventReasonHwThermalSlowdown,
+                 "sw_thermal_slowdown": nv.nvmlClocksEventReasonSwThermalSlowdown,
+                 "sw_power_cap": nv.nvmlClocksEventReasonSwPowerCap}
+        while not self.stop.is_set():
+            try:
+                mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append((mhz, [n for n, bit in names.items() if r & bit]))
+            except Exception:
+                pass
+            self.stop.wait(0.002)
 
     def __enter__(self):
-        try:
-            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.id}", f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "100"],
-                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except Exception:
-            self.p = None
+        import threading
+        self.stop = threading.Event()
+        self.t = None
+        if self.h is not None:
+            self.t = threading.Thread(target=self._loop, daemon=True)
+            self.t.start()
         return self
 
     def __exit__(self, *a):
-        if self.p:
-            self.p.terminate()
-            try:
-                out, _ = self.p.communicate(timeout=5)
-            except Exception:
-                self.p.kill()
-                out = ""
-            self.lines = [l for l in out.splitlines() if l.strip()]
-        else:
-            self.lines = []
+        self.stop.set()
+        if self.t:
+            self.t.join()
 
     def summary(self) -> dict:
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in self.lines:
-            f = [x.strip() for x in l.split(",")]
-            try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
-                for n, v in zip(names, f[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
-            except (ValueError, IndexError):
-                continue
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        sm = [m for m, _ in self.samples]
+        reasons = sorted({n for _, rs in self.samples for n in rs})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(sm)}
 
 
 def cpu_baseline(w, x, seqs: int) -> dict:
@@ -241,6 +275,7 @@ def main() -> None:
     ab = algorithmic_bytes(w)
     peak, peak_kind = peaks()
     achieved = ab["index"] / (k_avg / 1e3) / 1e9
+    traffic, traffic_note = recorded_traffic("score_tc_kernel", SCORE_SOURCES)
     step_gbs = ab["step"] / (total_ms / args.steps / 1e3) / 1e9
 
     # ---- end to end: host (pinned) inputs of the new token in, outputs out
@@ -294,7 +329,8 @@ def main() -> None:
             "roofline": {"kernel": "score_tc_kernel (csa_index_topk scores, k=0)",
                          "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
-                         "traffic": None, "avg_launch_ms": k_avg,
+                         "traffic": traffic, "traffic_source": traffic_note,
+                         "avg_launch_ms": k_avg,
                          "algorithmic_bytes_per_launch": ab["index"]},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * args.steps,
             "device_errors": errs, "clocks": clk.summary(),
