@@ -131,6 +131,41 @@ int csa_index_topk(int q_dtype, int B, int T, int HI, int dI, int m, int k, cons
 size_t csa_index_topk_workspace_bytes(int B, int T, int N_cap, int k);
 
 /* ---------------------------------------------------------------------------
+ * csa_index_topk_noalloc -- csa_index_topk for callers that cannot give the
+ * library any scratch memory.  The pages have no counterpart to this call;
+ * it is a convenience of this library.
+ *
+ * Who needs it: a caller that owns every byte of device memory and hands a
+ * kernel library only its inputs and outputs -- for example a serving engine
+ * that reserved the whole GPU for its KV-cache pool at start-up, or a plugin
+ * whose host framework forbids side allocations -- and a decode loop that
+ * cannot afford cudaMalloc, which may synchronise the device and takes
+ * unbounded time.
+ *
+ * Same operation, arguments, layouts and device errors as csa_index_topk,
+ * without scores_out, scores_in and the workspace.  q_dtype must be SA_F32 or
+ * SA_BF16.  The scores live in a fixed device array inside the library
+ * (SA_NOALLOC_MAX_SCORES floats, 8 MiB), which every GPU that loads the
+ * library holds until the process exits.  Limit: B * T * N_cap <=
+ * SA_NOALLOC_MAX_SCORES, otherwise SA_ERR_UNSUPPORTED is returned before any
+ * work is enqueued.  Nothing is allocated or freed (no cudaMalloc, cudaFree
+ * or allocating library routine).
+ *
+ * First call on a device: it looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current and caches it; make that
+ * first call before any stream capture.  Calls on the same device share the
+ * one array and it keeps the last call's scores: two calls that overlap on
+ * the GPU (different streams, no ordering between them) race and give wrong
+ * results.  No part of the array needs to start at zero -- every score the
+ * top-k reads is written by the same call first -- so nothing is cleared.
+ */
+#define SA_NOALLOC_MAX_SCORES 2097152
+int csa_index_topk_noalloc(int q_dtype, int B, int T, int HI, int dI, int m, int k,
+                           const void* q_idx, const void* q_scales, const float* w,
+                           const void* ik_c, const void* ik_scales, int N_cap,
+                           const int32_t* q_pos, int32_t* idx, int32_t* err, void* stream);
+
+/* ---------------------------------------------------------------------------
  * csa_attend -- sparse multi-query attention over the selected compressed
  * rows plus the sliding window, in one softmax ([P2]; [P3] CSA steps 3-4).
  * For query row r (sequence b, position p), n = floor((p+1)/m),

@@ -26,7 +26,7 @@ SA_F32, SA_BF16, SA_MXFP4 = 0, 1, 2
 EXPORTS = (
     "sa_status_string", "csa_compress", "csa_index_topk", "csa_index_topk_workspace_bytes",
     "csa_attend", "csa_attend_workspace_bytes", "hca_compress_attend",
-    "hca_compress_attend_workspace_bytes", "attn_merge",
+    "hca_compress_attend_workspace_bytes", "attn_merge", "csa_index_topk_noalloc",
 )
 
 
@@ -50,6 +50,8 @@ _lib.csa_index_topk.argtypes = [_i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, 
                                 _vp, _vp, _vp, _vp, _sz, _vp, _vp]
 _lib.csa_index_topk_workspace_bytes.argtypes = [_i, _i, _i, _i]
 _lib.csa_index_topk_workspace_bytes.restype = _sz
+_lib.csa_index_topk_noalloc.argtypes = [_i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i,
+                                        _vp, _vp, _vp, _vp]
 _lib.csa_attend.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _i, _vp, _vp,
                             _vp, _i, _vp, _vp, _vp, _sz, _vp, _vp]
 _lib.csa_attend_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
@@ -116,6 +118,18 @@ def csa_index_topk(q_dtype, B, T, HI, dI, m, k, q_idx, q_scales, w, ik_c, ik_sca
                                _p(ik_c), _p(ik_scales), N_cap, _p(q_pos), _p(idx),
                                _p(scores_out), _p(scores_in), _p(ws), ws_bytes, _p(err),
                                _stream(stream)), "csa_index_topk")
+
+
+def csa_index_topk_noalloc(q_dtype, B, T, HI, dI, m, k, q_idx, q_scales, w, ik_c, ik_scales,
+                           N_cap, q_pos, idx, err=None, stream=None):
+    """csa_index_topk without a workspace: the scores live in the library's
+    own fixed device array (at most SA_NOALLOC_MAX_SCORES = B*T*N_cap)."""
+    _check(_lib.csa_index_topk_noalloc(q_dtype, B, T, HI, dI, m, k, _p(q_idx), _p(q_scales), _p(w),
+                                       _p(ik_c), _p(ik_scales), N_cap, _p(q_pos), _p(idx), _p(err),
+                                       _stream(stream)), "csa_index_topk_noalloc")
+
+
+NOALLOC_MAX_SCORES = 2097152
 
 
 def csa_attend_workspace_bytes(dtype, B, T, H, d, k, W) -> int:
