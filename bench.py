@@ -86,38 +86,48 @@ def algorithmic_bytes(w) -> dict:
 
 
 class Clocks:
-    """SM clock and clock-event reasons sampled through NVML every ~2 ms by a
-    background thread while the timed region runs."""
+    """SM clock and clock-event reasons sampled every ~2 ms by a background
+    thread while the timed region runs, read through NVML (the driver's
+    libnvidia-ml.so.1, via ctypes; reading only, no setting is changed)."""
+
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40}
 
     def __init__(self, device: int):
+        import ctypes
         import torch
         self.samples = []
         self.max_mhz = None
         self.h = None
+        self.why = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            u = str(torch.cuda.get_device_properties(device).uuid)
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(device)
+            u = str(props.uuid)
             u = u if u.startswith("GPU-") else "GPU-" + u
-            self.h = pynvml.nvmlDeviceGetHandleByUUID(u.encode())
-            self.nv = pynvml
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception:
+            if nv.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) != 0:
+                bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+                if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                    raise RuntimeError("no NVML handle for " + u + " / " + bus)
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self.nv, self.h, self.ct = nv, h, ctypes
+        except Exception as e:  # no NVML: report no samples, and why
             self.h = None
+            self.why = str(e)
 
     def _loop(self):
-        nv = self.nv
-        names = {"hw_slowdown": nv.nvmlClocksEventReasonHwSlowdown,
-                 "hw_thermal_slowdown": nv.nvmlClocksEventReasonHwThermalSlowdown,
-                 "sw_thermal_slowdown": nv.nvmlClocksEventReasonSwThermalSlowdown,
-                 "sw_power_cap": nv.nvmlClocksEventReasonSwPowerCap}
+        ct, nv = self.ct, self.nv
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
         while not self.stop.is_set():
-            try:
-                mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
-                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                self.samples.append((mhz, [n for n, bit in names.items() if r & bit]))
-            except Exception:
-                pass
+            if (nv.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk)) == 0 and
+                    nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ct.byref(rs)) == 0):
+                self.samples.append((float(clk.value),
+                                     [n for n, bit in self.REASONS.items() if rs.value & bit]))
             self.stop.wait(0.002)
 
     def __enter__(self):
@@ -137,8 +147,91 @@ class Clocks:
     def summary(self) -> dict:
         sm = [m for m, _ in self.samples]
         reasons = sorted({n for _, rs in self.samples for n in rs})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+               "reasons": reasons, "samples": len(sm)}
+        if self.why:
+            out["unavailable"] = self.why
+        return out
+
+
+class StepIO:
+    """Host <-> device traffic of one decode step for the end-to-end figure.
+
+    The new token's inputs (q, q_hca, q_I, w, positions) live in one device
+    buffer filled by one copy from one pinned host buffer; its raw rows (ring
+    slot t mod R of the seven per-token arrays of both layers) are written by
+    one strided 2-D copy per array; the step's outputs (O and LSE of both
+    layers) live in one device buffer read back by one copy."""
+
+    IN = ["q", "q_hca", "q_idx", "w_idx", "q_pos"]
+    RING = ["k_raw", "v_raw", "ik_raw", "z", "hk_raw", "hv_raw", "hz"]
+    OUT = ["o", "lse", "ho", "hlse"]
+
+    def __init__(self, step, x, w):
+        import ctypes
+        import numpy as np
+        import torch
+        dev = step.o.device
+
+        def carve(tensors):
+            offs, off = [], 0
+            for t in tensors:
+                offs.append(off)
+                off += (t.numel() * t.element_size() + 255) // 256 * 256
+            buf = torch.empty(off, dtype=torch.uint8, device=dev)
+            views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                     for o, t in zip(offs, tensors)]
+            return buf, views
+
+        ins = [step.x[n] for n in self.IN]
+        self.d_in, views = carve(ins)
+        for n, t, v in zip(self.IN, ins, views):
+            v.copy_(t)
+            step.x[n] = v
+        self.h_in = torch.empty(self.d_in.numel(), dtype=torch.uint8, pin_memory=True)
+        self.h_in.copy_(self.d_in.cpu())
+        outs = [getattr(step, n) for n in self.OUT]
+        self.d_out, views = carve(outs)
+        for n, v in zip(self.OUT, views):
+            setattr(step, n, v)
+        self.h_out = torch.empty(self.d_out.numel(), dtype=torch.uint8, pin_memory=True)
+        slot = (w.L - 1) % w.ring
+        self.rings = []
+        for n in self.RING:
+            d = step.x[n]
+            row = d[0, 0].numel() * d.element_size()
+            h = torch.from_numpy(np.ascontiguousarray(x[n][:, slot]).view(np.uint8).reshape(-1)).pin_memory()
+            self.rings.append((d.data_ptr() + slot * row, d.stride(0) * d.element_size(), h, row,
+                               d.shape[0]))
+        self.h2d_bytes = self.d_in.numel() + sum(r[3] * r[4] for r in self.rings)
+        self.d2h_bytes = self.d_out.numel()
+        self.copies = 2 + len(self.rings)
+        self.cudart = None
+        for name in ("libcudart.so.13", "libcudart.so"):
+            try:
+                self.cudart = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if self.cudart is None:
+            raise RuntimeError("libcudart not found for the strided host-to-device copies")
+        self.ct = ctypes
+
+    def h2d(self):
+        import torch
+        stream = torch.cuda.current_stream().cuda_stream
+        self.d_in.copy_(self.h_in, non_blocking=True)
+        ct = self.ct
+        for dst, pitch, h, row, nrows in self.rings:
+            rc = self.cudart.cudaMemcpy2DAsync(ct.c_void_p(dst), ct.c_size_t(pitch),
+                                               ct.c_void_p(h.data_ptr()), ct.c_size_t(row),
+                                               ct.c_size_t(row), ct.c_size_t(nrows), 1,
+                                               ct.c_void_p(stream))
+            if rc != 0:
+                raise RuntimeError(f"cudaMemcpy2DAsync failed: {rc}")
+
+    def d2h(self):
+        self.h_out.copy_(self.d_out, non_blocking=True)
 
 
 def cpu_baseline(w, x, seqs: int) -> dict:
@@ -214,6 +307,7 @@ def main() -> None:
     w = synth.WORKLOADS[WORKLOAD]
     x = synth.make_inputs(w)
     step = make_step(w, x)
+    io = StepIO(step, x, w)         # packs per-step inputs and outputs (before capture)
     launches = step.kernel_launches()
     s_csa, s_hca = torch.cuda.Stream(), torch.cuda.Stream()
     main_s = torch.cuda.current_stream()
@@ -281,33 +375,16 @@ def main() -> None:
     # ---- end to end: host (pinned) inputs of the new token in, outputs out
     e2e = None
     if rank == 0 or world > 1:
-        new_names = ["q", "q_hca", "q_idx", "w_idx", "q_pos"]
-        host_in = {n: torch.from_numpy(np.ascontiguousarray(x[n]).view(
-            np.int16 if x[n].dtype == np.uint16 else x[n].dtype)).pin_memory() for n in new_names}
-        # the new token's raw rows (ring slot t mod R) of every ring
-        slot = (w.L - 1) % w.ring
-        ring_names = ["k_raw", "v_raw", "ik_raw", "z", "hk_raw", "hv_raw", "hz"]
-        host_ring = {n: torch.from_numpy(np.ascontiguousarray(x[n][:, slot]).view(
-            np.int16 if x[n].dtype == np.uint16 else x[n].dtype)).pin_memory() for n in ring_names}
-        outs = [step.o, step.lse, step.ho, step.hlse]
-        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-        h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + \
-            sum(t.numel() * t.element_size() for t in host_ring.values())
-        d2h = sum(t.numel() * t.element_size() for t in outs)
-
         def e2e_step():
-            for n, t in host_in.items():
-                step.x[n].view(t.dtype).copy_(t, non_blocking=True)
-            for n, t in host_ring.items():
-                step.x[n][:, slot].view(t.dtype).copy_(t, non_blocking=True)
+            io.h2d()
             g.replay()
-            for hd, dv in zip(host_out, outs):
-                hd.copy_(dv, non_blocking=True)
+            io.d2h()
         for _ in range(3):
             e2e_step()
         e_ms = timed(e2e_step, args.steps)
         e2e = {"value": world * w.B * w.T * args.steps / (sum(e_ms) / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": io.h2d_bytes, "d2h_bytes_per_step": io.d2h_bytes,
+               "copies_per_step": io.copies}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

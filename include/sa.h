@@ -119,7 +119,13 @@ int csa_compress(int dtype, int ik_dtype, int B, int d, int dI, int m, const voi
  *  ws          scratch of csa_index_topk_workspace_bytes() bytes when
  *              scores_out and scores_in are both NULL (holds the scores)
  * Kernels: bf16 with HI = 64, dI = 64 scores on the tensor cores (tcgen05);
- * other f32/bf16 shapes (HI*dI <= 12K) on CUDA cores.  N_cap <= 393216.
+ * other f32/bf16 shapes (HI*dI <= 12K) on CUDA cores.  SA_MXFP4 (HI = 64,
+ * dI = 64, N_cap a multiple of 8, 16-byte aligned codes and key scales):
+ * codes are dequantised in-kernel to e4m3 with each 64-wide row's larger
+ * block exponent factored out -- exact while the row's two block exponents
+ * differ by at most 8 -- contracted with tcgen05 kind::f8f6f4 into fp32, and
+ * the row exponents applied in fp32 before the weighted ReLU head sum.
+ * N_cap <= 393216.
  * Device errors: NaN score -> SA_ERR_NAN (row written as all -1);
  * n > N_cap -> SA_ERR_BOUNDS (n clamped).
  */
@@ -207,6 +213,22 @@ int hca_compress_attend(int dtype, int B, int T, int H, int d, int m2, int W, fl
                         int32_t* err, void* stream);
 size_t hca_compress_attend_workspace_bytes(int dtype, int B, int T, int H, int d, int N2_cap,
                                            int W);
+
+/* ---------------------------------------------------------------------------
+ * sa_mxfp4_quantize -- MXFP4 storage of bf16 rows for the low-precision
+ * indexer path ([P2q]: the indexer QK path is stored in FP4 (MXFP4)).
+ * Block rule of the OCP Microscaling Formats (MX) v1.0 specification: for
+ * each block of 32 consecutive values, e = floor(log2(max |x|)) - 2 clamped to
+ * [-127, 127] (an all-zero block gets -127); each element is x / 2^e rounded
+ * to the nearest e2m1 value (0, .5, 1, 1.5, 2, 3, 4, 6; ties to the even
+ * code), saturating at 6; a negative element that rounds to 0 is stored as +0.
+ *  x       [nblk * 32] bf16 (device)
+ *  codes   [nblk * 16] u8: element 2i in the low nibble of byte i
+ *  scales  [nblk] u8: e + 127 (e8m0)
+ * Used for the indexer queries of each step (the indexer key cache is written
+ * in this format by csa_compress with ik_dtype = SA_MXFP4).
+ */
+int sa_mxfp4_quantize(const void* x, int64_t nblk, void* codes, void* scales, void* stream);
 
 /* ---------------------------------------------------------------------------
  * attn_merge -- exact log-sum-exp merge of attention partials computed over

@@ -27,6 +27,7 @@ EXPORTS = (
     "sa_status_string", "csa_compress", "csa_index_topk", "csa_index_topk_workspace_bytes",
     "csa_attend", "csa_attend_workspace_bytes", "hca_compress_attend",
     "hca_compress_attend_workspace_bytes", "attn_merge", "csa_index_topk_noalloc",
+    "sa_mxfp4_quantize",
 )
 
 
@@ -52,6 +53,7 @@ _lib.csa_index_topk_workspace_bytes.argtypes = [_i, _i, _i, _i]
 _lib.csa_index_topk_workspace_bytes.restype = _sz
 _lib.csa_index_topk_noalloc.argtypes = [_i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i,
                                         _vp, _vp, _vp, _vp]
+_lib.sa_mxfp4_quantize.argtypes = [_vp, _i64, _vp, _vp, _vp]
 _lib.csa_attend.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _i, _vp, _vp,
                             _vp, _i, _vp, _vp, _vp, _sz, _vp, _vp]
 _lib.csa_attend_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
@@ -154,6 +156,14 @@ def hca_compress_attend(dtype, B, T, H, d, m2, W, sm_scale, q, q_pos, k_raw, v_r
                                     _p(k_raw), _p(v_raw), _p(z_hca), R, _p(blk_lo), _p(blk_hi),
                                     max_blocks, _p(hk_c), _p(hv_c), N2_cap, _p(o), _p(lse), _p(ws),
                                     ws_bytes, _p(err), _stream(stream)), "hca_compress_attend")
+
+
+def sa_mxfp4_quantize(x, codes, scales, stream=None):
+    """x: bf16 tensor whose element count is a multiple of 32; codes: uint8
+    with half as many elements; scales: uint8 with one per 32 elements."""
+    nblk = x.numel() // 32
+    _check(_lib.sa_mxfp4_quantize(_p(x), nblk, _p(codes), _p(scales), _stream(stream)),
+           "sa_mxfp4_quantize")
 
 
 def attn_merge(o_parts, lse_parts, o, lse, err=None, stream=None):

@@ -38,11 +38,11 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 struct Split {
   int nsplit, split_tiles;
 };
-Split choose_split(int64_t rows, int max_tiles) {
+// Splits per row: enough (row, split) items for `per_sm` items per SM.
+Split choose_split(int64_t rows, int max_tiles, int per_sm) {
   Split s{1, max_tiles > 0 ? max_tiles : 1};
   if (rows <= 0 || max_tiles <= 1) return s;
-  // one resident CTA per SM: at most one wave of row splits
-  const int64_t want = std::max<int64_t>(1, device_sms() / rows);
+  const int64_t want = std::max<int64_t>(1, ((int64_t)per_sm * device_sms() + rows - 1) / rows);
   int ns = (int)std::min<int64_t>(want, max_tiles);
   if (ns < 1) ns = 1;
   s.split_tiles = (max_tiles + ns - 1) / ns;
@@ -58,9 +58,18 @@ int attn_tiles(int64_t n_comp_max, int W) {
   return (int)((n_comp_max + kAttnTile - 1) / kAttnTile + (W + kAttnTile - 1) / kAttnTile);
 }
 
+// Items per SM for an attention call: the tensor-core kernel is a persistent
+// pipeline that takes about two items per SM; the CUDA-core kernel runs one
+// CTA per item, at most one wave.
+int attention_items_per_sm(int dtype, int H, int d) {
+  AttnArgs probe{};
+  probe.dtype = dtype; probe.H = H; probe.d = d;
+  return attend_tc_supported(probe) ? attend_tc_items_per_sm() : 1;
+}
+
 int run_attention(AttnArgs& a, void* ws, size_t ws_bytes, int max_tiles, cudaStream_t st) {
   const int64_t rows = (int64_t)a.B * a.T;
-  const Split s = choose_split(rows, max_tiles);
+  const Split s = choose_split(rows, max_tiles, attention_items_per_sm(a.dtype, a.H, a.d));
   a.nsplit = s.nsplit;
   a.split_tiles = s.split_tiles;
   a.part_o = nullptr;
@@ -72,7 +81,8 @@ int run_attention(AttnArgs& a, void* ws, size_t ws_bytes, int max_tiles, cudaStr
     a.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) +
                                           round256(sizeof(float) * (size_t)rows * s.nsplit * a.H * a.d));
   }
-  cudaError_t e = attend_tc_supported(a) ? launch_attend_tc(a, st) : launch_attend_simt(a, st);
+  cudaError_t e = attend_tc_supported(a) ? launch_attend_tc(a, device_sms(), st)
+                                         : launch_attend_simt(a, st);
   if (e != cudaSuccess) return status_of(e);
   return status_of(launch_merge_splits(a, st));
 }
@@ -152,7 +162,8 @@ int csa_index_topk(int q_dtype, int B, int T, int HI, int dI, int m, int k, cons
                   q_pos, dst, (int64_t)N_cap, err};
     cudaError_t e;
     if (q_dtype == SA_MXFP4) {
-      return SA_ERR_UNSUPPORTED;
+      if (!score_mx_supported(sa_)) return SA_ERR_UNSUPPORTED;
+      e = launch_score_mx(sa_, device_sms(), st);
     } else if (score_tc_supported(sa_)) {
       e = launch_score_tc(sa_, device_sms(), st);
     } else {
@@ -168,10 +179,10 @@ int csa_index_topk(int q_dtype, int B, int T, int HI, int dI, int m, int k, cons
 }
 
 size_t csa_attend_workspace_bytes(int dtype, int B, int T, int H, int d, int k, int W) {
-  (void)dtype;
   const int64_t rows = (int64_t)B * T;
   if (rows <= 0 || H <= 0 || d <= 0) return 0;
-  return split_bytes(rows, H, d, choose_split(rows, attn_tiles(k, W)));
+  return split_bytes(rows, H, d,
+                     choose_split(rows, attn_tiles(k, W), attention_items_per_sm(dtype, H, d)));
 }
 
 int csa_attend(int dtype, int B, int T, int H, int d, int m, int k, int W, float sm_scale,
@@ -199,10 +210,10 @@ int csa_attend(int dtype, int B, int T, int H, int d, int m, int k, int W, float
 
 size_t hca_compress_attend_workspace_bytes(int dtype, int B, int T, int H, int d, int N2_cap,
                                            int W) {
-  (void)dtype;
   const int64_t rows = (int64_t)B * T;
   if (rows <= 0 || H <= 0 || d <= 0) return 0;
-  return split_bytes(rows, H, d, choose_split(rows, attn_tiles(N2_cap, W)));
+  return split_bytes(rows, H, d,
+                     choose_split(rows, attn_tiles(N2_cap, W), attention_items_per_sm(dtype, H, d)));
 }
 
 int hca_compress_attend(int dtype, int B, int T, int H, int d, int m2, int W, float sm_scale,
@@ -238,6 +249,12 @@ int hca_compress_attend(int dtype, int B, int T, int H, int d, int m2, int W, fl
   a.k = 0; a.m = m2; a.kr = k_raw; a.vr = v_raw; a.R = R; a.W = W; a.o = o; a.lse = lse;
   a.err = err;
   return run_attention(a, ws, ws_bytes, attn_tiles(N2_cap, W), st);
+}
+
+int sa_mxfp4_quantize(const void* x, int64_t nblk, void* codes, void* scales, void* stream) {
+  if (nblk < 0 || (nblk > 0 && (!x || !codes || !scales))) return SA_ERR_INVALID_ARG;
+  if (nblk == 0) return SA_OK;
+  return status_of(launch_mxfp4_quantize(x, nblk, codes, scales, static_cast<cudaStream_t>(stream)));
 }
 
 int attn_merge(int n, const float* const* o_parts, const float* const* lse_parts, int64_t rows,

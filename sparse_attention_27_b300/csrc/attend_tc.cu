@@ -8,42 +8,60 @@
 // Attention (CSA)" steps 3-4 and "Heavily Compressed Attention (HCA)", and
 // "EP 95. DeepSeek-V4 논문 읽기 — 노정석", section IDEAS (one shared KV head).
 //
-// One CTA per (query row, split of its key list), 128 threads.  Keys come in
-// tiles of 64: the compressed part (rows idx[r, i] for CSA, rows 0.. for HCA)
-// then the window rows (ring slot u mod R).  Every thread gathers 16-byte
-// chunks of K and V rows with cp.async straight into the 128-byte-swizzled
-// layout the tensor core reads (masked keys are zero-filled), four tiles in
-// flight.  Per tile:
-//   S[128 x 64]  = Q[128 x 128] . K_tile^T     (tcgen05, A = Q K-major, B = K K-major)
-//   P            = exp2(S * scale*log2e - m)   (one thread per head row, fp32)
-//   O[128 x 128] += P . V_tile                 (tcgen05, A = P K-major, B = V MN-major)
-// The 64 query heads of the one query fill rows 32w..32w+15 of the M = 128
-// MMA (16 heads per TMEM lane quadrant), so all four warps share the softmax.
-// The running max is raised only when it grows by more than 8 (log2 units);
-// then O is rescaled in TMEM.  The result is normalised (or written as a
-// normalised split partial with its LSE for the merge kernel).
+// Work: an item is (query row, split of the row's key list); a persistent grid
+// of at most one CTA per SM takes items c, c+G, ...  A row's keys come in
+// tiles of 64: the compressed part (rows idx[r, i] for CSA, rows 0.. for
+// HCA), then the window rows (ring slot u mod R).
+//
+// Warp roles (288 threads):
+//  * warps 0-3, producer: gather the 16-byte chunks of each tile's K and V
+//    rows with cp.async straight into the 128B-swizzled layout the tensor core
+//    reads (masked keys zero-filled), and the item's 64 query heads into a
+//    double-buffered Q tile.  A tile is signalled (fence.proxy.async, then an
+//    mbarrier arrive) once the thread's copies two tiles back have landed, so
+//    up to four 32 KB tiles are in flight per SM, across item boundaries.
+//    Before the producer blocks on a Q buffer it signals every tile it has in
+//    flight (the MMA warp frees that buffer only after using them).
+//  * warp 4, MMA: S(n) = Q . K(n)^T (M = 64 heads, N = 64 keys, K = 128) into
+//    one of two TMEM S buffers, issued before PV(n-1) so that the softmax of
+//    tile n overlaps the tensor core; O += P(n) . V(n) (M = 64, N = 128,
+//    K = 64) into one of two TMEM O buffers (one per item in flight).
+//  * warps 5-8, softmax: one thread per head (the M = 64 accumulator puts
+//    rows 16q..16q+15 in TMEM lanes 32q..32q+15), fp32 exp2 of the scaled
+//    logits, P to shared memory in bf16; the running max is raised only when
+//    it grows by more than 8 (log2 units), and then O is rescaled in TMEM.
+//    At the end of an item it writes the normalised O and the LSE (or a
+//    normalised split partial, merged by merge_splits_kernel).
+// Every wait is bounded; on a timeout the CTA records SA_ERR_DEVICE_TIMEOUT,
+// stops, waits for its copies in flight and still frees its TMEM.
 #include "kernels.cuh"
 
 namespace sa {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 288;
 constexpr int kKeys = 64;                      // keys per tile
 constexpr int kStages = 4;
+constexpr int kLag = 2;                        // producer tiles in flight before signalling
 constexpr int kD = 128;                        // head dim
-constexpr int kQBytes = 128 * kD * 2;          // 32 KB: Q as two 64-column swizzled blocks
-constexpr int kKVBlock = kKeys * 128;          // 8 KB: one 64-dim half of a K or V tile
-constexpr int kStageBytes = 4 * kKVBlock;      // K (2 halves) + V (2 halves) = 32 KB
-constexpr int kPBytes = 128 * kKeys * 2;       // 16 KB
-constexpr int kTmemCols = 256;                 // S: 64 cols at 0; O: 128 cols at 128
+constexpr int kHeads = 64;                     // MMA M
+constexpr int kHalf = kKeys * 128;             // 8 KB: a 64-dim half of a K or V tile
+constexpr int kQBytes = kHeads * kD * 2;       // 16 KB: two 64-column halves
+constexpr int kStageBytes = 4 * kHalf;         // K (2 halves) + V (2 halves) = 32 KB
+constexpr int kPBytes = kHeads * kKeys * 2;    // 8 KB
+constexpr int kTmemCols = 512;                 // S: 2 x 64 at 0; O: 2 x 128 at 128
 constexpr float kRescaleThreshold = 8.f;       // log2 units
 
-struct Smem {
-  // 1024-aligned region follows: Q | stages | P
-  uint64_t bar_s, bar_o;
+struct Ctl {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_full[2], p_empty[2];
+  uint64_t o_empty[2], q_empty[2];
+  uint64_t pv_done;
   uint32_t tmem;
-  int valid[kStages][kKeys];
+  int abort;
+  uint8_t valid[kStages][kKeys];
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -65,276 +83,395 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-struct RowInfo {
-  int64_t nvis, n_comp, n_win, n_keys;
-  int p, b;
-};
-
-__device__ __forceinline__ RowInfo row_info(const AttnArgs& a, int64_t row) {
-  RowInfo ri;
-  ri.b = (int)(row / a.T);
-  ri.p = __ldg(a.q_pos + row);
-  ri.nvis = ri.p < 0 ? 0 : ((int64_t)ri.p + 1) / a.m;
-  if (ri.nvis > a.N_cap) ri.nvis = a.N_cap;
-  ri.n_comp = a.gather ? min64(a.k, ri.nvis) : ri.nvis;
-  ri.n_win = ri.p < 0 ? 0 : min64(a.W, (int64_t)ri.p + 1);
-  ri.n_keys = ri.n_comp + ri.n_win;
-  return ri;
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
-// Gather key tile `tile` (64 keys) of this row into stage `st`.  Thread t
-// copies key (t >> 1), 64-dim half (t & 1): 8 chunks of K and 8 of V.
-__device__ __forceinline__ void gather_tile(const AttnArgs& a, const RowInfo& ri, int64_t row,
-                                            int64_t tile, unsigned char* stage, int* valid,
-                                            int32_t* err) {
-  const int t = threadIdx.x;
+struct Item {
+  int64_t row;
+  int split;
+  int b, p;
+  int64_t nvis, n_comp, n_win, n_keys;
+  int64_t t_begin;
+  int nt;
+};
+
+__device__ __forceinline__ Item make_item(const AttnArgs& a, int64_t it) {
+  Item I;
+  I.row = it / a.nsplit;
+  I.split = (int)(it % a.nsplit);
+  I.b = (int)(I.row / a.T);
+  I.p = __ldg(a.q_pos + I.row);
+  I.nvis = I.p < 0 ? 0 : ((int64_t)I.p + 1) / a.m;
+  if (I.nvis > a.N_cap) I.nvis = a.N_cap;
+  I.n_comp = a.gather ? min64(a.k, I.nvis) : I.nvis;
+  I.n_win = I.p < 0 ? 0 : min64(a.W, (int64_t)I.p + 1);
+  I.n_keys = I.n_comp + I.n_win;
+  const int64_t nt_row = (I.n_keys + kKeys - 1) / kKeys;
+  I.t_begin = (int64_t)I.split * a.split_tiles;
+  I.nt = (int)max64(0, min64(nt_row, I.t_begin + a.split_tiles) - I.t_begin);
+  return I;
+}
+
+// Gather key tile `tile` of item I into `stage`: thread t (0..127) copies key
+// t >> 1, 64-dim half t & 1 (8 chunks of K and 8 of V).  Returns whether the
+// key is real (not padding, not a -1 index).
+__device__ __forceinline__ bool gather_tile(const AttnArgs& a, const Item& I, int64_t tile,
+                                            unsigned char* stage, int t) {
   const int key = t >> 1, half = t & 1;
   const int64_t s = tile * kKeys + key;
   const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(a.kr);
   const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(a.vr);
   int64_t src = -1;
-  if (s < ri.n_keys) {
-    if (s < ri.n_comp) {
-      int64_t j = a.gather ? (int64_t)__ldg(a.idx + row * a.k + s) : s;
-      if (j < -1 || j >= ri.nvis) {
-        set_err(err, SA_ERR_BOUNDS);
+  if (s < I.n_keys) {
+    if (s < I.n_comp) {
+      int64_t j = a.gather ? (int64_t)__ldg(a.idx + I.row * a.k + s) : s;
+      if (j < -1 || j >= I.nvis) {
+        if (half == 0) set_err(a.err, SA_ERR_BOUNDS);
         j = -1;
       }
       if (j >= 0) {
-        src = (int64_t)ri.b * a.N_cap + j;
+        src = (int64_t)I.b * a.N_cap + j;
         kp = static_cast<const __nv_bfloat16*>(a.kc);
         vp = static_cast<const __nv_bfloat16*>(a.vc);
       }
     } else {
-      const int64_t u = (int64_t)ri.p - ri.n_win + 1 + (s - ri.n_comp);
-      src = (int64_t)ri.b * a.R + u % a.R;
+      const int64_t u = (int64_t)I.p - I.n_win + 1 + (s - I.n_comp);
+      src = (int64_t)I.b * a.R + u % a.R;
     }
   }
   const uint32_t bytes = src >= 0 ? 16u : 0u;
   const int64_t off = (src >= 0 ? src : 0) * kD + half * 64;
-  const uint32_t kdst = smem_u32(stage) + half * kKVBlock;
-  const uint32_t vdst = smem_u32(stage) + 2 * kKVBlock + half * kKVBlock;
+  const uint32_t kdst = smem_u32(stage) + half * kHalf;
+  const uint32_t vdst = smem_u32(stage) + 2 * kHalf + half * kHalf;
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     cp_async16(kdst + swz(key, c), kp + off + c * 8, bytes);
     cp_async16(vdst + swz(key, c), vp + off + c * 8, bytes);
   }
-  if (half == 0) valid[key] = src >= 0;
+  return src >= 0;
 }
 
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttnArgs a) {
   extern __shared__ unsigned char smem_raw[];
-  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  Ctl& C = *reinterpret_cast<Ctl*>(smem_raw);
   unsigned char* base = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + sizeof(Smem) + 1023) & ~uintptr_t(1023));
-  unsigned char* sQ = base;
-  unsigned char* sKV = sQ + kQBytes;
-  unsigned char* sP = sKV + kStages * kStageBytes;
+      (reinterpret_cast<uintptr_t>(smem_raw) + sizeof(Ctl) + 1023) & ~uintptr_t(1023));
+  unsigned char* sQ = base;                          // [2][kQBytes]
+  unsigned char* sKV = sQ + 2 * kQBytes;             // [kStages][kStageBytes]
+  unsigned char* sP = sKV + kStages * kStageBytes;   // [2][kPBytes]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t row = blockIdx.x / a.nsplit;
-  const int split = blockIdx.x % a.nsplit;
-  const RowInfo ri = row_info(a, row);
-  const int64_t nt_row = (ri.n_keys + kKeys - 1) / kKeys;
-  const int64_t t_begin = (int64_t)split * a.split_tiles;
-  const int64_t t_end = min64(nt_row, t_begin + a.split_tiles);
-  const int nt = (int)max64(0, t_end - t_begin);
+  const int64_t n_items = (int64_t)a.B * a.T * a.nsplit;
+  volatile int* abort_flag = &C.abort;
 
   if (tid == 0) {
-    mbar_init(&S.bar_s, 1);
-    mbar_init(&S.bar_o, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&C.full[s], 128);
+      mbar_init(&C.empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&C.s_full[s], 1);
+      mbar_init(&C.s_empty[s], 128);
+      mbar_init(&C.p_full[s], 128);
+      mbar_init(&C.p_empty[s], 1);
+      mbar_init(&C.o_empty[s], 128);
+      mbar_init(&C.q_empty[s], 1);
+    }
+    mbar_init(&C.pv_done, 1);
+    C.abort = 0;
     mbar_fence_init();
   }
-  if (warp == 0) tmem_alloc(&S.tmem, kTmemCols);
-
-  // start the first gathers before staging Q
-  for (int i = 0; i < kStages - 1; ++i) {
-    if (i < nt) gather_tile(a, ri, row, t_begin + i, sKV + i * kStageBytes, S.valid[i], a.err);
-    cp_async_commit();
-  }
-  // Q rows: head h -> row 32*(h/16) + h%16; all other rows zero.  P likewise.
-  {
-    uint4* q4 = reinterpret_cast<uint4*>(sQ);
-    for (int i = tid; i < kQBytes / 16; i += kThreads) q4[i] = make_uint4(0, 0, 0, 0);
-    uint4* p4 = reinterpret_cast<uint4*>(sP);
-    for (int i = tid; i < kPBytes / 16; i += kThreads) p4[i] = make_uint4(0, 0, 0, 0);
-  }
-  __syncthreads();
-  {
-    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + row * a.H * kD;
-    for (int i = tid; i < a.H * 16; i += kThreads) {     // 16 chunks of 8 per head row
-      const int h = i >> 4, c = i & 15;
-      const int r = (h >> 4) * 32 + (h & 15);
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(q + h * kD + c * 8));
-      *reinterpret_cast<uint4*>(sQ + (c >> 3) * (128 * 128) + swz(r, c & 7)) = v;
-    }
-  }
+  // Q rows of heads >= H stay zero for the whole kernel
+  for (int i = tid; i < 2 * kQBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
+  if (warp == 4) tmem_alloc(&C.tmem, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = S.tmem;
-  const uint32_t tS = tmem, tO = tmem + 128;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const bool is_head = lane < 16 && (warp * 16 + lane) < a.H;
-  const int my_row = warp * 32 + lane;
+  const uint32_t tmem = C.tmem;
 
-  constexpr uint32_t idS = idesc_bf16(128, kKeys, 0, 0);
-  constexpr uint32_t idO = idesc_bf16(128, kD, 0, 1);
-  const float c2 = a.sm_scale * 1.4426950408889634f;   // natural logits -> log2 units
-  float m_run = -INFINITY, l_run = 0.f;
-  bool ok = true;
-
-  for (int j = 0; j < nt && ok; ++j) {
-    const int st = j % kStages;
-    unsigned char* stage = sKV + st * kStageBytes;
-    // tile j landed (groups complete in order; kStages-1 younger groups may pend)
-    cp_async_wait<kStages - 2>();
+  if (warp < 4) {
+    // ============================================================ producer
+    int64_t n = 0, ns = 0;          // tiles issued / signalled by this CTA
+    int64_t e = 0;                  // items with keys
+    bool ok = true;
+    for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const Item I = make_item(a, it);
+      if (I.nt == 0) continue;
+      const int qb = (int)(e & 1);
+      const uint32_t qpar = (uint32_t)(((e >> 1) & 1) ^ 1);
+      if (!mbar_try_wait(&C.q_empty[qb], qpar)) {
+        // The Q buffer frees only after the MMA warp has used tiles this
+        // thread has not signalled yet: signal them before blocking.
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        for (; ns < n; ++ns) mbar_arrive(&C.full[ns % kStages]);
+        if (!mbar_wait(&C.q_empty[qb], qpar, a.err)) { ok = false; break; }
+      }
+      for (int t = 0; t < I.nt; ++t, ++n) {
+        if (*abort_flag) { ok = false; break; }
+        const int st = (int)(n % kStages);
+        if (!mbar_wait(&C.empty[st], (uint32_t)(((n / kStages) & 1) ^ 1), a.err)) {
+          ok = false;
+          break;
+        }
+        if (t == 0) {             // the item's query heads, with this tile's group
+          const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + I.row * a.H * kD;
+          unsigned char* dq = sQ + qb * kQBytes;
+          for (int i = tid; i < a.H * 16; i += 128) {
+            const int h = i >> 4, c = i & 15;
+            cp_async16(smem_u32(dq + (c >> 3) * (kHeads * 128) + swz(h, c & 7)), q + h * kD + c * 8,
+                       16u);
+          }
+        }
+        const bool v = gather_tile(a, I, I.t_begin + t, sKV + st * kStageBytes, tid);
+        if ((tid & 1) == 0) C.valid[st][tid >> 1] = v ? 1 : 0;
+        cp_async_commit();
+        if (n - ns >= kLag) {     // tile ns has landed (this thread's part)
+          cp_async_wait<kLag>();
+          fence_proxy_async_smem();
+          mbar_arrive(&C.full[ns % kStages]);
+          ++ns;
+        }
+      }
+      ++e;
+    }
+    cp_async_wait<0>();
     fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
+    for (; ns < n; ++ns) mbar_arrive(&C.full[ns % kStages]);
+    if (!ok) *abort_flag = 1;
+  } else if (warp == 4) {
+    // ================================================================= MMA
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(kHeads, kKeys, 0, 0);
+      constexpr uint32_t idO = idesc_bf16(kHeads, kD, 0, 1);
+      int64_t n = 0, e = 0;
+      bool ok = true;
+      // PV of tile ordinal m (item-local t) into O buffer ob
+      auto pv = [&](int64_t m, int t, int ob, int64_t e_item) -> bool {
+        const int pb = (int)(m & 1);
+        if (!mbar_wait(&C.p_full[pb], (uint32_t)((m >> 1) & 1), a.err)) return false;
+        if (t == 0 &&
+            !mbar_wait(&C.o_empty[ob], (uint32_t)(((e_item >> 1) & 1) ^ 1), a.err))
+          return false;
+        tc_fence_after();
+        const uint32_t pa = smem_u32(sP + pb * kPBytes);
+        const uint32_t va = smem_u32(sKV + (m % kStages) * kStageBytes) + 2 * kHalf;
+        const uint32_t tO = tmem + 128 + ob * 128;
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          tc_mma_f16(tO, sdesc_kmajor_sw128(pa + kk * 32),
+                     sdesc_mnmajor_sw128(va + kk * 2048, kHalf, 1024), idO,
+                     (t > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&C.empty[m % kStages]);
+        tc_commit(&C.p_empty[pb]);
+        tc_commit(&C.pv_done);
+        return true;
+      };
+      for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const Item I = make_item(a, it);
+        if (I.nt == 0) continue;
+        const int qb = (int)(e & 1), ob = (int)(e & 1);
+        const uint32_t qa = smem_u32(sQ + qb * kQBytes);
+        for (int t = 0; t < I.nt; ++t, ++n) {
+          if (*abort_flag) { ok = false; break; }
+          const int st = (int)(n % kStages), sb = (int)(n & 1);
+          if (!mbar_wait(&C.full[st], (uint32_t)((n / kStages) & 1), a.err) ||
+              !mbar_wait(&C.s_empty[sb], (uint32_t)(((n >> 1) & 1) ^ 1), a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ka = smem_u32(sKV + st * kStageBytes);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            tc_mma_f16(tmem + sb * 64,
+                       sdesc_kmajor_sw128(qa + (kk >> 2) * (kHeads * 128) + (kk & 3) * 32),
+                       sdesc_kmajor_sw128(ka + (kk >> 2) * kHalf + (kk & 3) * 32), idS,
+                       kk > 0 ? 1u : 0u);
+          tc_commit(&C.s_full[sb]);
+          if (t == I.nt - 1) tc_commit(&C.q_empty[qb]);
+          if (t > 0 && !pv(n - 1, t - 1, ob, e)) { ok = false; break; }
+        }
+        if (!ok) break;
+        if (!pv(n - 1, I.nt - 1, ob, e)) { ok = false; break; }
+        ++e;
+      }
+      if (!ok) *abort_flag = 1;
+    }
+    __syncwarp();
+  } else {
+    // ============================================================= softmax
+    const int quad = warp & 3;
+    const int h = quad * 16 + lane;                    // head of this thread (lane < 16)
+    const bool is_head = lane < 16 && h < a.H;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const float c2 = a.sm_scale * 1.4426950408889634f;   // natural logits -> log2 units
+    int64_t n = 0, e = 0;
+    bool ok = true;
+    for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x) {
+      const Item I = make_item(a, it);
+      float* out_o = a.nsplit > 1 ? a.part_o + (I.row * a.nsplit + I.split) * a.H * kD
+                                  : a.o + I.row * a.H * kD;
+      float* out_l = a.nsplit > 1 ? a.part_lse + (I.row * a.nsplit + I.split) * a.H
+                                  : a.lse + I.row * a.H;
+      if (I.nt == 0 || !ok) {                      // no keys (or stopped): empty result
+        if (is_head) {
+          float4* dst = reinterpret_cast<float4*>(out_o + h * kD);
+          for (int i = 0; i < kD / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          out_l[h] = -INFINITY;
+        }
+        continue;
+      }
+      const int ob = (int)(e & 1);
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int t = 0; t < I.nt && ok; ++t, ++n) {
+        const int sb = (int)(n & 1), st = (int)(n % kStages), pb = (int)(n & 1);
+        ok = mbar_wait(&C.s_full[sb], (uint32_t)((n >> 1) & 1), a.err) &&
+             mbar_wait(&C.full[st], (uint32_t)((n / kStages) & 1), a.err);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        float v[64];
+        {
+          uint32_t r[64];
+          tmem_ld32_async(tmem + lane_base + sb * 64, r);
+          tmem_ld32_async(tmem + lane_base + sb * 64 + 32, r + 32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+        }
+        tc_fence_before();
+        mbar_arrive(&C.s_empty[sb]);
+        const uint32_t* vf = reinterpret_cast<const uint32_t*>(C.valid[st]);
+        float mt = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t f = vf[i];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const int k = 4 * i + b;
+            v[k] = ((f >> (8 * b)) & 0xFFu) ? v[k] * c2 : -INFINITY;
+            mt = fmaxf(mt, v[k]);
+          }
+        }
+        float alpha = 1.f;
+        bool need = false;
+        if (is_head && mt > m_run) {
+          if (m_run == -INFINITY) {
+            m_run = mt;                               // O of this item holds nothing yet
+          } else if (mt > m_run + kRescaleThreshold) {
+            alpha = fast_exp2(m_run - mt);
+            m_run = mt;
+            need = true;
+          }
+        }
+        // PV(n-1) is awaited at every tile after the first, rescale or not: the
+        // pv_done barrier is waited by parity, which is only sound while it is
+        // at most one phase away from the awaited PV.
+        if (t > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&C.pv_done, (uint32_t)((n - 1) & 1), a.err));
+          if (!ok) break;
+        }
+        if (__any_sync(0xffffffffu, need)) {          // rescale O (PV(n-1) is done)
+          tc_fence_after();
+          const uint32_t tO = tmem + lane_base + 128 + ob * 128;
+#pragma unroll 1
+          for (int c = 0; c < kD; c += 32) {
+            float o[32];
+            tmem_ld32(tO + c, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tO + c, o);
+          }
+          tmem_st_wait();
+        }
+        l_run *= alpha;
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&C.p_empty[pb], (uint32_t)(((n >> 1) & 1) ^ 1), a.err));
+        if (!ok) break;
+        if (lane < 16) {
+          unsigned char* prow = sP + pb * kPBytes;
+          float psum = 0.f;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float x0 = v[c * 8 + 2 * q], x1 = v[c * 8 + 2 * q + 1];
+              const float p0 = (!is_head || x0 == -INFINITY) ? 0.f : fast_exp2(x0 - m_run);
+              const float p1 = (!is_head || x1 == -INFINITY) ? 0.f : fast_exp2(x1 - m_run);
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+              psum += __low2float(h2) + __high2float(h2);
+              w4[q] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            *reinterpret_cast<uint4*>(prow + swz(h, c)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+          if (is_head) l_run += psum;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&C.p_full[pb]);
+      }
+      // ---- end of item: O = all PVs of the item
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&C.pv_done, (uint32_t)((n - 1) & 1), a.err));
       tc_fence_after();
-      const uint32_t qa = smem_u32(sQ), ka = smem_u32(stage);
-#pragma unroll
-      for (int kk = 0; kk < kD / 16; ++kk)
-        tc_mma_f16(tS, sdesc_kmajor_sw128(qa + (kk >> 2) * (128 * 128) + (kk & 3) * 32),
-                   sdesc_kmajor_sw128(ka + (kk >> 2) * kKVBlock + (kk & 3) * 32), idS,
-                   kk > 0 ? 1u : 0u);
-      tc_commit(&S.bar_s);
-    }
-    ok = mbar_wait(&S.bar_s, j & 1, a.err);
-    tc_fence_after();
-    // PV of tile j-1 must be done before P and O are touched, and before its
-    // stage is refilled.
-    if (j > 0) ok = ok && mbar_wait(&S.bar_o, (j - 1) & 1, a.err);
-    tc_fence_after();
-    ok = __syncthreads_and(ok);          // CTA-uniform, so no thread is left at a barrier
-    if (!ok) break;
-    // refill the stage tile j-1 used with tile j+kStages-1
-    {
-      const int jn = j + kStages - 1;
-      if (jn < nt) {
-        const int sn = jn % kStages;
-        gather_tile(a, ri, row, t_begin + jn, sKV + sn * kStageBytes, S.valid[sn], a.err);
-      }
-      cp_async_commit();
-    }
-    // ---- softmax of this tile's rows
-    float v[64];
-    tmem_ld32(tS + lane_base, v);
-    tmem_ld32(tS + lane_base + 32, v + 32);
-    float mt = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      v[i] = S.valid[st][i] ? v[i] * c2 : -INFINITY;
-      mt = fmaxf(mt, v[i]);
-    }
-    float alpha = 1.f;
-    bool need = false;
-    if (is_head && mt > m_run) {
-      if (m_run == -INFINITY) {
-        m_run = mt;                                 // O holds zeros so far
-      } else if (mt > m_run + kRescaleThreshold) {
-        alpha = exp2f(m_run - mt);
-        m_run = mt;
-        need = true;
-      }
-    }
-    if (__any_sync(0xffffffffu, need) && j > 0) {
+      const bool have = ok && l_run > 0.f;
+      const float inv = have ? 1.f / l_run : 0.f;
+      const uint32_t tO = tmem + lane_base + 128 + ob * 128;
 #pragma unroll 1
       for (int c = 0; c < kD; c += 32) {
         float o[32];
-        tmem_ld32(tO + lane_base + c, o);
+        tmem_ld32(tO + c, o);
+        if (is_head) {
+          float4* dst = reinterpret_cast<float4*>(out_o + h * kD + c);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-        tmem_st32(tO + lane_base + c, o);
-      }
-      tmem_st_wait();
-    }
-    l_run *= alpha;
-    if (is_head) {
-      float psum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = v[c * 8 + 2 * e] == -INFINITY ? 0.f : exp2f(v[c * 8 + 2 * e] - m_run);
-          const float p1 =
-              v[c * 8 + 2 * e + 1] == -INFINITY ? 0.f : exp2f(v[c * 8 + 2 * e + 1] - m_run);
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-          psum += __low2float(h2) + __high2float(h2);
-          w4[e] = *reinterpret_cast<uint32_t*>(&h2);
+          for (int i = 0; i < 8; ++i)
+            dst[i] = have ? make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                        o[4 * i + 3] * inv)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        *reinterpret_cast<uint4*>(sP + swz(my_row, c)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
-      l_run += psum;
+      if (is_head) out_l[h] = have ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+      tc_fence_before();
+      mbar_arrive(&C.o_empty[ob]);
+      ++e;
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t pa = smem_u32(sP), va = smem_u32(stage) + 2 * kKVBlock;
-#pragma unroll
-      for (int kk = 0; kk < kKeys / 16; ++kk)
-        tc_mma_f16(tO, sdesc_kmajor_sw128(pa + kk * 32),
-                   sdesc_mnmajor_sw128(va + kk * 2048, kKVBlock, 1024), idO,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-      tc_commit(&S.bar_o);
-    }
+    if (!ok) *abort_flag = 1;
   }
-  if (ok && nt > 0) ok = mbar_wait(&S.bar_o, (nt - 1) & 1, a.err);
-  ok = __syncthreads_and(ok);
-  cp_async_wait<0>();
-  tc_fence_after();
-
-  // ---- output: normalised O and LSE (or a split partial)
-  float* out_o = a.nsplit > 1 ? a.part_o + (row * a.nsplit + split) * a.H * kD : a.o + row * a.H * kD;
-  float* out_l = a.nsplit > 1 ? a.part_lse + (row * a.nsplit + split) * a.H : a.lse + row * a.H;
-  const int h = warp * 16 + lane;
-  const bool have = ok && nt > 0 && l_run > 0.f;
-  const float inv = have ? 1.f / l_run : 0.f;
-#pragma unroll 1
-  for (int c = 0; c < kD; c += 32) {
-    float o[32];
-    if (nt > 0) tmem_ld32(tO + lane_base + c, o);
-    if (is_head) {
-      float4* dst = reinterpret_cast<float4*>(out_o + h * kD + c);
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        dst[i] = have ? make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
-                                    o[4 * i + 3] * inv)
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
-  if (is_head) out_l[h] = have ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 4) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 bool attend_tc_supported(const AttnArgs& a) {
-  return a.dtype == SA_BF16 && a.d == kD && a.H >= 1 && a.H <= 64;
+  return a.dtype == SA_BF16 && a.d == kD && a.H >= 1 && a.H <= kHeads;
 }
 
-size_t attend_tc_smem() {
-  return sizeof(Smem) + 1024 + kQBytes + kStages * kStageBytes + kPBytes;
+int attend_tc_items_per_sm() { return 2; }
+
+static size_t attend_tc_smem() {
+  return sizeof(Ctl) + 1024 + 2 * kQBytes + kStages * kStageBytes + 2 * kPBytes;
 }
 
-cudaError_t launch_attend_tc(const AttnArgs& a, cudaStream_t st) {
-  const int64_t rows = (int64_t)a.B * a.T;
-  if (rows == 0) return cudaSuccess;
+cudaError_t launch_attend_tc(const AttnArgs& a, int num_sms, cudaStream_t st) {
+  const int64_t items = (int64_t)a.B * a.T * a.nsplit;
+  if (items == 0) return cudaSuccess;
   const size_t smem = attend_tc_smem();
   cudaError_t e =
       cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  attend_tc_kernel<<<(unsigned)(rows * a.nsplit), kThreads, smem, st>>>(a);
+  const int grid = (int)min64(num_sms, items);
+  attend_tc_kernel<<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -70,6 +70,40 @@ __global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressArgs
   }
   const int m = a.m, R = a.R;
   const int64_t p0 = j * m;
+  // ---- work split.  Thread (chunk c, row group g) accumulates rows
+  // i = g, g+RG, ... of one 16-byte output chunk; the RG partial sums are then
+  // added in shared memory in a fixed order.
+  const int ckv = a.d / kVec;                         // chunks per K or V row
+  const bool ik_plain = a.ik_raw != nullptr && a.ik_dtype != SA_MXFP4;
+  const int cik = ik_plain ? a.dI / kVec : 0;
+  const int nchunks = 2 * ckv + cik;
+  int RG = 1;
+  while (RG * 2 <= m && RG * 2 * nchunks <= (int)blockDim.x) RG *= 2;
+  float* s_part = s_w + m;                            // [RG][nchunks][kVec]
+  const int c = nchunks > 0 ? threadIdx.x % nchunks : 0;
+  const int g = nchunks > 0 ? threadIdx.x / nchunks : RG;
+  const void* src = nullptr;
+  void* dst = nullptr;
+  int width = 0, off = 0;
+  if (c < ckv) { src = a.k_raw; dst = a.k_c; width = a.d; off = c * kVec; }
+  else if (c < 2 * ckv) { src = a.v_raw; dst = a.v_c; width = a.d; off = (c - ckv) * kVec; }
+  else { src = a.ik_raw; dst = a.ik_c; width = a.dI; off = (c - 2 * ckv) * kVec; }
+  const bool worker = g < RG && nchunks > 0;
+  const char* base = worker ? static_cast<const char*>(src) + (int64_t)b * R * width * S::kBytes
+                            : nullptr;
+  // the first kPre rows of this thread are loaded before the pooling weights
+  // are known, so the two trips to memory overlap
+  constexpr int kPre = 16;
+  uint4 pre[kPre];
+#pragma unroll
+  for (int q = 0; q < kPre; ++q) {
+    const int i = g + q * RG;
+    if (worker && i < m) {
+      const int64_t slot = (p0 + i) % R;
+      pre[q] = __ldg(reinterpret_cast<const uint4*>(base + (slot * width + off) * S::kBytes));
+    }
+  }
+
   // ---- pooling weights: softmax of the block's logits
   for (int i = threadIdx.x; i < m; i += blockDim.x)
     s_w[i] = __ldg(a.z + (int64_t)b * R + (p0 + i) % R);
@@ -91,32 +125,12 @@ __global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressArgs
   for (int i = threadIdx.x; i < m; i += blockDim.x) s_w[i] = expf(s_w[i] - mu) * inv;
   __syncthreads();
 
-  // ---- weighted sums.  Thread (chunk c, row group g) accumulates rows
-  // i = g, g+RG, ... of one 16-byte output chunk; the RG partial sums are then
-  // added in shared memory in a fixed order.
-  const int ckv = a.d / kVec;                         // chunks per K or V row
-  const bool ik_plain = a.ik_raw != nullptr && a.ik_dtype != SA_MXFP4;
-  const int cik = ik_plain ? a.dI / kVec : 0;
-  const int nchunks = 2 * ckv + cik;
-  int RG = 1;
-  while (RG * 2 <= m && RG * 2 * nchunks <= (int)blockDim.x) RG *= 2;
-  float* s_part = s_w + m;                            // [RG][nchunks][kVec]
-  const int c = threadIdx.x % nchunks, g = threadIdx.x / nchunks;
-  const void* src = nullptr;
-  void* dst = nullptr;
-  int width = 0, off = 0;
-  if (c < ckv) { src = a.k_raw; dst = a.k_c; width = a.d; off = c * kVec; }
-  else if (c < 2 * ckv) { src = a.v_raw; dst = a.v_c; width = a.d; off = (c - ckv) * kVec; }
-  else { src = a.ik_raw; dst = a.ik_c; width = a.dI; off = (c - 2 * ckv) * kVec; }
-  if (g < RG && nchunks > 0) {
+  // ---- weighted sums
+  if (worker) {
     float acc[kVec];
 #pragma unroll
     for (int e = 0; e < kVec; ++e) acc[e] = 0.f;
-    const char* base = static_cast<const char*>(src) + (int64_t)b * R * width * S::kBytes;
-#pragma unroll 4
-    for (int i = g; i < m; i += RG) {
-      const int64_t slot = (p0 + i) % R;
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(base + (slot * width + off) * S::kBytes));
+    auto add_row = [&](const uint4& u, float wi) {
       float f[kVec];
       if constexpr (DT == SA_BF16) {
         bf16x8_to_f32(u, f);
@@ -124,9 +138,19 @@ __global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressArgs
         f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
         f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
       }
-      const float wi = s_w[i];
 #pragma unroll
       for (int e = 0; e < kVec; ++e) acc[e] = fmaf(wi, f[e], acc[e]);
+    };
+#pragma unroll
+    for (int q = 0; q < kPre; ++q) {
+      const int i = g + q * RG;
+      if (i < m) add_row(pre[q], s_w[i]);
+    }
+#pragma unroll 4
+    for (int i = g + kPre * RG; i < m; i += RG) {
+      const int64_t slot = (p0 + i) % R;
+      add_row(__ldg(reinterpret_cast<const uint4*>(base + (slot * width + off) * S::kBytes)),
+              s_w[i]);
     }
 #pragma unroll
     for (int e = 0; e < kVec; ++e) s_part[(g * nchunks + c) * kVec + e] = acc[e];

@@ -42,6 +42,8 @@ struct ScoreArgs {
 cudaError_t launch_score_simt(const ScoreArgs& a, cudaStream_t st);
 cudaError_t launch_score_tc(const ScoreArgs& a, int num_sms, cudaStream_t st);
 bool score_tc_supported(const ScoreArgs& a);
+cudaError_t launch_score_mx(const ScoreArgs& a, int num_sms, cudaStream_t st);
+bool score_mx_supported(const ScoreArgs& a);
 
 // Per-row top-k over scores (see csa_index_topk).
 struct TopkArgs {
@@ -83,8 +85,9 @@ struct AttnArgs {
 };
 constexpr int kAttnTile = 64;     // keys per attention tile (split granularity)
 cudaError_t launch_attend_simt(const AttnArgs& a, cudaStream_t st);
-cudaError_t launch_attend_tc(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_attend_tc(const AttnArgs& a, int num_sms, cudaStream_t st);
 bool attend_tc_supported(const AttnArgs& a);
+int attend_tc_items_per_sm();   // (row, split) items per SM the split choice aims at
 // Merge nsplit partials per (row, head) into o/lse.
 cudaError_t launch_merge_splits(const AttnArgs& a, cudaStream_t st);
 

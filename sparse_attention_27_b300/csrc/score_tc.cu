@@ -13,36 +13,33 @@
 // folds w and ReLU in fp32 -- no cross-thread reduction and no rounding of w
 // into bf16 operands.
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and
-// TMEM owner, warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
-// A ring of shared-memory stages holds the streamed Ik_c tiles; two TMEM
-// accumulators let the epilogue of tile i overlap the MMA of tile i+1.
-// Persistent grid: CTA c takes jobs c, c+G, ...; a job is (query group,
-// chunk of entry tiles), tiles past the group's causal limit are never loaded.
+// Warp roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer and
+// TMEM owner, warps 2..9 = two epilogue warpgroups taking alternate tiles
+// (warp w reads TMEM lanes 32*(w%4)..+31).  Decode keeps 12 tiles (192 KB) in
+// flight per SM: under load a tile takes microseconds to arrive, and the
+// bytes in flight set the bandwidth.
+// A ring of shared-memory stages holds the streamed Ik_c tiles; several TMEM
+// accumulators let the epilogue of tile i overlap the MMAs of later tiles.
+// Persistent grid of at most one CTA per SM; a job is (query group, chunk of
+// entry tiles), and tiles past the group's causal limit are never loaded.
+// With few query groups (decode) each CTA takes one contiguous run of jobs;
+// with many (prefill) it takes every G-th job.
 // Every wait is bounded; on a timeout the CTA records SA_ERR_DEVICE_TIMEOUT,
 // drops its remaining work and still frees its TMEM.
 #include <cudaTypedefs.h>
 
 #include "kernels.cuh"
+#include "score_jobs.cuh"
 
 namespace sa {
 
-constexpr int kScoreTcThreads = 192;
-constexpr int kTileEntries = 128;
-constexpr int kDI = 64;
-constexpr int kHI = 64;
-
-constexpr int kMaxJobsPerCta = 256;
-
-template <int QG>
-struct JobRec {
-  int b, t0, nq, t_lo, t_hi, g;
-  int n[QG];            // visible entries of each query of the group
-};
+constexpr int kScoreTcThreads = 320;
+constexpr int kDI = kIdxDim;
+constexpr int kHI = kIdxHeads;
 
 template <int QG>
 struct ScoreTcCfg {
-  static constexpr int kStages = QG == 1 ? 8 : 6;
+  static constexpr int kStages = QG == 1 ? 12 : 8;
   static constexpr int kAccCols = QG * kHI;
   static constexpr int kAccBufs = QG == 1 ? 4 : 2;
   static constexpr int kTmemCols = kAccBufs * kAccCols;       // 256 or 512
@@ -52,48 +49,10 @@ struct ScoreTcCfg {
                                   kMaxJobsPerCta * sizeof(JobRec<QG>);
 };
 
-struct ScoreTcParams {
-  const float* w;
-  const int32_t* q_pos;
-  int B, T, m, N_cap;
-  int chunk_tiles, max_chunks;
-  int64_t njobs;
-  float* scores;
-  int64_t ld;
-  int32_t* err;
-};
-
-template <int QG>
-__device__ __forceinline__ JobRec<QG> make_job(const ScoreTcParams& p, int64_t job) {
-  JobRec<QG> J;
-  const int64_t g = job / p.max_chunks;
-  const int c = (int)(job % p.max_chunks);
-  const int gpb = (p.T + QG - 1) / QG;
-  J.g = (int)g;
-  J.b = (int)(g / gpb);
-  J.t0 = (int)(g % gpb) * QG;
-  J.nq = min(QG, p.T - J.t0);
-  int64_t nmax = 0;
-#pragma unroll
-  for (int q = 0; q < QG; ++q) {
-    int64_t n = 0;
-    if (q < J.nq) {
-      const int pos = __ldg(p.q_pos + (int64_t)J.b * p.T + J.t0 + q);
-      n = pos < 0 ? 0 : min64(((int64_t)pos + 1) / p.m, p.N_cap);
-    }
-    J.n[q] = (int)n;
-    nmax = max64(nmax, n);
-  }
-  const int ntiles = (int)((nmax + kTileEntries - 1) / kTileEntries);
-  J.t_lo = c * p.chunk_tiles;
-  J.t_hi = min(ntiles, J.t_lo + p.chunk_tiles);
-  return J;
-}
-
 template <int QG>
 __global__ void __launch_bounds__(kScoreTcThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tm_ik,
-                    const __grid_constant__ CUtensorMap tm_q, ScoreTcParams p) {
+                    const __grid_constant__ CUtensorMap tm_q, ScoreJobs p) {
   using Cfg = ScoreTcCfg<QG>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -111,9 +70,7 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   JobRec<QG>* jobs = reinterpret_cast<JobRec<QG>*>(
       reinterpret_cast<unsigned char*>(bars) + 512);
-  const int n_my = (int)((p.njobs - blockIdx.x + gridDim.x - 1) / gridDim.x);
-  for (int i = threadIdx.x; i < n_my; i += blockDim.x)
-    jobs[i] = make_job<QG>(p, blockIdx.x + (int64_t)i * gridDim.x);
+  const int n_my = fill_job_table<QG>(p, jobs);
 
   const int warp = (int)warp_id(), lane = (int)lane_id();
   if (threadIdx.x == 0) {
@@ -209,16 +166,21 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
+    // Two warpgroups take alternate tiles (ordinal o of this CTA's tiles:
+    // group o % 2, accumulator o % kAccBufs).
+    const int grp = (warp - 2) >> 2;
     const int quad = warp & 3;
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    int acc = 0;
-    uint32_t acc_ph = 0;
+    int64_t o = 0;
     for (int ji = 0; ji < n_my && !*s_abort; ++ji) {
       const JobRec<QG>& J = jobs[ji];
       if (J.t_lo >= J.t_hi) continue;
       bool stop = false;
-      for (int t = J.t_lo; t < J.t_hi; ++t) {
+      for (int t = J.t_lo; t < J.t_hi; ++t, ++o) {
+        if ((int)(o & 1) != grp) continue;
+        const int acc = (int)(o % Cfg::kAccBufs);
+        const uint32_t acc_ph = (uint32_t)((o / Cfg::kAccBufs) & 1);
         if (!mbar_wait(&tfull[acc], acc_ph, p.err)) { *s_abort = 1; stop = true; break; }
         tc_fence_after();
         const int64_t j = (int64_t)t * kTileEntries + row_in_tile;
@@ -245,7 +207,6 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
-        if (++acc == Cfg::kAccBufs) { acc = 0; acc_ph ^= 1; }
       }
       if (stop) break;
     }
@@ -299,7 +260,7 @@ static cudaError_t launch_qg(const ScoreArgs& a, int num_sms, cudaStream_t st) {
   if (!make_tmap_bf16_rows64(&tm_ik, a.ik, (uint64_t)a.B * a.N_cap, kTileEntries) ||
       !make_tmap_bf16_rows64(&tm_q, a.q, (uint64_t)a.B * a.T * kHI, QG * kHI))
     return cudaErrorInvalidValue;
-  ScoreTcParams p;
+  ScoreJobs p{};
   p.w = a.w;
   p.q_pos = a.q_pos;
   p.B = a.B;
@@ -309,24 +270,9 @@ static cudaError_t launch_qg(const ScoreArgs& a, int num_sms, cudaStream_t st) {
   p.scores = a.scores;
   p.ld = a.ld;
   p.err = a.err;
-  const int64_t ngroups = (int64_t)a.B * ((a.T + QG - 1) / QG);
-  const int ntiles_max = (a.N_cap + kTileEntries - 1) / kTileEntries;
-  if (ngroups == 0 || ntiles_max == 0) return cudaSuccess;
-  // chunk so that there are ~16 jobs per CTA, and never more jobs than a
-  // CTA's job table holds
-  int64_t ct = (ngroups * ntiles_max) / (16LL * num_sms);
-  if (ct < 1) ct = 1;
-  if (ct > ntiles_max) ct = ntiles_max;
-  while (ct < ntiles_max &&
-         ngroups * ((ntiles_max + ct - 1) / ct) > (int64_t)kMaxJobsPerCta * num_sms)
-    ct *= 2;
-  if (ct > ntiles_max) ct = ntiles_max;
-  if (ngroups * ((ntiles_max + ct - 1) / ct) > (int64_t)kMaxJobsPerCta * num_sms)
-    return cudaErrorInvalidValue;
-  p.chunk_tiles = (int)ct;
-  p.max_chunks = (int)((ntiles_max + ct - 1) / ct);
-  p.njobs = ngroups * p.max_chunks;
-  const int grid = (int)min64(num_sms, p.njobs);
+  const int grid = plan_score_jobs(p, QG, num_sms);
+  if (grid == 0) return cudaSuccess;
+  if (grid < 0) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<QG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)Cfg::kSmem);

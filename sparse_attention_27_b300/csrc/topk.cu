@@ -30,9 +30,8 @@ constexpr int kMaxCluster = 8;       // portable cluster size
 
 struct TopkSmem {
   int hist[2][kBins];
-  int ghist[kBins];
   int scan[kTopkThreads / 32 + 1];
-  int cnt[2];          // this CTA: keys > T, keys == T
+  __align__(8) int cnt[2];   // this CTA: keys > T, keys == T
   int nan_flag;
   int sel_bin, above;
 };
@@ -85,7 +84,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(TopkArgs a, 
     cluster_sync();
     if (pass == 0) {
       int any_nan = 0;
-      for (int r = 0; r < C; ++r) any_nan |= (int)dsmem_ld_u32(&S.nan_flag, r);
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < C) any_nan |= *static_cast<const int*>(__cluster_map_shared_rank(&S.nan_flag, r));
       if (any_nan) {                              // reject the row: all -1
         if (rank == 0 && tid == 0) set_err(a.err, SA_ERR_NAN);
         for (int64_t i = (int64_t)rank * kTopkThreads + tid; i < k; i += (int64_t)C * kTopkThreads)
@@ -94,20 +95,32 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(TopkArgs a, 
         return;
       }
     }
-    for (int i = tid; i < nb; i += kTopkThreads) {
-      int g = 0;
-      for (int r = 0; r < C; ++r) g += (int)dsmem_ld_u32(&h[i], r);
-      S.ghist[i] = g;
-    }
-    __syncthreads();
-    // suffix counts from the top digit down: thread t owns reversed bins
-    // [4t, 4t+4) (nb = 2048) or [2t, 2t+2) (nb = 1024)
+    // Sum the C histograms.  Counting from the top digit down, thread t owns
+    // bins nb-1-per*t .. nb-per*(t+1) (per = 4 for nb = 2048, 2 for 1024):
+    // one 16- or 8-byte load from every CTA of the cluster, all issued before
+    // any is used.
     const int per = nb / kTopkThreads;
-    int loc[4], tot = 0;
-    for (int e = 0; e < per; ++e) {
-      loc[e] = S.ghist[nb - 1 - (tid * per + e)];
-      tot += loc[e];
+    int loc[4] = {0, 0, 0, 0};
+    if (per == 4) {
+      int4 v[kMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < C) v[r] = *static_cast<const int4*>(__cluster_map_shared_rank(
+                       reinterpret_cast<const int4*>(h + nb - 4 * (tid + 1)), r));
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < C) { loc[0] += v[r].w; loc[1] += v[r].z; loc[2] += v[r].y; loc[3] += v[r].x; }
+    } else {
+      int2 v[kMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < C) v[r] = *static_cast<const int2*>(__cluster_map_shared_rank(
+                       reinterpret_cast<const int2*>(h + nb - 2 * (tid + 1)), r));
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < C) { loc[0] += v[r].y; loc[1] += v[r].x; }
     }
+    int tot = loc[0] + loc[1] + loc[2] + loc[3];
     int base = block_exclusive_scan<kTopkThreads>(tot, S.scan, nullptr);
     for (int e = 0; e < per; ++e) {
       const int before = base, incl = base + loc[e];
@@ -140,9 +153,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cluster_kernel(TopkArgs a, 
   __syncthreads();
   cluster_sync();
   int eq_before = 0, gt_before = 0;
-  for (int r = 0; r < rank; ++r) {
-    gt_before += (int)dsmem_ld_u32(&S.cnt[0], r);
-    eq_before += (int)dsmem_ld_u32(&S.cnt[1], r);
+  {
+    int2 v[kMaxCluster];
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
+      if (r < rank) v[r] = *static_cast<const int2*>(__cluster_map_shared_rank(
+                       reinterpret_cast<const int2*>(S.cnt), r));
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
+      if (r < rank) { gt_before += v[r].x; eq_before += v[r].y; }
   }
   const int quota = max(0, min(krem - eq_before, eq_total));
   const int sel_before = gt_before + min(eq_before, krem);

@@ -14,11 +14,13 @@ own caches and sliding window.)  torch is used only to allocate device memory
 and to provide streams; all arithmetic runs in libsa27's kernels.
 
 Tensor names (device tensors, layouts row-major):
-  q, q_hca [B,T,H,d]; q_idx [B,T,HI,dI] (MXFP4: q_idx codes + q_idx_scales);
+  q, q_hca [B,T,H,d]; q_idx [B,T,HI,dI] (bf16 also for the MXFP4 indexer:
+  each pass quantises it to MXFP4 codes + scales before scoring);
   w_idx [B,T,HI] f32; q_pos [B,T] int32;
   k_raw, v_raw [B,R,d]; ik_raw [B,R,dI]; z [B,R] f32 (CSA layer ring);
   hk_raw, hv_raw [B,R,d]; hz [B,R] f32 (HCA layer ring);
-  k_c, v_c [B,ncap,d]; ik_c [B,ncap,dI] (MXFP4: ik_c codes + ik_c_scales);
+  k_c, v_c [B,ncap,d]; ik_c [B,ncap,dI] (MXFP4: ik_c = codes [B,ncap,dI/2] u8
+  and ik_c_scales [B,ncap,dI/32] u8);
   hk_c, hv_c [B,ncap2,d];
   blk_lo, blk_hi, hblk_lo, hblk_hi [B] int32 (blocks compressed this pass).
 """
@@ -30,7 +32,7 @@ import torch
 
 from . import (SA_BF16, SA_F32, SA_MXFP4, csa_attend, csa_attend_workspace_bytes, csa_compress,
                csa_index_topk, csa_index_topk_workspace_bytes, hca_compress_attend,
-               hca_compress_attend_workspace_bytes)
+               hca_compress_attend_workspace_bytes, sa_mxfp4_quantize)
 
 _CODES = {"f32": SA_F32, "bf16": SA_BF16, "mxfp4": SA_MXFP4}
 
@@ -77,6 +79,10 @@ class HybridStep:
         self.ws_b = torch.empty(max(self.ws_attend, 256), dtype=torch.uint8, device=dev)
         self.ws_c = torch.empty(max(self.ws_hca, 256), dtype=torch.uint8, device=dev)
         self.scores = None
+        if D.indexer == "mxfp4":
+            self.q_codes = torch.empty((D.B, D.T, D.HI, D.dI // 2), dtype=torch.uint8, device=dev)
+            self.q_scales = torch.empty((D.B, D.T, D.HI, D.dI // 32), dtype=torch.uint8,
+                                        device=dev)
         assert rows > 0
 
     # -------------------------------------------------------------- layers
@@ -89,8 +95,12 @@ class HybridStep:
 
     def index_topk(self, stream=None, scores_out=None, scores_in=None):
         D, x = self.D, self.x
-        csa_index_topk(_CODES[D.indexer], D.B, D.T, D.HI, D.dI, D.m, D.k, x["q_idx"],
-                       x.get("q_idx_scales"), x["w_idx"], x["ik_c"], x.get("ik_c_scales"), D.ncap,
+        q, q_scales = x["q_idx"], None
+        if D.indexer == "mxfp4" and scores_in is None:
+            sa_mxfp4_quantize(x["q_idx"], self.q_codes, self.q_scales, stream=stream)
+            q, q_scales = self.q_codes, self.q_scales
+        csa_index_topk(_CODES[D.indexer], D.B, D.T, D.HI, D.dI, D.m, D.k, q,
+                       q_scales, x["w_idx"], x["ik_c"], x.get("ik_c_scales"), D.ncap,
                        x["q_pos"], self.idx, scores_out=scores_out, scores_in=scores_in,
                        ws=self.ws_a, ws_bytes=self.ws_a.numel(), err=self.err, stream=stream)
 
@@ -135,10 +145,12 @@ class HybridStep:
         cur.wait_event(e2)
 
     def kernel_launches(self) -> int:
-        """Kernels one ``run`` launches: compress, score, top-k, attend (+ split
-        merge), HCA compress (if any block closes), HCA attend (+ split merge)."""
+        """Kernels one ``run`` launches: compress, (MXFP4: query quantiser),
+        score, top-k, attend (+ split merge), HCA compress (if any block
+        closes), HCA attend (+ split merge)."""
         D = self.D
         n = (1 if D.max_blocks > 0 else 0) + 2 + 1 + (1 if self.ws_attend > 0 else 0)
+        n += 1 if D.indexer == "mxfp4" else 0
         n += (1 if D.max_blocks2 > 0 else 0) + 1 + (1 if self.ws_hca > 0 else 0)
         return n
 

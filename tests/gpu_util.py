@@ -36,12 +36,23 @@ def dims_of(w: synth.Workload, x: dict):
 
 def device_inputs(w: synth.Workload, x: dict, device="cuda") -> dict:
     t = {k: dev(v, device) for k, v in x.items()}
+    if w.indexer == "mxfp4":
+        # the indexer key cache is stored as MXFP4: quantise the drawn bf16 cache
+        # with the library's quantiser (prefill: empty cache, written by compress)
+        import sparse_attention_27_b300 as sa
+        ik = t.pop("ik_c", None)
+        codes = torch.zeros((w.B, w.ncap, w.dI // 2), dtype=torch.uint8, device=device)
+        scales = torch.zeros((w.B, w.ncap, w.dI // 32), dtype=torch.uint8, device=device)
+        if ik is not None:
+            sa.sa_mxfp4_quantize(ik, codes, scales)
+        t["ik_c"], t["ik_c_scales"] = codes, scales
     if w.mode == "prefill":
         cdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
         idt = torch.bfloat16 if w.indexer in ("bf16", "mxfp4") else torch.float32
         t["k_c"] = torch.zeros((w.B, w.ncap, w.d), dtype=cdt, device=device)
         t["v_c"] = torch.zeros_like(t["k_c"])
-        t["ik_c"] = torch.zeros((w.B, w.ncap, w.dI), dtype=idt, device=device)
+        if w.indexer != "mxfp4":
+            t["ik_c"] = torch.zeros((w.B, w.ncap, w.dI), dtype=idt, device=device)
         t["hk_c"] = torch.zeros((w.B, w.ncap2, w.d), dtype=cdt, device=device)
         t["hv_c"] = torch.zeros_like(t["hk_c"])
     return t
