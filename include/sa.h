@@ -184,7 +184,7 @@ int csa_index_topk_noalloc(int q_dtype, int B, int T, int HI, int dI, int m, int
  *  q [B,T,H,d]; k_c, v_c [B,N_cap,d]; idx [B,T,k]; k_raw, v_raw [B,R,d]
  *  o [B,T,H,d] f32; lse [B,T,H] f32 (natural log)
  * bf16 with H <= 64, d = 128 runs on the tensor cores; other shapes on CUDA
- * cores (d <= 256).  Requires R >= W.
+ * cores (d <= 256, d a multiple of 4, H * d <= 16384).  Requires R >= W.
  * Device errors: idx entry >= n or < -1 -> SA_ERR_BOUNDS (entry ignored).
  */
 int csa_attend(int dtype, int B, int T, int H, int d, int m, int k, int W, float sm_scale,
@@ -203,7 +203,7 @@ size_t csa_attend_workspace_bytes(int dtype, int B, int T, int H, int d, int k, 
  * with the same softmax, o and lse definitions as csa_attend.
  *  q [B,T,H,d]; k_raw, v_raw [B,R,d]; z_hca [B,R] f32; hk_c, hv_c [B,N2_cap,d]
  *  o [B,T,H,d] f32; lse [B,T,H] f32
- * Requires R >= W and, when compressing, R >= m2.
+ * Requires R >= W and, when compressing, R >= m2; d <= 256, a multiple of 4.
  */
 int hca_compress_attend(int dtype, int B, int T, int H, int d, int m2, int W, float sm_scale,
                         const void* q, const int32_t* q_pos, const void* k_raw,

@@ -38,12 +38,14 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 struct Split {
   int nsplit, split_tiles;
 };
-// Splits per row: enough (row, split) items for `per_sm` items per SM.
-Split choose_split(int64_t rows, int max_tiles, int per_sm) {
+// Splits per row: enough (row, split) items for `per_sm` items per SM, and
+// no split longer than `cap` key tiles.
+Split choose_split(int64_t rows, int max_tiles, int per_sm, int cap) {
   Split s{1, max_tiles > 0 ? max_tiles : 1};
   if (rows <= 0 || max_tiles <= 1) return s;
   const int64_t want = std::max<int64_t>(1, ((int64_t)per_sm * device_sms() + rows - 1) / rows);
   int ns = (int)std::min<int64_t>(want, max_tiles);
+  ns = std::max(ns, (max_tiles + cap - 1) / cap);
   if (ns < 1) ns = 1;
   s.split_tiles = (max_tiles + ns - 1) / ns;
   s.nsplit = (max_tiles + s.split_tiles - 1) / s.split_tiles;
@@ -66,10 +68,19 @@ int attention_items_per_sm(int dtype, int H, int d) {
   probe.dtype = dtype; probe.H = H; probe.d = d;
   return attend_tc_supported(probe) ? attend_tc_items_per_sm() : 1;
 }
+int attention_split_cap(int dtype, int H, int d) {
+  AttnArgs probe{};
+  probe.dtype = dtype; probe.H = H; probe.d = d;
+  return attend_tc_supported(probe) ? kAttnTcMaxSplitTiles : (1 << 30);
+}
+Split attention_split(int dtype, int64_t rows, int H, int d, int max_tiles) {
+  return choose_split(rows, max_tiles, attention_items_per_sm(dtype, H, d),
+                      attention_split_cap(dtype, H, d));
+}
 
 int run_attention(AttnArgs& a, void* ws, size_t ws_bytes, int max_tiles, cudaStream_t st) {
   const int64_t rows = (int64_t)a.B * a.T;
-  const Split s = choose_split(rows, max_tiles, attention_items_per_sm(a.dtype, a.H, a.d));
+  const Split s = attention_split(a.dtype, rows, a.H, a.d, max_tiles);
   a.nsplit = s.nsplit;
   a.split_tiles = s.split_tiles;
   a.part_o = nullptr;
@@ -181,8 +192,7 @@ int csa_index_topk(int q_dtype, int B, int T, int HI, int dI, int m, int k, cons
 size_t csa_attend_workspace_bytes(int dtype, int B, int T, int H, int d, int k, int W) {
   const int64_t rows = (int64_t)B * T;
   if (rows <= 0 || H <= 0 || d <= 0) return 0;
-  return split_bytes(rows, H, d,
-                     choose_split(rows, attn_tiles(k, W), attention_items_per_sm(dtype, H, d)));
+  return split_bytes(rows, H, d, attention_split(dtype, rows, H, d, attn_tiles(k, W)));
 }
 
 int csa_attend(int dtype, int B, int T, int H, int d, int m, int k, int W, float sm_scale,
@@ -197,7 +207,7 @@ int csa_attend(int dtype, int B, int T, int H, int d, int m, int k, int W, float
   if (!al16(q) || !al16(o) || !al16(k_raw) || !al16(v_raw) || (k_c && !al16(k_c)) ||
       (v_c && !al16(v_c)))
     return SA_ERR_INVALID_ARG;
-  if ((size_t)H * d > 16384) return SA_ERR_UNSUPPORTED;
+  if ((size_t)H * d > 16384 || d % 4) return SA_ERR_UNSUPPORTED;
   if ((int64_t)B * T == 0) return SA_OK;
   AttnArgs a{};
   a.dtype = dtype; a.B = B; a.T = T; a.H = H; a.d = d; a.sm_scale = sm_scale;
@@ -212,8 +222,7 @@ size_t hca_compress_attend_workspace_bytes(int dtype, int B, int T, int H, int d
                                            int W) {
   const int64_t rows = (int64_t)B * T;
   if (rows <= 0 || H <= 0 || d <= 0) return 0;
-  return split_bytes(rows, H, d,
-                     choose_split(rows, attn_tiles(N2_cap, W), attention_items_per_sm(dtype, H, d)));
+  return split_bytes(rows, H, d, attention_split(dtype, rows, H, d, attn_tiles(N2_cap, W)));
 }
 
 int hca_compress_attend(int dtype, int B, int T, int H, int d, int m2, int W, float sm_scale,
@@ -230,7 +239,7 @@ int hca_compress_attend(int dtype, int B, int T, int H, int d, int m2, int W, fl
   if (!al16(q) || !al16(o) || !al16(k_raw) || !al16(v_raw) || (hk_c && !al16(hk_c)) ||
       (hv_c && !al16(hv_c)))
     return SA_ERR_INVALID_ARG;
-  if ((size_t)H * d > 16384) return SA_ERR_UNSUPPORTED;
+  if ((size_t)H * d > 16384 || d % 4) return SA_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (max_blocks > 0 && B > 0) {
     if (!z_hca || !blk_lo || !blk_hi || R < m2) return SA_ERR_INVALID_ARG;

@@ -173,35 +173,55 @@ cudaError_t launch_attend_simt(const AttnArgs& a, cudaStream_t st) {
 // (The multi-branch design of "EP 95. DeepSeek-V4 논문 읽기 — 노정석", IDEAS, and
 // the split-K partials of the kernels above.)  One warp per (row, head).
 
-// Partials are laid out [row, split, head, :]; g = row*H + head.
-__global__ void merge_splits_kernel(const float* part_o, const float* part_lse, int nsplit,
-                                    int64_t rh, int H, int d, float* o, float* lse) {
-  const int64_t g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (g >= rh) return;
-  const int lane = threadIdx.x & 31;
-  const int64_t row = g / H;
-  const int h = (int)(g % H);
-  auto L_at = [&](int s) { return part_lse[(row * nsplit + s) * H + h]; };
-  float mx = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, L_at(s));
-  float* oo = o + g * d;
-  if (mx == -INFINITY) {
-    for (int c = lane; c < d; c += 32) oo[c] = 0.f;
-    if (lane == 0) lse[g] = -INFINITY;
-    return;
-  }
-  float sum = 0.f;
-  for (int s = 0; s < nsplit; ++s) sum += expf(L_at(s) - mx);
-  const float L = mx + logf(sum);
-  for (int c = lane; c < d; c += 32) {
-    float acc = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float wgt = expf(L_at(s) - L);
-      if (wgt > 0.f) acc = fmaf(wgt, part_o[((row * nsplit + s) * H + h) * d + c], acc);
+// Partials are laid out [row, split, head, :].  A CTA merges kMergeHeads
+// heads of one query row: their split weights exp(LSE_s - LSE) go to shared
+// memory first, then each thread streams outputs with 16-byte loads that are
+// independent across splits.  Grid: (rows, ceil(H / kMergeHeads)).
+constexpr int kMergeThreads = 256;
+constexpr int kMergeHeads = 8;
+
+__global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(
+    const float* __restrict__ part_o, const float* __restrict__ part_lse, int nsplit, int H,
+    int d, float* __restrict__ o, float* __restrict__ lse) {
+  extern __shared__ float s_w[];                 // [nsplit][kMergeHeads] merge weights
+  const int64_t row = blockIdx.x;
+  const int h0 = blockIdx.y * kMergeHeads;
+  const int nh = min(kMergeHeads, H - h0);
+  const float* pl = part_lse + row * nsplit * H;
+  for (int hh = threadIdx.x; hh < nh; hh += blockDim.x) {
+    const int h = h0 + hh;
+    float mx = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, pl[s * H + h]);
+    float L = -INFINITY;
+    if (mx != -INFINITY) {
+      float sum = 0.f;
+      for (int s = 0; s < nsplit; ++s) sum += expf(pl[s * H + h] - mx);
+      L = mx + logf(sum);
     }
-    oo[c] = acc;
+    for (int s = 0; s < nsplit; ++s)
+      s_w[s * kMergeHeads + hh] = L == -INFINITY ? 0.f : expf(pl[s * H + h] - L);
+    lse[row * H + h] = L;
   }
-  if (lane == 0) lse[g] = L;
+  __syncthreads();
+  const int d4 = d / 4;
+  const int n4 = nh * d4;                        // float4 outputs of this CTA
+  const int64_t stride4 = (int64_t)H * d4;       // float4 per split of the row
+  const float4* po = reinterpret_cast<const float4*>(part_o + (row * nsplit * H + h0) * d);
+  float4* out = reinterpret_cast<float4*>(o + (row * H + h0) * d);
+  for (int e = threadIdx.x; e < n4; e += blockDim.x) {
+    const int hh = e / d4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int s = 0; s < nsplit; ++s) {
+      const float wgt = s_w[s * kMergeHeads + hh];
+      const float4 v = __ldg(po + s * stride4 + e);
+      acc.x = fmaf(wgt, v.x, acc.x);
+      acc.y = fmaf(wgt, v.y, acc.y);
+      acc.z = fmaf(wgt, v.z, acc.z);
+      acc.w = fmaf(wgt, v.w, acc.w);
+    }
+    out[e] = acc;
+  }
 }
 
 __global__ void merge_parts_kernel(MergeArgs a) {
@@ -234,11 +254,17 @@ __global__ void merge_parts_kernel(MergeArgs a) {
 
 cudaError_t launch_merge_splits(const AttnArgs& a, cudaStream_t st) {
   if (a.nsplit <= 1) return cudaSuccess;
-  const int64_t rh = (int64_t)a.B * a.T * a.H;
-  const int threads = 256;
-  const int64_t blocks = (rh * 32 + threads - 1) / threads;
-  merge_splits_kernel<<<(unsigned)blocks, threads, 0, st>>>(a.part_o, a.part_lse, a.nsplit, rh,
-                                                            a.H, a.d, a.o, a.lse);
+  const int64_t rows = (int64_t)a.B * a.T;
+  if (a.d % 4) return cudaErrorInvalidValue;
+  const size_t smem = sizeof(float) * (size_t)a.nsplit * kMergeHeads;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(merge_splits_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid((unsigned)rows, (unsigned)((a.H + kMergeHeads - 1) / kMergeHeads));
+  merge_splits_kernel<<<grid, kMergeThreads, smem, st>>>(a.part_o, a.part_lse, a.nsplit, a.H,
+                                                          a.d, a.o, a.lse);
   return cudaGetLastError();
 }
 

@@ -9,78 +9,81 @@
 // "EP 95. DeepSeek-V4 논문 읽기 — 노정석", section IDEAS (one shared KV head).
 //
 // Work: an item is (query row, split of the row's key list); a persistent grid
-// of at most one CTA per SM takes items c, c+G, ...  A row's keys come in
-// tiles of 64: the compressed part (rows idx[r, i] for CSA, rows 0.. for
-// HCA), then the window rows (ring slot u mod R).
+// of at most one CTA per SM takes items c, c+G, ...  A row's key list is the
+// compressed part (rows idx[r, i] for CSA, rows 0.. for HCA), padded to a
+// multiple of 4 keys, then the window rows (ring slot u mod R); it is
+// processed in tiles of 64 keys.
 //
-// Warp roles (288 threads):
-//  * warps 0-3, producer: gather the 16-byte chunks of each tile's K and V
-//    rows with cp.async straight into the 128B-swizzled layout the tensor core
-//    reads (masked keys zero-filled), and the item's 64 query heads into a
-//    double-buffered Q tile.  A tile is signalled (fence.proxy.async, then an
-//    mbarrier arrive) once the thread's copies two tiles back have landed, so
-//    up to four 32 KB tiles are in flight per SM, across item boundaries.
-//    Before the producer blocks on a Q buffer it signals every tile it has in
-//    flight (the MMA warp frees that buffer only after using them).
-//  * warp 4, MMA: S(n) = Q . K(n)^T (M = 64 heads, N = 64 keys, K = 128) into
+// Warp roles (192 threads):
+//  * warp 0, producer: TMA.  Each tile's K and V rows are gathered four rows
+//    at a time (cp.async.bulk.tensor tile::gather4, box 64 columns x 1 row,
+//    128-byte swizzle: the layout the tensor core reads), completing on the
+//    stage's mbarrier by byte count; rows past the key list are out-of-range
+//    coordinates and arrive as zeros.  The item's 64 query heads come by one
+//    tiled load per 64-column half into a double-buffered Q tile, and the
+//    item's slice of idx is copied to shared memory first.
+//  * warp 1, MMA: S(n) = Q . K(n)^T (M = 64 heads, N = 64 keys, K = 128) into
 //    one of two TMEM S buffers, issued before PV(n-1) so that the softmax of
 //    tile n overlaps the tensor core; O += P(n) . V(n) (M = 64, N = 128,
 //    K = 64) into one of two TMEM O buffers (one per item in flight).
-//  * warps 5-8, softmax: one thread per head (the M = 64 accumulator puts
+//  * warps 2-5, softmax: one thread per head (the M = 64 accumulator puts
 //    rows 16q..16q+15 in TMEM lanes 32q..32q+15), fp32 exp2 of the scaled
 //    logits, P to shared memory in bf16; the running max is raised only when
 //    it grows by more than 8 (log2 units), and then O is rescaled in TMEM.
 //    At the end of an item it writes the normalised O and the LSE (or a
 //    normalised split partial, merged by merge_splits_kernel).
-// Every wait is bounded; on a timeout the CTA records SA_ERR_DEVICE_TIMEOUT,
-// stops, waits for its copies in flight and still frees its TMEM.
+// Mbarriers are waited by phase parity, which is sound only while a barrier is
+// at most one phase away from the awaited one; every wait below is placed so
+// that this holds.  Every wait is bounded; on a timeout the CTA records
+// SA_ERR_DEVICE_TIMEOUT, stops and still frees its TMEM.
+#include <cudaTypedefs.h>
+
 #include "kernels.cuh"
 
 namespace sa {
 
 namespace {
 
-constexpr int kThreads = 288;
+constexpr int kThreads = 192;
 constexpr int kKeys = 64;                      // keys per tile
-constexpr int kStages = 4;
-constexpr int kLag = 2;                        // producer tiles in flight before signalling
+constexpr int kStages = 5;
 constexpr int kD = 128;                        // head dim
 constexpr int kHeads = 64;                     // MMA M
 constexpr int kHalf = kKeys * 128;             // 8 KB: a 64-dim half of a K or V tile
 constexpr int kQBytes = kHeads * kD * 2;       // 16 KB: two 64-column halves
 constexpr int kStageBytes = 4 * kHalf;         // K (2 halves) + V (2 halves) = 32 KB
 constexpr int kPBytes = kHeads * kKeys * 2;    // 8 KB
+constexpr int kIdxMax = kAttnTcMaxSplitTiles * kKeys;   // idx entries of one item (x2 buffers)
 constexpr int kTmemCols = 512;                 // S: 2 x 64 at 0; O: 2 x 128 at 128
 constexpr float kRescaleThreshold = 8.f;       // log2 units
 
 struct Ctl {
   uint64_t full[kStages], empty[kStages];
+  uint64_t q_full[2], q_empty[2];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], p_empty[2];
-  uint64_t o_empty[2], q_empty[2];
-  uint64_t pv_done;
+  uint64_t o_empty[2];
   uint32_t tmem;
   int abort;
-  uint8_t valid[kStages][kKeys];
 };
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+struct TMaps {
+  CUtensorMap kc, vc, kr, vr, q;
+};
+
+__device__ __forceinline__ void tma_gather4(const CUtensorMap* m, uint64_t* bar, void* dst,
+                                            int32_t x, int32_t y0, int32_t y1, int32_t y2,
+                                            int32_t y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+      "r"(smem_u32(bar))
+      : "memory");
 }
 
-// Byte offset of 16-byte chunk `c` (0..7) of 128-byte row `r` inside a
-// 128B-swizzled block whose base is 1024-aligned.
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -89,11 +92,17 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Byte offset of 16-byte chunk `c` (0..7) of 128-byte row `r` inside a
+// 128B-swizzled block whose base is 1024-aligned.
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
 struct Item {
   int64_t row;
   int split;
   int b, p;
-  int64_t nvis, n_comp, n_win, n_keys;
+  int64_t nvis, n_comp, n_comp_pad, n_win;
   int64_t t_begin;
   int nt;
 };
@@ -107,56 +116,18 @@ __device__ __forceinline__ Item make_item(const AttnArgs& a, int64_t it) {
   I.nvis = I.p < 0 ? 0 : ((int64_t)I.p + 1) / a.m;
   if (I.nvis > a.N_cap) I.nvis = a.N_cap;
   I.n_comp = a.gather ? min64(a.k, I.nvis) : I.nvis;
+  I.n_comp_pad = (I.n_comp + 3) & ~int64_t(3);
   I.n_win = I.p < 0 ? 0 : min64(a.W, (int64_t)I.p + 1);
-  I.n_keys = I.n_comp + I.n_win;
-  const int64_t nt_row = (I.n_keys + kKeys - 1) / kKeys;
+  const int64_t nt_row = (I.n_comp_pad + I.n_win + kKeys - 1) / kKeys;
   I.t_begin = (int64_t)I.split * a.split_tiles;
   I.nt = (int)max64(0, min64(nt_row, I.t_begin + a.split_tiles) - I.t_begin);
   return I;
 }
 
-// Gather key tile `tile` of item I into `stage`: thread t (0..127) copies key
-// t >> 1, 64-dim half t & 1 (8 chunks of K and 8 of V).  Returns whether the
-// key is real (not padding, not a -1 index).
-__device__ __forceinline__ bool gather_tile(const AttnArgs& a, const Item& I, int64_t tile,
-                                            unsigned char* stage, int t) {
-  const int key = t >> 1, half = t & 1;
-  const int64_t s = tile * kKeys + key;
-  const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(a.kr);
-  const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(a.vr);
-  int64_t src = -1;
-  if (s < I.n_keys) {
-    if (s < I.n_comp) {
-      int64_t j = a.gather ? (int64_t)__ldg(a.idx + I.row * a.k + s) : s;
-      if (j < -1 || j >= I.nvis) {
-        if (half == 0) set_err(a.err, SA_ERR_BOUNDS);
-        j = -1;
-      }
-      if (j >= 0) {
-        src = (int64_t)I.b * a.N_cap + j;
-        kp = static_cast<const __nv_bfloat16*>(a.kc);
-        vp = static_cast<const __nv_bfloat16*>(a.vc);
-      }
-    } else {
-      const int64_t u = (int64_t)I.p - I.n_win + 1 + (s - I.n_comp);
-      src = (int64_t)I.b * a.R + u % a.R;
-    }
-  }
-  const uint32_t bytes = src >= 0 ? 16u : 0u;
-  const int64_t off = (src >= 0 ? src : 0) * kD + half * 64;
-  const uint32_t kdst = smem_u32(stage) + half * kHalf;
-  const uint32_t vdst = smem_u32(stage) + 2 * kHalf + half * kHalf;
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    cp_async16(kdst + swz(key, c), kp + off + c * 8, bytes);
-    cp_async16(vdst + swz(key, c), vp + off + c * 8, bytes);
-  }
-  return src >= 0;
-}
-
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    attend_tc_kernel(const __grid_constant__ TMaps tm, AttnArgs a) {
   extern __shared__ unsigned char smem_raw[];
   Ctl& C = *reinterpret_cast<Ctl*>(smem_raw);
   unsigned char* base = reinterpret_cast<unsigned char*>(
@@ -164,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttnArgs a) {
   unsigned char* sQ = base;                          // [2][kQBytes]
   unsigned char* sKV = sQ + 2 * kQBytes;             // [kStages][kStageBytes]
   unsigned char* sP = sKV + kStages * kStageBytes;   // [2][kPBytes]
+  int32_t* sIdx = reinterpret_cast<int32_t*>(sP + 2 * kPBytes);   // [2][kIdxMax]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t n_items = (int64_t)a.B * a.T * a.nsplit;
@@ -171,48 +143,80 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttnArgs a) {
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&C.full[s], 128);
+      mbar_init(&C.full[s], 1);
       mbar_init(&C.empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
+      mbar_init(&C.q_full[s], 1);
+      mbar_init(&C.q_empty[s], 1);
       mbar_init(&C.s_full[s], 1);
       mbar_init(&C.s_empty[s], 128);
       mbar_init(&C.p_full[s], 128);
       mbar_init(&C.p_empty[s], 1);
       mbar_init(&C.o_empty[s], 128);
-      mbar_init(&C.q_empty[s], 1);
     }
-    mbar_init(&C.pv_done, 1);
     C.abort = 0;
     mbar_fence_init();
   }
-  // Q rows of heads >= H stay zero for the whole kernel
-  for (int i = tid; i < 2 * kQBytes / 16; i += kThreads)
-    reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
-  fence_proxy_async_smem();
-  if (warp == 4) tmem_alloc(&C.tmem, kTmemCols);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm.kc);
+    tma_prefetch_desc(&tm.vc);
+    tma_prefetch_desc(&tm.kr);
+    tma_prefetch_desc(&tm.vr);
+    tma_prefetch_desc(&tm.q);
+  }
+  if (warp == 1) tmem_alloc(&C.tmem, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = C.tmem;
 
-  if (warp < 4) {
+  if (warp == 0) {
     // ============================================================ producer
-    int64_t n = 0, ns = 0;          // tiles issued / signalled by this CTA
-    int64_t e = 0;                  // items with keys
+    const int32_t oob_c = (int32_t)min64((int64_t)a.B * a.N_cap, 0x7fffffff);
+    const int32_t oob_r = (int32_t)min64((int64_t)a.B * a.R, 0x7fffffff);
+    const int g = lane & 15;           // key group: keys 4g .. 4g+3 of the tile
+    const int sel = lane >> 4;         // 0: K rows, 1: V rows
+    int64_t n = 0, e = 0;
     bool ok = true;
-    for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    // idx slices go to shared memory one item ahead: the slice of item e is
+    // copied (cp.async) while item e-1 is issued; buffer e & 1
+    auto next_item = [&](int64_t it) -> int64_t {   // next item with keys, from `it`
+      for (; it < n_items; it += gridDim.x)
+        if (make_item(a, it).nt > 0) return it;
+      return n_items;
+    };
+    auto fetch_idx = [&](int64_t it, int buf) {      // commits one cp.async group
+      if (it < n_items && a.gather) {
+        const Item J = make_item(a, it);
+        const int64_t s0 = J.t_begin * kKeys;
+        const int n_sl = (int)max64(0, min64(J.n_comp, s0 + (int64_t)J.nt * kKeys) - s0);
+        const int32_t* src = a.idx + J.row * a.k + s0;
+        int32_t* dst = sIdx + buf * kIdxMax;
+        for (int i = lane; i < n_sl; i += 32) cp_async4(smem_u32(dst + i), src + i);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    int64_t it_next = next_item(blockIdx.x);
+    fetch_idx(it_next, 0);
+    for (int64_t it = it_next; it < n_items && ok; it = it_next) {
       const Item I = make_item(a, it);
-      if (I.nt == 0) continue;
       const int qb = (int)(e & 1);
-      const uint32_t qpar = (uint32_t)(((e >> 1) & 1) ^ 1);
-      if (!mbar_try_wait(&C.q_empty[qb], qpar)) {
-        // The Q buffer frees only after the MMA warp has used tiles this
-        // thread has not signalled yet: signal them before blocking.
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        for (; ns < n; ++ns) mbar_arrive(&C.full[ns % kStages]);
-        if (!mbar_wait(&C.q_empty[qb], qpar, a.err)) { ok = false; break; }
+      // ---- this item's idx slice has landed; start the next one
+      __syncwarp();                                  // all lanes are done with buffer (e+1) & 1
+      it_next = next_item(it + gridDim.x);
+      fetch_idx(it_next, (int)((e + 1) & 1));
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      __syncwarp();
+      const int64_t s0 = I.t_begin * kKeys;
+      const int32_t* idx_s = sIdx + (e & 1) * kIdxMax;
+      // ---- the item's query heads (after the MMA warp is done with this buffer)
+      if (!mbar_wait(&C.q_empty[qb], (uint32_t)(((e >> 1) & 1) ^ 1), a.err)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&C.q_full[qb], kQBytes);
+        const int32_t qrow = (int32_t)(I.row * a.H);
+        tma_load_2d(&tm.q, &C.q_full[qb], sQ + qb * kQBytes, 0, qrow);
+        tma_load_2d(&tm.q, &C.q_full[qb], sQ + qb * kQBytes + kHeads * 128, 64, qrow);
       }
       for (int t = 0; t < I.nt; ++t, ++n) {
         if (*abort_flag) { ok = false; break; }
@@ -221,32 +225,46 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttnArgs a) {
           ok = false;
           break;
         }
-        if (t == 0) {             // the item's query heads, with this tile's group
-          const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + I.row * a.H * kD;
-          unsigned char* dq = sQ + qb * kQBytes;
-          for (int i = tid; i < a.H * 16; i += 128) {
-            const int h = i >> 4, c = i & 15;
-            cp_async16(smem_u32(dq + (c >> 3) * (kHeads * 128) + swz(h, c & 7)), q + h * kD + c * 8,
-                       16u);
+        if (lane == 0) mbar_arrive_expect_tx(&C.full[st], kStageBytes);
+        __syncwarp();
+        // the group's four rows: compressed part, padding, window, or past the list
+        const int64_t sg = (I.t_begin + t) * kKeys + 4 * g;
+        const bool comp = sg < I.n_comp_pad;
+        int32_t y[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int64_t s = sg + q;
+          int32_t row;
+          if (comp) {
+            row = oob_c;
+            if (s < I.n_comp) {
+              const int64_t j = a.gather ? (int64_t)idx_s[s - s0] : s;
+              if (j >= 0 && j < I.nvis) {
+                row = (int32_t)((int64_t)I.b * a.N_cap + j);
+              } else if (j != -1 && sel == 0) {
+                set_err(a.err, SA_ERR_BOUNDS);
+              }
+            }
+          } else {
+            const int64_t w = s - I.n_comp_pad;
+            row = oob_r;
+            if (w < I.n_win) {
+              const int64_t u = (int64_t)I.p - I.n_win + 1 + w;
+              row = (int32_t)((int64_t)I.b * a.R + u % a.R);
+            }
           }
+          y[q] = row;
         }
-        const bool v = gather_tile(a, I, I.t_begin + t, sKV + st * kStageBytes, tid);
-        if ((tid & 1) == 0) C.valid[st][tid >> 1] = v ? 1 : 0;
-        cp_async_commit();
-        if (n - ns >= kLag) {     // tile ns has landed (this thread's part)
-          cp_async_wait<kLag>();
-          fence_proxy_async_smem();
-          mbar_arrive(&C.full[ns % kStages]);
-          ++ns;
-        }
+        const CUtensorMap* map = comp ? (sel ? &tm.vc : &tm.kc) : (sel ? &tm.vr : &tm.kr);
+        unsigned char* dst = sKV + st * kStageBytes + sel * 2 * kHalf + 4 * g * 128;
+        tma_gather4(map, &C.full[st], dst, 0, y[0], y[1], y[2], y[3]);
+        tma_gather4(map, &C.full[st], dst + kHalf, 64, y[0], y[1], y[2], y[3]);
       }
       ++e;
     }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    for (; ns < n; ++ns) mbar_arrive(&C.full[ns % kStages]);
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     if (!ok) *abort_flag = 1;
-  } else if (warp == 4) {
+  } else if (warp == 1) {
     // ================================================================= MMA
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(kHeads, kKeys, 0, 0);
@@ -271,7 +289,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttnArgs a) {
                      (t > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&C.empty[m % kStages]);
         tc_commit(&C.p_empty[pb]);
-        tc_commit(&C.pv_done);
         return true;
       };
       for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -279,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttnArgs a) {
         if (I.nt == 0) continue;
         const int qb = (int)(e & 1), ob = (int)(e & 1);
         const uint32_t qa = smem_u32(sQ + qb * kQBytes);
+        if (!mbar_wait(&C.q_full[qb], (uint32_t)((e >> 1) & 1), a.err)) { ok = false; break; }
         for (int t = 0; t < I.nt; ++t, ++n) {
           if (*abort_flag) { ok = false; break; }
           const int st = (int)(n % kStages), sb = (int)(n & 1);
@@ -332,10 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttnArgs a) {
       const int ob = (int)(e & 1);
       float m_run = -INFINITY, l_run = 0.f;
       for (int t = 0; t < I.nt && ok; ++t, ++n) {
-        const int sb = (int)(n & 1), st = (int)(n % kStages), pb = (int)(n & 1);
-        ok = mbar_wait(&C.s_full[sb], (uint32_t)((n >> 1) & 1), a.err) &&
-             mbar_wait(&C.full[st], (uint32_t)((n / kStages) & 1), a.err);
-        ok = __all_sync(0xffffffffu, ok);
+        const int sb = (int)(n & 1), pb = (int)(n & 1);
+        ok = __all_sync(0xffffffffu, mbar_wait(&C.s_full[sb], (uint32_t)((n >> 1) & 1), a.err));
         if (!ok) break;
         tc_fence_after();
         float v[64];
@@ -349,18 +365,21 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttnArgs a) {
         }
         tc_fence_before();
         mbar_arrive(&C.s_empty[sb]);
-        const uint32_t* vf = reinterpret_cast<const uint32_t*>(C.valid[st]);
-        float mt = -INFINITY;
+        // key i of the tile is real iff it is in the compressed part or the
+        // window: bits [0, c_hi) and [w_lo, w_hi) of a 64-bit mask
+        const int64_t s0 = (I.t_begin + t) * kKeys;
+        const int c_hi = (int)max64(0, min64(64, I.n_comp - s0));
+        const int w_lo = (int)max64(0, min64(64, I.n_comp_pad - s0));
+        const int w_hi = (int)max64(0, min64(64, I.n_comp_pad + I.n_win - s0));
+        auto ones = [](int k) -> uint64_t { return k >= 64 ? ~0ull : ((1ull << k) - 1ull); };
+        const uint64_t real = ones(c_hi) | (ones(w_hi) & ~ones(w_lo));
+        float mraw = -INFINITY;                    // max of the raw logits (c2 > 0)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t f = vf[i];
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const int k = 4 * i + b;
-            v[k] = ((f >> (8 * b)) & 0xFFu) ? v[k] * c2 : -INFINITY;
-            mt = fmaxf(mt, v[k]);
-          }
+        for (int i = 0; i < 64; ++i) {
+          v[i] = ((real >> i) & 1ull) ? v[i] : -INFINITY;
+          mraw = fmaxf(mraw, v[i]);
         }
+        const float mt = mraw * c2;
         float alpha = 1.f;
         bool need = false;
         if (is_head && mt > m_run) {
@@ -372,14 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttnArgs a) {
             need = true;
           }
         }
-        // PV(n-1) is awaited at every tile after the first, rescale or not: the
-        // pv_done barrier is waited by parity, which is only sound while it is
-        // at most one phase away from the awaited PV.
-        if (t > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&C.pv_done, (uint32_t)((n - 1) & 1), a.err));
+        if (__any_sync(0xffffffffu, need)) {
+          // rescale O after PV(n-1), which signals p_empty of its P buffer (the
+          // wait at tile n-1 already covered PV(n-3) on that barrier)
+          ok = __all_sync(0xffffffffu, mbar_wait(&C.p_empty[(n - 1) & 1],
+                                                 (uint32_t)(((n - 1) >> 1) & 1), a.err));
           if (!ok) break;
-        }
-        if (__any_sync(0xffffffffu, need)) {          // rescale O (PV(n-1) is done)
           tc_fence_after();
           const uint32_t tO = tmem + lane_base + 128 + ob * 128;
 #pragma unroll 1
@@ -393,20 +410,23 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttnArgs a) {
           tmem_st_wait();
         }
         l_run *= alpha;
+        // P buffer pb is free once PV(n-2) is done
         ok = __all_sync(0xffffffffu,
                         mbar_wait(&C.p_empty[pb], (uint32_t)(((n >> 1) & 1) ^ 1), a.err));
         if (!ok) break;
         if (lane < 16) {
           unsigned char* prow = sP + pb * kPBytes;
+          const float mref = m_run == -INFINITY ? 0.f : m_run;
           float psum = 0.f;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             uint32_t w4[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const float x0 = v[c * 8 + 2 * q], x1 = v[c * 8 + 2 * q + 1];
-              const float p0 = (!is_head || x0 == -INFINITY) ? 0.f : fast_exp2(x0 - m_run);
-              const float p1 = (!is_head || x1 == -INFINITY) ? 0.f : fast_exp2(x1 - m_run);
+              // exp2(c2 * v - m): masked keys (-inf) give +0; with nothing real
+              // so far m is -inf and every v is -inf
+              const float p0 = is_head ? fast_exp2(fmaf(v[c * 8 + 2 * q], c2, -mref)) : 0.f;
+              const float p1 = is_head ? fast_exp2(fmaf(v[c * 8 + 2 * q + 1], c2, -mref)) : 0.f;
               __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
               psum += __low2float(h2) + __high2float(h2);
               w4[q] = *reinterpret_cast<uint32_t*>(&h2);
@@ -419,8 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttnArgs a) {
         tc_fence_before();
         mbar_arrive(&C.p_full[pb]);
       }
-      // ---- end of item: O = all PVs of the item
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&C.pv_done, (uint32_t)((n - 1) & 1), a.err));
+      // ---- end of item: O = all PVs of the item (PV(n-1) signals p_empty)
+      if (ok)
+        ok = __all_sync(0xffffffffu, mbar_wait(&C.p_empty[(n - 1) & 1],
+                                               (uint32_t)(((n - 1) >> 1) & 1), a.err));
       tc_fence_after();
       const bool have = ok && l_run > 0.f;
       const float inv = have ? 1.f / l_run : 0.f;
@@ -447,10 +469,40 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttnArgs a) {
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// ---------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// bf16 matrix [rows, 128] (256-byte rows), box 64 columns x box_rows rows,
+// 128-byte swizzle, zero fill out of range.
+static bool tmap_rows128(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (!enc || rows == 0) return false;
+  cuuint64_t dims[2] = {128, rows};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool attend_tc_supported(const AttnArgs& a) {
@@ -460,18 +512,30 @@ bool attend_tc_supported(const AttnArgs& a) {
 int attend_tc_items_per_sm() { return 2; }
 
 static size_t attend_tc_smem() {
-  return sizeof(Ctl) + 1024 + 2 * kQBytes + kStages * kStageBytes + 2 * kPBytes;
+  return sizeof(Ctl) + 1024 + 2 * kQBytes + kStages * kStageBytes + 2 * kPBytes +
+         2 * sizeof(int32_t) * kIdxMax;
 }
 
 cudaError_t launch_attend_tc(const AttnArgs& a, int num_sms, cudaStream_t st) {
   const int64_t items = (int64_t)a.B * a.T * a.nsplit;
   if (items == 0) return cudaSuccess;
+  if (a.split_tiles > kAttnTcMaxSplitTiles) return cudaErrorInvalidValue;
+  const uint64_t ring_rows = (uint64_t)a.B * a.R;
+  const uint64_t comp_rows = (uint64_t)a.B * a.N_cap;
+  TMaps tm;
+  // a call without compressed rows never reads them: point those maps at the ring
+  const bool have_c = a.kc != nullptr && a.vc != nullptr && comp_rows > 0;
+  if (!tmap_rows128(&tm.kr, a.kr, ring_rows, 1) || !tmap_rows128(&tm.vr, a.vr, ring_rows, 1) ||
+      !tmap_rows128(&tm.kc, have_c ? a.kc : a.kr, have_c ? comp_rows : ring_rows, 1) ||
+      !tmap_rows128(&tm.vc, have_c ? a.vc : a.vr, have_c ? comp_rows : ring_rows, 1) ||
+      !tmap_rows128(&tm.q, a.q, (uint64_t)a.B * a.T * a.H, kHeads))
+    return cudaErrorInvalidValue;
   const size_t smem = attend_tc_smem();
   cudaError_t e =
       cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = (int)min64(num_sms, items);
-  attend_tc_kernel<<<grid, kThreads, smem, st>>>(a);
+  attend_tc_kernel<<<grid, kThreads, smem, st>>>(tm, a);
   return cudaGetLastError();
 }
 

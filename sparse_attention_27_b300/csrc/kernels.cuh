@@ -84,6 +84,7 @@ struct AttnArgs {
   int32_t* err;
 };
 constexpr int kAttnTile = 64;     // keys per attention tile (split granularity)
+constexpr int kAttnTcMaxSplitTiles = 32;   // tensor-core kernel: key tiles per split at most
 cudaError_t launch_attend_simt(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_attend_tc(const AttnArgs& a, int num_sms, cudaStream_t st);
 bool attend_tc_supported(const AttnArgs& a);

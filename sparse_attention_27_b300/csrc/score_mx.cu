@@ -19,7 +19,8 @@
 // the nearest e4m3 value).
 //
 // Warp roles (320 threads): warp 0 = bulk-copy producer (raw codes + scales of
-// 128 entries per tile, 4352 bytes), warp 1 = MMA issuer and TMEM owner,
+// 128 entries per tile, 4352 bytes, into a ring of raw stages that the
+// converters and the epilogue both release), warp 1 = MMA issuer and TMEM owner,
 // warps 2..5 = converters (one entry row per thread: e2m1 -> e4m3 into a
 // 128B-swizzled K-major tile; they also convert each query group's B tile),
 // warps 6..9 = epilogue (weighted ReLU head sum, as in the bf16 kernel).
@@ -35,7 +36,6 @@ namespace sa {
 namespace {
 
 constexpr int kMxThreads = 320;
-constexpr int kRawStages = 8;
 constexpr int kAStages = 4;
 constexpr int kCodeRowBytes = kIdxDim / 2;                       // 32
 constexpr int kScaleRowBytes = kIdxDim / 32;                     // 2
@@ -46,6 +46,9 @@ constexpr int kABytes = kTileEntries * kARowBytes;               // 16 KB
 
 template <int QG>
 struct MxCfg {
+  // raw stages are released by the converters and the epilogue, which trails
+  // the converters by up to kAStages + kAccBufs tiles
+  static constexpr int kRawStages = QG == 1 ? 16 : 12;
   static constexpr int kAccCols = QG * kIdxHeads;
   static constexpr int kAccBufs = QG == 1 ? 4 : 2;
   static constexpr int kTmemCols = kAccBufs * kAccCols;          // 256 or 512
@@ -149,6 +152,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
   unsigned char* sA = smem;
   unsigned char* sB = sA + kAStages * kABytes;
   unsigned char* sRaw = sB + 2 * Cfg::kBBytes;
+  constexpr int kRawStages = Cfg::kRawStages;
   uint32_t* lut = reinterpret_cast<uint32_t*>(sRaw + kRawStages * kRawBytes);   // [16][2]
   uint64_t* bars = reinterpret_cast<uint64_t*>(lut + 32);
   uint64_t* raw_full = bars;
@@ -170,7 +174,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
     reinterpret_cast<uint8_t*>(lut)[s * 8 + c] = e4m3_of(c, s);
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kRawStages; ++s) { mbar_init(&raw_full[s], 1); mbar_init(&raw_empty[s], 128); }
+    for (int s = 0; s < kRawStages; ++s) { mbar_init(&raw_full[s], 1); mbar_init(&raw_empty[s], 256); }
     for (int s = 0; s < kAStages; ++s) { mbar_init(&a_full[s], 128); mbar_init(&a_empty[s], 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(&b_full[s], 128); mbar_init(&b_empty[s], 1); }
     for (int s = 0; s < Cfg::kAccBufs; ++s) { mbar_init(&t_full[s], 1); mbar_init(&t_empty[s], 128); }
@@ -296,6 +300,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     int acc = 0;
     uint32_t acc_ph = 0;
+    int64_t o = 0;                // tile ordinal (raw stage o % kRawStages)
     float wq[64];                 // w[r,h] * 2^(e_row(q_h)) of the current query
     for (int ji = 0; ji < n_my && !*s_abort; ++ji) {
       const JobRec<QG>& J = jobs[ji];
@@ -304,11 +309,20 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
       bool stop = false;
       for (int t = J.t_lo; t < J.t_hi; ++t) {
         if (!mbar_wait(&t_full[acc], acc_ph, p.err)) { *s_abort = 1; stop = true; break; }
+        // this entry row's key scales, from the raw stage of tile o (held until
+        // the epilogue has read them)
+        const int rs = (int)(o % kRawStages);
+        if (!mbar_wait(&raw_full[rs], (uint32_t)((o / kRawStages) & 1), p.err)) {
+          *s_abort = 1;
+          stop = true;
+          break;
+        }
+        const unsigned char* rsc = sRaw + rs * kRawBytes + kRawCodeBytes + 2 * row_in_tile;
+        const float kscale = pow2i(max((int)rsc[0], (int)rsc[1]) - 127);
+        mbar_arrive(&raw_empty[rs]);
+        ++o;
         tc_fence_after();
         const int64_t j = (int64_t)t * kTileEntries + row_in_tile;
-        const int64_t jj = min64(j, (int64_t)p.N_cap - 1);
-        const uint8_t* ks = x.k_scales + ((int64_t)J.b * p.N_cap + jj) * kScaleRowBytes;
-        const float kscale = pow2i(max((int)__ldg(ks), (int)__ldg(ks + 1)) - 127);
 #pragma unroll 1
         for (int q = 0; q < J.nq; ++q) {
           const int64_t r = (int64_t)J.b * p.T + J.t0 + q;
