@@ -14,19 +14,20 @@
 // multiple of 4 keys, then the window rows (ring slot u mod R); it is
 // processed in tiles of 64 keys.
 //
-// Warp roles (192 threads):
-//  * warp 0, producer: TMA.  Each tile's K and V rows are gathered four rows
-//    at a time (cp.async.bulk.tensor tile::gather4, box 64 columns x 1 row,
-//    128-byte swizzle: the layout the tensor core reads), completing on the
-//    stage's mbarrier by byte count; rows past the key list are out-of-range
-//    coordinates and arrive as zeros.  The item's 64 query heads come by one
-//    tiled load per 64-column half into a double-buffered Q tile, and the
-//    item's slice of idx is copied to shared memory first.
-//  * warp 1, MMA: S(n) = Q . K(n)^T (M = 64 heads, N = 64 keys, K = 128) into
+// Warp roles (288 threads):
+//  * warps 0-3, producers: warp w issues the tiles with ordinal n = w (mod 4).
+//    Lane l gathers keys 2l and 2l+1 -- sixteen 16-byte chunks of the K row
+//    and of the V row each, by cp.async, straight into the 128B-swizzled
+//    layout the tensor core reads (keys past the list are zero-filled) --
+//    waits for its copies, fences them to the async proxy and arrives on the
+//    stage's mbarrier, so four tiles are in flight per SM without coupling.
+//    Warp 0 also brings the item's 64 query heads by one TMA tiled load per
+//    64-column half into a double-buffered Q tile.
+//  * warp 4, MMA: S(n) = Q . K(n)^T (M = 64 heads, N = 64 keys, K = 128) into
 //    one of two TMEM S buffers, issued before PV(n-1) so that the softmax of
 //    tile n overlaps the tensor core; O += P(n) . V(n) (M = 64, N = 128,
 //    K = 64) into one of two TMEM O buffers (one per item in flight).
-//  * warps 2-5, softmax: one thread per head (the M = 64 accumulator puts
+//  * warps 5-8, softmax: one thread per head (the M = 64 accumulator puts
 //    rows 16q..16q+15 in TMEM lanes 32q..32q+15), fp32 exp2 of the scaled
 //    logits, P to shared memory in bf16; the running max is raised only when
 //    it grows by more than 8 (log2 units), and then O is rescaled in TMEM.
@@ -44,7 +45,7 @@ namespace sa {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 288;
 constexpr int kKeys = 64;                      // keys per tile
 constexpr int kStages = 5;
 constexpr int kD = 128;                        // head dim
@@ -53,7 +54,6 @@ constexpr int kHalf = kKeys * 128;             // 8 KB: a 64-dim half of a K or 
 constexpr int kQBytes = kHeads * kD * 2;       // 16 KB: two 64-column halves
 constexpr int kStageBytes = 4 * kHalf;         // K (2 halves) + V (2 halves) = 32 KB
 constexpr int kPBytes = kHeads * kKeys * 2;    // 8 KB
-constexpr int kIdxMax = kAttnTcMaxSplitTiles * kKeys;   // idx entries of one item (x2 buffers)
 constexpr int kTmemCols = 512;                 // S: 2 x 64 at 0; O: 2 x 128 at 128
 constexpr float kRescaleThreshold = 8.f;       // log2 units
 
@@ -68,22 +68,13 @@ struct Ctl {
 };
 
 struct TMaps {
-  CUtensorMap kc, vc, kr, vr, q;
+  CUtensorMap q;
 };
 
-__device__ __forceinline__ void tma_gather4(const CUtensorMap* m, uint64_t* bar, void* dst,
-                                            int32_t x, int32_t y0, int32_t y1, int32_t y2,
-                                            int32_t y3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
-      "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -135,7 +126,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* sQ = base;                          // [2][kQBytes]
   unsigned char* sKV = sQ + 2 * kQBytes;             // [kStages][kStageBytes]
   unsigned char* sP = sKV + kStages * kStageBytes;   // [2][kPBytes]
-  int32_t* sIdx = reinterpret_cast<int32_t*>(sP + 2 * kPBytes);   // [2][kIdxMax]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t n_items = (int64_t)a.B * a.T * a.nsplit;
@@ -143,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&C.full[s], 1);
+      mbar_init(&C.full[s], 32);
       mbar_init(&C.empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -158,113 +148,85 @@ __global__ void __launch_bounds__(kThreads, 1)
     C.abort = 0;
     mbar_fence_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm.kc);
-    tma_prefetch_desc(&tm.vc);
-    tma_prefetch_desc(&tm.kr);
-    tma_prefetch_desc(&tm.vr);
-    tma_prefetch_desc(&tm.q);
-  }
-  if (warp == 1) tmem_alloc(&C.tmem, kTmemCols);
+  if (warp == 0 && lane == 0) tma_prefetch_desc(&tm.q);
+  if (warp == 4) tmem_alloc(&C.tmem, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = C.tmem;
 
-  if (warp == 0) {
+  if (warp < 4) {
     // ============================================================ producer
-    const int32_t oob_c = (int32_t)min64((int64_t)a.B * a.N_cap, 0x7fffffff);
-    const int32_t oob_r = (int32_t)min64((int64_t)a.B * a.R, 0x7fffffff);
-    const int g = lane & 15;           // key group: keys 4g .. 4g+3 of the tile
-    const int sel = lane >> 4;         // 0: K rows, 1: V rows
+    // warp w issues the tiles with ordinal n = w (mod 4): lane l gathers keys
+    // 2l and 2l+1 (16 chunks of K and 16 of V each), waits for its copies,
+    // fences them to the async proxy and arrives on the stage's barrier.
+    const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(a.kc);
+    const __nv_bfloat16* vc = static_cast<const __nv_bfloat16*>(a.vc);
+    const __nv_bfloat16* kr = static_cast<const __nv_bfloat16*>(a.kr);
+    const __nv_bfloat16* vr = static_cast<const __nv_bfloat16*>(a.vr);
     int64_t n = 0, e = 0;
     bool ok = true;
-    // idx slices go to shared memory one item ahead: the slice of item e is
-    // copied (cp.async) while item e-1 is issued; buffer e & 1
-    auto next_item = [&](int64_t it) -> int64_t {   // next item with keys, from `it`
-      for (; it < n_items; it += gridDim.x)
-        if (make_item(a, it).nt > 0) return it;
-      return n_items;
-    };
-    auto fetch_idx = [&](int64_t it, int buf) {      // commits one cp.async group
-      if (it < n_items && a.gather) {
-        const Item J = make_item(a, it);
-        const int64_t s0 = J.t_begin * kKeys;
-        const int n_sl = (int)max64(0, min64(J.n_comp, s0 + (int64_t)J.nt * kKeys) - s0);
-        const int32_t* src = a.idx + J.row * a.k + s0;
-        int32_t* dst = sIdx + buf * kIdxMax;
-        for (int i = lane; i < n_sl; i += 32) cp_async4(smem_u32(dst + i), src + i);
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-    int64_t it_next = next_item(blockIdx.x);
-    fetch_idx(it_next, 0);
-    for (int64_t it = it_next; it < n_items && ok; it = it_next) {
+    for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const Item I = make_item(a, it);
-      const int qb = (int)(e & 1);
-      // ---- this item's idx slice has landed; start the next one
-      __syncwarp();                                  // all lanes are done with buffer (e+1) & 1
-      it_next = next_item(it + gridDim.x);
-      fetch_idx(it_next, (int)((e + 1) & 1));
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-      __syncwarp();
-      const int64_t s0 = I.t_begin * kKeys;
-      const int32_t* idx_s = sIdx + (e & 1) * kIdxMax;
-      // ---- the item's query heads (after the MMA warp is done with this buffer)
-      if (!mbar_wait(&C.q_empty[qb], (uint32_t)(((e >> 1) & 1) ^ 1), a.err)) { ok = false; break; }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&C.q_full[qb], kQBytes);
-        const int32_t qrow = (int32_t)(I.row * a.H);
-        tma_load_2d(&tm.q, &C.q_full[qb], sQ + qb * kQBytes, 0, qrow);
-        tma_load_2d(&tm.q, &C.q_full[qb], sQ + qb * kQBytes + kHeads * 128, 64, qrow);
+      if (I.nt == 0) continue;
+      if (warp == 0) {            // the item's query heads, once the MMA warp has let go of the buffer
+        const int qb = (int)(e & 1);
+        if (!mbar_wait(&C.q_empty[qb], (uint32_t)(((e >> 1) & 1) ^ 1), a.err)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&C.q_full[qb], kQBytes);
+          const int32_t qrow = (int32_t)(I.row * a.H);
+          tma_load_2d(&tm.q, &C.q_full[qb], sQ + qb * kQBytes, 0, qrow);
+          tma_load_2d(&tm.q, &C.q_full[qb], sQ + qb * kQBytes + kHeads * 128, 64, qrow);
+        }
       }
       for (int t = 0; t < I.nt; ++t, ++n) {
+        if ((int)(n & 3) != warp) continue;
         if (*abort_flag) { ok = false; break; }
         const int st = (int)(n % kStages);
         if (!mbar_wait(&C.empty[st], (uint32_t)(((n / kStages) & 1) ^ 1), a.err)) {
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&C.full[st], kStageBytes);
-        __syncwarp();
-        // the group's four rows: compressed part, padding, window, or past the list
-        const int64_t sg = (I.t_begin + t) * kKeys + 4 * g;
-        const bool comp = sg < I.n_comp_pad;
-        int32_t y[4];
+        unsigned char* stage = sKV + st * kStageBytes;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int64_t s = sg + q;
-          int32_t row;
-          if (comp) {
-            row = oob_c;
-            if (s < I.n_comp) {
-              const int64_t j = a.gather ? (int64_t)idx_s[s - s0] : s;
-              if (j >= 0 && j < I.nvis) {
-                row = (int32_t)((int64_t)I.b * a.N_cap + j);
-              } else if (j != -1 && sel == 0) {
-                set_err(a.err, SA_ERR_BOUNDS);
-              }
+        for (int q = 0; q < 2; ++q) {
+          const int key = 2 * lane + q;
+          const int64_t s = (I.t_begin + t) * kKeys + key;
+          const __nv_bfloat16* ks = kr;
+          const __nv_bfloat16* vs = vr;
+          int64_t row = -1;
+          if (s < I.n_comp) {
+            const int64_t j = a.gather ? (int64_t)__ldg(a.idx + I.row * a.k + s) : s;
+            if (j >= 0 && j < I.nvis) {
+              row = (int64_t)I.b * a.N_cap + j;
+              ks = kc;
+              vs = vc;
+            } else if (j != -1) {
+              set_err(a.err, SA_ERR_BOUNDS);
             }
-          } else {
-            const int64_t w = s - I.n_comp_pad;
-            row = oob_r;
-            if (w < I.n_win) {
-              const int64_t u = (int64_t)I.p - I.n_win + 1 + w;
-              row = (int32_t)((int64_t)I.b * a.R + u % a.R);
-            }
+          } else if (s >= I.n_comp_pad && s < I.n_comp_pad + I.n_win) {
+            const int64_t u = (int64_t)I.p - I.n_win + 1 + (s - I.n_comp_pad);
+            row = (int64_t)I.b * a.R + u % a.R;
           }
-          y[q] = row;
+          const uint32_t bytes = row >= 0 ? 16u : 0u;
+          const int64_t off = (row >= 0 ? row : 0) * kD;
+          const uint32_t kd = smem_u32(stage), vd = smem_u32(stage) + 2 * kHalf;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const uint32_t o = (c >> 3) * kHalf + swz(key, c & 7);
+            cp_async16(kd + o, ks + off + c * 8, bytes);
+            cp_async16(vd + o, vs + off + c * 8, bytes);
+          }
         }
-        const CUtensorMap* map = comp ? (sel ? &tm.vc : &tm.kc) : (sel ? &tm.vr : &tm.kr);
-        unsigned char* dst = sKV + st * kStageBytes + sel * 2 * kHalf + 4 * g * 128;
-        tma_gather4(map, &C.full[st], dst, 0, y[0], y[1], y[2], y[3]);
-        tma_gather4(map, &C.full[st], dst + kHalf, 64, y[0], y[1], y[2], y[3]);
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        fence_proxy_async_smem();
+        mbar_arrive(&C.full[st]);
       }
       ++e;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     if (!ok) *abort_flag = 1;
-  } else if (warp == 1) {
+  } else if (warp == 4) {
     // ================================================================= MMA
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(kHeads, kKeys, 0, 0);
@@ -469,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 4) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -512,24 +474,15 @@ bool attend_tc_supported(const AttnArgs& a) {
 int attend_tc_items_per_sm() { return 2; }
 
 static size_t attend_tc_smem() {
-  return sizeof(Ctl) + 1024 + 2 * kQBytes + kStages * kStageBytes + 2 * kPBytes +
-         2 * sizeof(int32_t) * kIdxMax;
+  return sizeof(Ctl) + 1024 + 2 * kQBytes + kStages * kStageBytes + 2 * kPBytes;
 }
 
 cudaError_t launch_attend_tc(const AttnArgs& a, int num_sms, cudaStream_t st) {
   const int64_t items = (int64_t)a.B * a.T * a.nsplit;
   if (items == 0) return cudaSuccess;
   if (a.split_tiles > kAttnTcMaxSplitTiles) return cudaErrorInvalidValue;
-  const uint64_t ring_rows = (uint64_t)a.B * a.R;
-  const uint64_t comp_rows = (uint64_t)a.B * a.N_cap;
   TMaps tm;
-  // a call without compressed rows never reads them: point those maps at the ring
-  const bool have_c = a.kc != nullptr && a.vc != nullptr && comp_rows > 0;
-  if (!tmap_rows128(&tm.kr, a.kr, ring_rows, 1) || !tmap_rows128(&tm.vr, a.vr, ring_rows, 1) ||
-      !tmap_rows128(&tm.kc, have_c ? a.kc : a.kr, have_c ? comp_rows : ring_rows, 1) ||
-      !tmap_rows128(&tm.vc, have_c ? a.vc : a.vr, have_c ? comp_rows : ring_rows, 1) ||
-      !tmap_rows128(&tm.q, a.q, (uint64_t)a.B * a.T * a.H, kHeads))
-    return cudaErrorInvalidValue;
+  if (!tmap_rows128(&tm.q, a.q, (uint64_t)a.B * a.T * a.H, kHeads)) return cudaErrorInvalidValue;
   const size_t smem = attend_tc_smem();
   cudaError_t e =
       cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -18,12 +18,14 @@
 // (rows whose blocks differ by more than 8 exponents round the small block to
 // the nearest e4m3 value).
 //
-// Warp roles (320 threads): warp 0 = bulk-copy producer (raw codes + scales of
+// Warp roles (448 threads): warp 0 = bulk-copy producer (raw codes + scales of
 // 128 entries per tile, 4352 bytes, into a ring of raw stages that the
 // converters and the epilogue both release), warp 1 = MMA issuer and TMEM owner,
 // warps 2..5 = converters (one entry row per thread: e2m1 -> e4m3 into a
 // 128B-swizzled K-major tile; they also convert each query group's B tile),
-// warps 6..9 = epilogue (weighted ReLU head sum, as in the bf16 kernel).
+// warps 6..13 = two epilogue warpgroups taking alternate tiles (weighted ReLU
+// head sum as in the bf16 kernel; each warp keeps its query weights, with the
+// row exponents folded in, in shared memory).
 // Every wait is bounded; on a timeout the CTA records SA_ERR_DEVICE_TIMEOUT,
 // stops and still frees its TMEM.
 #include <cuda_fp8.h>
@@ -35,7 +37,8 @@ namespace sa {
 
 namespace {
 
-constexpr int kMxThreads = 320;
+constexpr int kMxThreads = 448;
+constexpr int kMxEpiWarps = 8;     // two epilogue warpgroups
 constexpr int kAStages = 4;
 constexpr int kCodeRowBytes = kIdxDim / 2;                       // 32
 constexpr int kScaleRowBytes = kIdxDim / 32;                     // 2
@@ -53,9 +56,10 @@ struct MxCfg {
   static constexpr int kAccBufs = QG == 1 ? 4 : 2;
   static constexpr int kTmemCols = kAccBufs * kAccCols;          // 256 or 512
   static constexpr int kBBytes = QG * kIdxHeads * kARowBytes;    // 8 KB per query
+  static constexpr size_t kWqBytes = kMxEpiWarps * QG * kIdxHeads * sizeof(float);
   static constexpr size_t kSmem = 1024 + kAStages * kABytes + 2 * kBBytes +
                                   kRawStages * kRawBytes + 1024 /* LUT + barriers */ +
-                                  kMaxJobsPerCta * sizeof(JobRec<QG>);
+                                  kMaxJobsPerCta * sizeof(JobRec<QG>) + kWqBytes;
 };
 
 struct MxPtrs {
@@ -123,22 +127,19 @@ __device__ __forceinline__ float pow2i(int e) {
   return __int_as_float((e + 127) << 23);
 }
 
-// Head weights of query row r with its per-head row exponents folded in:
-// wq[h] = w[r,h] * 2^(max block exponent of q_I[r,h,:]).
-__device__ __forceinline__ void load_wq(const ScoreJobs& p, const MxPtrs& x, int64_t r,
-                                        float* wq) {
-  const float4* w4 = reinterpret_cast<const float4*>(p.w + r * kIdxHeads);
-  const uchar2* qs = reinterpret_cast<const uchar2*>(x.q_scales + r * kIdxHeads * 2);
+// Head weights of query row r with its per-head row exponents folded in,
+// wq[h] = w[r,h] * 2^(max block exponent of q_I[r,h,:]), written by the 32
+// lanes of a warp (two heads each) to that warp's 64 floats of shared memory.
+__device__ __forceinline__ void store_wq(const ScoreJobs& p, const MxPtrs& x, int64_t r,
+                                         float* dst) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float4 wv = __ldg(w4 + i);
-    wq[4 * i + 0] = wv.x; wq[4 * i + 1] = wv.y; wq[4 * i + 2] = wv.z; wq[4 * i + 3] = wv.w;
+  for (int u = 0; u < 2; ++u) {
+    const int h = lane + 32 * u;
+    const uint8_t* qs = x.q_scales + (r * kIdxHeads + h) * 2;
+    dst[h] = __ldg(p.w + r * kIdxHeads + h) * pow2i(max((int)__ldg(qs), (int)__ldg(qs + 1)) - 127);
   }
-#pragma unroll
-  for (int h = 0; h < 64; ++h) {
-    const uchar2 sc = __ldg(qs + h);
-    wq[h] *= pow2i(max((int)sc.x, (int)sc.y) - 127);
-  }
+  __syncwarp();
 }
 
 }  // namespace
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(t_empty + Cfg::kAccBufs);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   JobRec<QG>* jobs = reinterpret_cast<JobRec<QG>*>(reinterpret_cast<unsigned char*>(lut) + 1024);
+  float* s_wq = reinterpret_cast<float*>(jobs + kMaxJobsPerCta);   // [kMxEpiWarps][QG][64]
 
   const int n_my = fill_job_table<QG>(p, jobs);
   const int warp = (int)warp_id(), lane = (int)lane_id();
@@ -295,20 +297,28 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Two warpgroups take alternate tiles: tile ordinal o goes to group o % 2,
+    // accumulator o % kAccBufs.
+    const int grp = (warp - 6) >> 2;
     const int quad = warp & 3;
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    int acc = 0;
-    uint32_t acc_ph = 0;
+    float* wq = s_wq + (warp - 6) * QG * kIdxHeads;     // this warp's weights, per query
     int64_t o = 0;                // tile ordinal (raw stage o % kRawStages)
-    float wq[64];                 // w[r,h] * 2^(e_row(q_h)) of the current query
     for (int ji = 0; ji < n_my && !*s_abort; ++ji) {
       const JobRec<QG>& J = jobs[ji];
       if (J.t_lo >= J.t_hi) continue;
-      if constexpr (QG == 1) load_wq(p, x, (int64_t)J.b * p.T + J.t0, wq);
+      __syncwarp();                                      // previous job's weights are consumed
+      for (int q = 0; q < J.nq; ++q) store_wq(p, x, (int64_t)J.b * p.T + J.t0 + q, wq + q * kIdxHeads);
       bool stop = false;
-      for (int t = J.t_lo; t < J.t_hi; ++t) {
-        if (!mbar_wait(&t_full[acc], acc_ph, p.err)) { *s_abort = 1; stop = true; break; }
+      for (int t = J.t_lo; t < J.t_hi; ++t, ++o) {
+        if ((int)(o & 1) != grp) continue;
+        const int acc = (int)(o % Cfg::kAccBufs);
+        if (!mbar_wait(&t_full[acc], (uint32_t)((o / Cfg::kAccBufs) & 1), p.err)) {
+          *s_abort = 1;
+          stop = true;
+          break;
+        }
         // this entry row's key scales, from the raw stage of tile o (held until
         // the epilogue has read them)
         const int rs = (int)(o % kRawStages);
@@ -320,7 +330,6 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
         const unsigned char* rsc = sRaw + rs * kRawBytes + kRawCodeBytes + 2 * row_in_tile;
         const float kscale = pow2i(max((int)rsc[0], (int)rsc[1]) - 127);
         mbar_arrive(&raw_empty[rs]);
-        ++o;
         tc_fence_after();
         const int64_t j = (int64_t)t * kTileEntries + row_in_tile;
 #pragma unroll 1
@@ -329,21 +338,21 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
           uint32_t v[64];
           tmem_ld32_async(tmem + lane_base + acc * Cfg::kAccCols + q * kIdxHeads, v);
           tmem_ld32_async(tmem + lane_base + acc * Cfg::kAccCols + q * kIdxHeads + 32, v + 32);
-          if constexpr (QG != 1) load_wq(p, x, r, wq);
           tmem_wait_ld();
+          const float4* w4 = reinterpret_cast<const float4*>(wq + q * kIdxHeads);
           float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            s0 = fmaf(wq[4 * i + 0], fmaxf(__uint_as_float(v[4 * i + 0]), 0.f), s0);
-            s1 = fmaf(wq[4 * i + 1], fmaxf(__uint_as_float(v[4 * i + 1]), 0.f), s1);
-            s2 = fmaf(wq[4 * i + 2], fmaxf(__uint_as_float(v[4 * i + 2]), 0.f), s2);
-            s3 = fmaf(wq[4 * i + 3], fmaxf(__uint_as_float(v[4 * i + 3]), 0.f), s3);
+            const float4 wv = w4[i];
+            s0 = fmaf(wv.x, fmaxf(__uint_as_float(v[4 * i + 0]), 0.f), s0);
+            s1 = fmaf(wv.y, fmaxf(__uint_as_float(v[4 * i + 1]), 0.f), s1);
+            s2 = fmaf(wv.z, fmaxf(__uint_as_float(v[4 * i + 2]), 0.f), s2);
+            s3 = fmaf(wv.w, fmaxf(__uint_as_float(v[4 * i + 3]), 0.f), s3);
           }
           if (j < J.n[q]) p.scores[r * p.ld + j] = ((s0 + s1) + (s2 + s3)) * kscale;
         }
         tc_fence_before();
         mbar_arrive(&t_empty[acc]);
-        if (++acc == Cfg::kAccBufs) { acc = 0; acc_ph ^= 1; }
       }
       if (stop) break;
     }

@@ -35,7 +35,7 @@ constexpr int kMaxCluster = 8;        // portable cluster size
 struct TopkSmem {
   int hist[2][kBins];
   int scan[kTopkWarps + 1];
-  int wgt[kTopkWarps], weq[kTopkWarps];   // per-warp counts of one compaction round
+  int wgt[2 * kTopkWarps], weq[kTopkWarps];   // per-warp counts / min-max scratch
   __align__(8) int cnt[2];                // this CTA: keys > T, keys == T
   int nan_flag;
   int sel_bin, above;
@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a, int C, i
 // If the list comes out shorter than k or longer than its buffer (a skewed or
 // tied row), steps 3-4 fall back to the radix select over all the row's keys.
 constexpr int kRowMax = 32768;
+constexpr int kTopkSmemBytes = (sizeof(TopkSmem) + 15) & ~15;   // keys start 16-byte aligned
 constexpr int kCandMax = 8192;
 constexpr int kSampleStride = 16;
 
@@ -298,6 +299,21 @@ __device__ uint32_t radix_select(const uint32_t* keys, int m, int kk, TopkSmem& 
 constexpr int kKpt = 8;
 constexpr int kRound = kKpt * kTopkThreads;
 
+// keys[ib .. ib+7] by two 16-byte shared loads (entries past m read as 0 and
+// are masked by the callers).  Lists are 16-byte aligned and padded to a
+// multiple of 8 entries, so a group that starts below m is in bounds.
+__device__ __forceinline__ void load8(const uint32_t* keys, int ib, int m, uint32_t* kk) {
+  if (ib < m) {
+    const uint4 u0 = *reinterpret_cast<const uint4*>(keys + ib);
+    const uint4 u1 = *reinterpret_cast<const uint4*>(keys + ib + 4);
+    kk[0] = u0.x; kk[1] = u0.y; kk[2] = u0.z; kk[3] = u0.w;
+    kk[4] = u1.x; kk[5] = u1.y; kk[6] = u1.z; kk[7] = u1.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < kKpt; ++j) kk[j] = 0u;
+  }
+}
+
 // Write, in list order, the entries with key > T and the first `take` with
 // key == T: out[p] = idx_of(i) for the p-th such entry.  The counts of a
 // thread's entries (key > T in the high half, key == T in the low half of one
@@ -311,9 +327,9 @@ __device__ void emit_selected(const uint32_t* keys, int m, uint32_t T, int take,
     const int ib = i0 + tid * kKpt;
     uint32_t kk[kKpt];
     int ng = 0, ne = 0;
+    load8(keys, ib, m, kk);
 #pragma unroll
     for (int j = 0; j < kKpt; ++j) {
-      kk[j] = ib + j < m ? keys[ib + j] : 0u;
       ng += ib + j < m && kk[j] > T;
       ne += ib + j < m && kk[j] == T;
     }
@@ -336,10 +352,61 @@ __device__ void emit_selected(const uint32_t* keys, int m, uint32_t T, int take,
   }
 }
 
+// Min and max of v over the CTA, returned to every thread.
+__device__ __forceinline__ void block_minmax(uint32_t lo, uint32_t hi, uint32_t* mn, uint32_t* mx,
+                                             int* scratch /* >= 2 * kTopkWarps */) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  uint32_t a = lo, b = hi;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+  }
+  if (lane == 0) { scratch[2 * w] = (int)a; scratch[2 * w + 1] = (int)b; }
+  __syncthreads();
+  a = lane < kTopkWarps ? (uint32_t)scratch[2 * lane] : 0xffffffffu;
+  b = lane < kTopkWarps ? (uint32_t)scratch[2 * lane + 1] : 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+  }
+  __syncthreads();
+  *mn = a;
+  *mx = b;
+}
+
+// A key Ts such that at least r of keys[0..m) are >= Ts (1 <= r <= m), close
+// to the r-th largest: the lower edge of the linear bin (2048 bins over
+// [min, max]) that holds the r-th largest key.
+__device__ uint32_t threshold_at_least(const uint32_t* keys, int m, int r, TopkSmem& S) {
+  const int tid = threadIdx.x;
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  for (int i = tid; i < m; i += kTopkThreads) { lo = min(lo, keys[i]); hi = max(hi, keys[i]); }
+  uint32_t kmin, kmax;
+  block_minmax(lo, hi, &kmin, &kmax, S.wgt);
+  const uint64_t span = (uint64_t)(kmax - kmin) + 1;
+  int* h = S.hist[0];
+  for (int i = tid; i < kBins; i += kTopkThreads) h[i] = 0;
+  __syncthreads();
+  for (int i = tid; i < m; i += kTopkThreads)
+    atomicAdd(&h[(int)(((uint64_t)(keys[i] - kmin) * kBins) / span)], 1);
+  __syncthreads();
+  const int loc0 = h[kBins - 1 - 2 * tid], loc1 = h[kBins - 2 - 2 * tid];
+  const int base = block_exclusive_scan<kTopkThreads>(loc0 + loc1, S.scan, nullptr);
+  if (base < r && base + loc0 >= r) S.sel_bin = kBins - 1 - 2 * tid;
+  else if (base + loc0 < r && base + loc0 + loc1 >= r) S.sel_bin = kBins - 2 - 2 * tid;
+  __syncthreads();
+  const uint64_t b = (uint64_t)S.sel_bin;
+  __syncthreads();
+  // smallest key whose bin is >= b
+  return kmin + (uint32_t)((b * span + kBins - 1) / kBins);
+}
+
 __global__ void __launch_bounds__(kTopkThreads) topk_row_kernel(TopkArgs a, int n_pad) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   TopkSmem& S = *reinterpret_cast<TopkSmem*>(smem_raw);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + sizeof(TopkSmem));   // [n_pad]
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + kTopkSmemBytes);   // [n_pad]
   uint32_t* samp = keys + n_pad;                                             // [n_pad / 16]
   uint32_t* ck = samp + n_pad / kSampleStride;                               // [kCandMax]
   int32_t* ci = reinterpret_cast<int32_t*>(ck + kCandMax);                   // [kCandMax]
@@ -356,7 +423,19 @@ __global__ void __launch_bounds__(kTopkThreads) topk_row_kernel(TopkArgs a, int 
   }
   const float* src = a.scores + row * a.ld;
   int nan_local = 0;
-  for (int i = tid; i < n; i += kTopkThreads) {
+  int n4 = 0;
+  if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {       // 16-byte loads, four in flight
+    n4 = n / 4;
+    const float4* src4 = reinterpret_cast<const float4*>(src);
+    uint4* keys4 = reinterpret_cast<uint4*>(keys);
+#pragma unroll 4
+    for (int i = tid; i < n4; i += kTopkThreads) {
+      const float4 f = src4[i];
+      nan_local |= is_nan_bits(f.x) | is_nan_bits(f.y) | is_nan_bits(f.z) | is_nan_bits(f.w);
+      keys4[i] = make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
+    }
+  }
+  for (int i = 4 * n4 + tid; i < n; i += kTopkThreads) {
     const float f = src[i];
     nan_local |= is_nan_bits(f);
     keys[i] = score_key(f);
@@ -371,19 +450,16 @@ __global__ void __launch_bounds__(kTopkThreads) topk_row_kernel(TopkArgs a, int 
   __syncthreads();
   int rs = (int)(((int64_t)k * ns * 13 + (int64_t)n * 10 - 1) / ((int64_t)n * 10));   // ~1.3 k/16
   rs = max(1, min(rs, ns));
-  int dummy;
-  const uint32_t Ts = radix_select(samp, ns, rs, S, &dummy);
+  const uint32_t Ts = threshold_at_least(samp, ns, rs, S);
   // ---- candidates: keys >= Ts, in index order
   int count = 0;
   for (int i0 = 0; i0 < n; i0 += kRound) {
     const int ib = i0 + tid * kKpt;
     uint32_t kk[kKpt];
     int nc = 0;
+    load8(keys, ib, n, kk);
 #pragma unroll
-    for (int j = 0; j < kKpt; ++j) {
-      kk[j] = ib + j < n ? keys[ib + j] : 0u;
-      nc += ib + j < n && kk[j] >= Ts;
-    }
+    for (int j = 0; j < kKpt; ++j) nc += ib + j < n && kk[j] >= Ts;
     int tot;
     int pos = count + block_exclusive_scan<kTopkThreads>(nc, S.scan, &tot);
 #pragma unroll
@@ -411,8 +487,8 @@ bool topk_supported(int N_cap) { return N_cap <= kMaxChunk * kMaxCluster; }
 cudaError_t launch_topk(const TopkArgs& a, int num_sms, cudaStream_t st) {
   if (a.rows <= 0) return cudaSuccess;
   if (a.N_cap <= kRowMax) {
-    const int n_pad = (a.N_cap + 31) & ~31;
-    const size_t smem = sizeof(TopkSmem) + sizeof(uint32_t) * (size_t)(n_pad + n_pad / kSampleStride) +
+    const int n_pad = (a.N_cap + 63) & ~63;   // keeps every list 16-byte aligned
+    const size_t smem = kTopkSmemBytes + sizeof(uint32_t) * (size_t)(n_pad + n_pad / kSampleStride) +
                         (sizeof(uint32_t) + sizeof(int32_t)) * (size_t)kCandMax;
     cudaError_t e = cudaFuncSetAttribute(topk_row_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
