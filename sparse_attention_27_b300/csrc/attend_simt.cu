@@ -174,33 +174,43 @@ cudaError_t launch_attend_simt(const AttnArgs& a, cudaStream_t st) {
 // the split-K partials of the kernels above.)  One warp per (row, head).
 
 // Partials are laid out [row, split, head, :].  A CTA merges kMergeHeads
-// heads of one query row: their split weights exp(LSE_s - LSE) go to shared
-// memory first, then each thread streams outputs with 16-byte loads that are
-// independent across splits.  Grid: (rows, ceil(H / kMergeHeads)).
+// heads of one query row.  All threads first fetch the split LSEs into shared
+// memory at once (one memory round trip rather than nsplit dependent loads);
+// kMergeHeads threads turn them into weights exp(LSE_s - LSE); then each
+// thread issues up to kMergeBatch independent 16-byte partial loads before it
+// accumulates them.  Grid: (rows, ceil(H / kMergeHeads)).
 constexpr int kMergeThreads = 256;
 constexpr int kMergeHeads = 8;
+constexpr int kMergeBatch = 8;
 
 __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(
     const float* __restrict__ part_o, const float* __restrict__ part_lse, int nsplit, int H,
     int d, float* __restrict__ o, float* __restrict__ lse) {
-  extern __shared__ float s_w[];                 // [nsplit][kMergeHeads] merge weights
+  extern __shared__ float s_w[];                 // [nsplit][kMergeHeads]: LSEs, then weights
   const int64_t row = blockIdx.x;
   const int h0 = blockIdx.y * kMergeHeads;
   const int nh = min(kMergeHeads, H - h0);
-  const float* pl = part_lse + row * nsplit * H;
-  for (int hh = threadIdx.x; hh < nh; hh += blockDim.x) {
-    const int h = h0 + hh;
+  const float* pl = part_lse + row * nsplit * H + h0;
+  for (int i = threadIdx.x; i < nsplit * kMergeHeads; i += blockDim.x) {
+    const int s = i / kMergeHeads, hh = i % kMergeHeads;
+    s_w[i] = hh < nh ? __ldg(pl + s * H + hh) : -INFINITY;
+  }
+  __syncthreads();
+  if (threadIdx.x < nh) {
+    const int hh = threadIdx.x;
     float mx = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, pl[s * H + h]);
+    for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, s_w[s * kMergeHeads + hh]);
     float L = -INFINITY;
     if (mx != -INFINITY) {
       float sum = 0.f;
-      for (int s = 0; s < nsplit; ++s) sum += expf(pl[s * H + h] - mx);
+      for (int s = 0; s < nsplit; ++s) sum += expf(s_w[s * kMergeHeads + hh] - mx);
       L = mx + logf(sum);
     }
-    for (int s = 0; s < nsplit; ++s)
-      s_w[s * kMergeHeads + hh] = L == -INFINITY ? 0.f : expf(pl[s * H + h] - L);
-    lse[row * H + h] = L;
+    for (int s = 0; s < nsplit; ++s) {
+      const float l = s_w[s * kMergeHeads + hh];
+      s_w[s * kMergeHeads + hh] = L == -INFINITY ? 0.f : expf(l - L);
+    }
+    lse[row * H + h0 + hh] = L;
   }
   __syncthreads();
   const int d4 = d / 4;
@@ -211,14 +221,21 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(
   for (int e = threadIdx.x; e < n4; e += blockDim.x) {
     const int hh = e / d4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int s = 0; s < nsplit; ++s) {
-      const float wgt = s_w[s * kMergeHeads + hh];
-      const float4 v = __ldg(po + s * stride4 + e);
-      acc.x = fmaf(wgt, v.x, acc.x);
-      acc.y = fmaf(wgt, v.y, acc.y);
-      acc.z = fmaf(wgt, v.z, acc.z);
-      acc.w = fmaf(wgt, v.w, acc.w);
+    for (int s0 = 0; s0 < nsplit; s0 += kMergeBatch) {
+      float4 v[kMergeBatch];
+#pragma unroll
+      for (int j = 0; j < kMergeBatch; ++j)
+        if (s0 + j < nsplit) v[j] = __ldg(po + (s0 + j) * stride4 + e);
+#pragma unroll
+      for (int j = 0; j < kMergeBatch; ++j) {
+        if (s0 + j < nsplit) {
+          const float wgt = s_w[(s0 + j) * kMergeHeads + hh];
+          acc.x = fmaf(wgt, v[j].x, acc.x);
+          acc.y = fmaf(wgt, v[j].y, acc.y);
+          acc.z = fmaf(wgt, v[j].z, acc.z);
+          acc.w = fmaf(wgt, v[j].w, acc.w);
+        }
+      }
     }
     out[e] = acc;
   }
