@@ -27,10 +27,12 @@
 //    one of two TMEM S buffers, issued before PV(n-1) so that the softmax of
 //    tile n overlaps the tensor core; O += P(n) . V(n) (M = 64, N = 128,
 //    K = 64) into one of two TMEM O buffers (one per item in flight).
-//  * warps 5-8, softmax: one thread per head (the M = 64 accumulator puts
-//    rows 16q..16q+15 in TMEM lanes 32q..32q+15), fp32 exp2 of the scaled
-//    logits, P to shared memory in bf16; the running max is raised only when
-//    it grows by more than 8 (log2 units), and then O is rescaled in TMEM.
+//  * warps 5-8, softmax: the M = 64 accumulator puts rows 16q..16q+15 in
+//    TMEM lanes 32q..32q+15; the 16x256b load shape spreads those 16 rows
+//    over all 32 lanes (two heads and a quarter of the keys per lane), fp32
+//    exp2 of the scaled logits, P to shared memory in bf16; the running max
+//    is raised only when it grows by more than 8 (log2 units), and then O is
+//    rescaled in TMEM.
 //    At the end of an item it writes the normalised O and the LSE (or a
 //    normalised split partial, merged by merge_splits_kernel).
 // Mbarriers are waited by phase parity, which is sound only while a barrier is
@@ -288,9 +290,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ============================================================= softmax
+    // S and O are read with the 16x256b TMEM shape: lane l holds heads
+    // h0 = 16q + l/4 and h1 = h0 + 8 (q = this warp's TMEM quarter), keys
+    // 8g + 2(l%4) and +1 of every 8-key group g.  The four lanes of a head
+    // pair reduce the row max with two shuffles; each lane keeps a partial
+    // row sum, reduced once at the end of the item.
     const int quad = warp & 3;
-    const int h = quad * 16 + lane;                    // head of this thread (lane < 16)
-    const bool is_head = lane < 16 && h < a.H;
+    const int l4 = lane & 3;
+    const int h0 = quad * 16 + (lane >> 2), h1 = h0 + 8;
+    const bool ok0 = h0 < a.H, ok1 = h1 < a.H;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const float c2 = a.sm_scale * 1.4426950408889634f;   // natural logits -> log2 units
     int64_t n = 0, e = 0;
@@ -302,28 +310,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* out_l = a.nsplit > 1 ? a.part_lse + (I.row * a.nsplit + I.split) * a.H
                                   : a.lse + I.row * a.H;
       if (I.nt == 0 || !ok) {                      // no keys (or stopped): empty result
-        if (is_head) {
-          float4* dst = reinterpret_cast<float4*>(out_o + h * kD);
-          for (int i = 0; i < kD / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-          out_l[h] = -INFINITY;
+#pragma unroll 4
+        for (int g = 0; g < kD / 8; ++g) {
+          const int col = 8 * g + 2 * l4;
+          if (ok0) *reinterpret_cast<float2*>(out_o + h0 * kD + col) = make_float2(0.f, 0.f);
+          if (ok1) *reinterpret_cast<float2*>(out_o + h1 * kD + col) = make_float2(0.f, 0.f);
         }
+        if (l4 == 0 && ok0) out_l[h0] = -INFINITY;
+        if (l4 == 0 && ok1) out_l[h1] = -INFINITY;
         continue;
       }
       const int ob = (int)(e & 1);
-      float m_run = -INFINITY, l_run = 0.f;
+      float m0 = -INFINITY, m1 = -INFINITY;        // running max (log2 units), per head
+      float l0 = 0.f, l1 = 0.f;                    // this lane's share of the running sums
       for (int t = 0; t < I.nt && ok; ++t, ++n) {
         const int sb = (int)(n & 1), pb = (int)(n & 1);
         ok = __all_sync(0xffffffffu, mbar_wait(&C.s_full[sb], (uint32_t)((n >> 1) & 1), a.err));
         if (!ok) break;
         tc_fence_after();
-        float v[64];
+        float v[32];                               // group g: h0 keys k, k+1; h1 keys k, k+1
         {
-          uint32_t r[64];
-          tmem_ld32_async(tmem + lane_base + sb * 64, r);
-          tmem_ld32_async(tmem + lane_base + sb * 64 + 32, r + 32);
+          uint32_t r[32];
+          tmem_ld16x256b_x8_async(tmem + lane_base + sb * 64, r);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
         }
         tc_fence_before();
         mbar_arrive(&C.s_empty[sb]);
@@ -335,24 +346,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int w_hi = (int)max64(0, min64(64, I.n_comp_pad + I.n_win - s0));
         auto ones = [](int k) -> uint64_t { return k >= 64 ? ~0ull : ((1ull << k) - 1ull); };
         const uint64_t real = ones(c_hi) | (ones(w_hi) & ~ones(w_lo));
-        float mraw = -INFINITY;                    // max of the raw logits (c2 > 0)
+        if (real != ~0ull || !ok0 || !ok1) {
+          const uint64_t rl = real >> (2 * l4);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          v[i] = ((real >> i) & 1ull) ? v[i] : -INFINITY;
-          mraw = fmaxf(mraw, v[i]);
-        }
-        const float mt = mraw * c2;
-        float alpha = 1.f;
-        bool need = false;
-        if (is_head && mt > m_run) {
-          if (m_run == -INFINITY) {
-            m_run = mt;                               // O of this item holds nothing yet
-          } else if (mt > m_run + kRescaleThreshold) {
-            alpha = fast_exp2(m_run - mt);
-            m_run = mt;
-            need = true;
+          for (int g = 0; g < 8; ++g) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const bool keep = (rl >> (8 * g + j)) & 1ull;
+              if (!keep || !ok0) v[4 * g + j] = -INFINITY;
+              if (!keep || !ok1) v[4 * g + 2 + j] = -INFINITY;
+            }
           }
         }
+        float x0 = -INFINITY, x1 = -INFINITY;      // max of the raw logits (c2 > 0)
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          x0 = fmaxf(x0, fmaxf(v[4 * g], v[4 * g + 1]));
+          x1 = fmaxf(x1, fmaxf(v[4 * g + 2], v[4 * g + 3]));
+        }
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 1));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 1));
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 2));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 2));
+        float al0 = 1.f, al1 = 1.f;
+        bool need = false;
+        auto raise = [&](float mt, float& m, float& al) {
+          if (mt > m) {
+            if (m == -INFINITY) {
+              m = mt;                               // O of this item holds nothing yet
+            } else if (mt > m + kRescaleThreshold) {
+              al = fast_exp2(m - mt);
+              m = mt;
+              need = true;
+            }
+          }
+        };
+        raise(x0 * c2, m0, al0);
+        raise(x1 * c2, m1, al1);
         if (__any_sync(0xffffffffu, need)) {
           // rescale O after PV(n-1), which signals p_empty of its P buffer (the
           // wait at tile n-1 already covered PV(n-3) on that barrier)
@@ -363,39 +393,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t tO = tmem + lane_base + 128 + ob * 128;
 #pragma unroll 1
           for (int c = 0; c < kD; c += 32) {
-            float o[32];
-            tmem_ld32(tO + c, o);
+            float o[16];
+            tmem_ld16x256b_x4(tO + c, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(tO + c, o);
+            for (int g = 0; g < 4; ++g) {
+              o[4 * g] *= al0;
+              o[4 * g + 1] *= al0;
+              o[4 * g + 2] *= al1;
+              o[4 * g + 3] *= al1;
+            }
+            tmem_st16x256b_x4(tO + c, o);
           }
           tmem_st_wait();
         }
-        l_run *= alpha;
+        l0 *= al0;
+        l1 *= al1;
         // P buffer pb is free once PV(n-2) is done
         ok = __all_sync(0xffffffffu,
                         mbar_wait(&C.p_empty[pb], (uint32_t)(((n >> 1) & 1) ^ 1), a.err));
         if (!ok) break;
-        if (lane < 16) {
-          unsigned char* prow = sP + pb * kPBytes;
-          const float mref = m_run == -INFINITY ? 0.f : m_run;
-          float psum = 0.f;
+        {
+          // exp2(c2 * v - m): masked keys (-inf) give +0; with nothing real
+          // so far m is -inf and every v is -inf
+          unsigned char* prow = sP + pb * kPBytes + 4 * l4;
+          const float r0 = m0 == -INFINITY ? 0.f : m0, r1 = m1 == -INFINITY ? 0.f : m1;
+          float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              // exp2(c2 * v - m): masked keys (-inf) give +0; with nothing real
-              // so far m is -inf and every v is -inf
-              const float p0 = is_head ? fast_exp2(fmaf(v[c * 8 + 2 * q], c2, -mref)) : 0.f;
-              const float p1 = is_head ? fast_exp2(fmaf(v[c * 8 + 2 * q + 1], c2, -mref)) : 0.f;
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-              psum += __low2float(h2) + __high2float(h2);
-              w4[q] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            *reinterpret_cast<uint4*>(prow + swz(h, c)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          for (int g = 0; g < 8; ++g) {
+            const __nv_bfloat162 p0 = __floats2bfloat162_rn(fast_exp2(fmaf(v[4 * g], c2, -r0)),
+                                                            fast_exp2(fmaf(v[4 * g + 1], c2, -r0)));
+            const __nv_bfloat162 p1 = __floats2bfloat162_rn(fast_exp2(fmaf(v[4 * g + 2], c2, -r1)),
+                                                            fast_exp2(fmaf(v[4 * g + 3], c2, -r1)));
+            s0 += __low2float(p0) + __high2float(p0);
+            s1 += __low2float(p1) + __high2float(p1);
+            *reinterpret_cast<__nv_bfloat162*>(prow + swz(h0, g)) = p0;
+            *reinterpret_cast<__nv_bfloat162*>(prow + swz(h1, g)) = p1;
           }
-          if (is_head) l_run += psum;
+          l0 += s0;
+          l1 += s1;
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -406,23 +441,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(&C.p_empty[(n - 1) & 1],
                                                (uint32_t)(((n - 1) >> 1) & 1), a.err));
       tc_fence_after();
-      const bool have = ok && l_run > 0.f;
-      const float inv = have ? 1.f / l_run : 0.f;
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+      const bool have0 = ok && l0 > 0.f, have1 = ok && l1 > 0.f;
+      const float inv0 = have0 ? 1.f / l0 : 0.f, inv1 = have1 ? 1.f / l1 : 0.f;
       const uint32_t tO = tmem + lane_base + 128 + ob * 128;
 #pragma unroll 1
       for (int c = 0; c < kD; c += 32) {
-        float o[32];
-        tmem_ld32(tO + c, o);
-        if (is_head) {
-          float4* dst = reinterpret_cast<float4*>(out_o + h * kD + c);
+        float o[16];
+        tmem_ld16x256b_x4(tO + c, o);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = have ? make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
-                                        o[4 * i + 3] * inv)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int g = 0; g < 4; ++g) {
+          const int col = c + 8 * g + 2 * l4;
+          if (ok0)
+            *reinterpret_cast<float2*>(out_o + h0 * kD + col) =
+                have0 ? make_float2(o[4 * g] * inv0, o[4 * g + 1] * inv0) : make_float2(0.f, 0.f);
+          if (ok1)
+            *reinterpret_cast<float2*>(out_o + h1 * kD + col) =
+                have1 ? make_float2(o[4 * g + 2] * inv1, o[4 * g + 3] * inv1)
+                      : make_float2(0.f, 0.f);
         }
       }
-      if (is_head) out_l[h] = have ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+      if (l4 == 0 && ok0) out_l[h0] = have0 ? (m0 + log2f(l0)) * 0.6931471805599453f : -INFINITY;
+      if (l4 == 0 && ok1) out_l[h1] = have1 ? (m1 + log2f(l1)) * 0.6931471805599453f : -INFINITY;
       tc_fence_before();
       mbar_arrive(&C.o_empty[ob]);
       ++e;

@@ -7,16 +7,15 @@
 // index and the output is in ascending index order (readings where the pages
 // are silent).
 //
-// Rows of up to 32768 candidates use topk_row_kernel (one CTA per row; a
-// sample threshold cuts the row to a short candidate list first, see there).
-// Longer rows: the row's candidates are split over a thread-block cluster of
+// Rows of up to 32768 candidates use topk_row_kernel (one CTA per row, keys
+// in registers, one histogram pass and an exact select inside one bin; see
+// there).  Longer rows: the row's candidates are split over a thread-block cluster of
 // C CTAs (C = 1 while the row fits one CTA's shared memory); CTA c keeps the order-
 // preserving 32-bit keys of candidates [c*chunk, (c+1)*chunk) in shared
 // memory.  Three radix passes (11, 11, 10 bits, most significant first) find
 // the exact k-th largest key T: each CTA histograms the keys that still match
-// the prefix chosen so far (lanes of a warp that hit the same bin add once,
-// through match.any), the C histograms are summed through distributed shared
-// memory, and every CTA picks the digit where the count of larger keys first
+// the prefix chosen so far (one shared-memory atomic per key), the C
+// histograms are summed through distributed shared memory, and every CTA picks the digit where the count of larger keys first
 // reaches the remaining quota.  Then every key > T is kept and, of the keys
 // == T, the lowest indices fill what is left of k.  The output position of
 // candidate i is (#keys > T before i) + min(#keys == T before i, quota), so
@@ -38,7 +37,11 @@ struct TopkSmem {
   int wgt[2 * kTopkWarps], weq[kTopkWarps];   // per-warp counts / min-max scratch
   __align__(8) int cnt[2];                // this CTA: keys > T, keys == T
   int nan_flag;
+  int wg[kTopkWarps], we[kTopkWarps];     // row kernel: per-warp keys > T, keys == T
+  int wc[kTopkWarps];                     // row kernel: per-warp keys in the selected bin
   int sel_bin, above;
+  int ncand, take;                        // row kernel: keys in the selected bin, ties kept
+  uint32_t T;                             // row kernel: the k-th largest key
 };
 
 __device__ __forceinline__ unsigned lanemask_lt() {
@@ -114,13 +117,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a, int C, i
       const int i = i0 + tid;
       const bool in = i < cnt;
       const uint32_t key = in ? keys[i] : 0u;
-      const bool match = in && (key & maskbits) == prefix;
-      const unsigned act = __ballot_sync(0xffffffffu, match);
-      if (match) {
-        const int bin = (int)((key >> shift) & (uint32_t)(nb - 1));
-        const unsigned same = __match_any_sync(act, bin);
-        if ((same & lanemask_lt()) == 0) atomicAdd(&h[bin], __popc(same));
-      }
+      if (in && (key & maskbits) == prefix) atomicAdd(&h[(key >> shift) & (uint32_t)(nb - 1)], 1);
     }
     __syncthreads();
     csync();
@@ -236,249 +233,252 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a, int C, i
 }
 
 // ------------------------------------------------------------------------
-// Rows of at most kRowMax candidates: one CTA per row, no cluster.
-//  1. keys -> shared memory; every 16th key is a sample;
-//  2. a threshold Ts low enough that about 1.3 k keys reach it, read off the
-//     samples (an order statistic of the sample, by the radix select below);
-//  3. the keys >= Ts are compacted, in index order, into a candidate list;
-//  4. the exact radix select runs on the candidates only: every key >= the
-//     k-th largest T is >= Ts, so the list holds all of them and all ties at T.
-// If the list comes out shorter than k or longer than its buffer (a skewed or
-// tied row), steps 3-4 fall back to the radix select over all the row's keys.
+// Rows of at most kRowMax candidates: one CTA of NT threads per row; the row's
+// keys sit in shared memory in index order.  Warp w owns candidates
+// [w*32*kKpl, (w+1)*32*kKpl) and reads them 32 at a time (candidate
+// w*32*kKpl + 32j + l in lane l, bank-conflict free), so a ballot over one j
+// lists keys in index order.  Three passes over the row:
+//  A. keys -> shared memory (16-byte loads) and a histogram of their top 13
+//     bits (sign, exponent, 4 mantissa bits: 8192 bins, one atomic per key);
+//     a scan of it gives the bin holding the k-th largest key;
+//  B. that bin's keys are gathered with their indices, and every warp counts
+//     its keys in higher bins; the exact k-th largest T comes from the bin's
+//     keys alone (rank counting for a few, radix passes over the 19 low bits
+//     otherwise; over the whole row if the bin overflows kCandMax);
+//  C. emission in index order: out[#(> T) before i + min(#(== T) before i, take)].
 constexpr int kRowMax = 32768;
-constexpr int kTopkSmemBytes = (sizeof(TopkSmem) + 15) & ~15;   // keys start 16-byte aligned
-constexpr int kCandMax = 8192;
-constexpr int kSampleStride = 16;
+constexpr int kKpl = 32;                                   // keys per thread
+constexpr int kTopkSmemBytes = (sizeof(TopkSmem) + 15) & ~15;
+constexpr int kFineShift = 19;                             // bin = key >> 19
+constexpr int kFineBins = 1 << (32 - kFineShift);          // 8192
+constexpr int kCandMax = 4096;                             // gathered keys of one bin
+constexpr int kRankMax = 256;
 
-// The kk-th largest of keys[0..m) (1 <= kk <= m), by three radix passes of
-// 11, 11 and 10 bits; *take = how many keys equal to it belong to the top kk.
-__device__ uint32_t radix_select(const uint32_t* keys, int m, int kk, TopkSmem& S, int* take) {
+// Over the histogram h[0..nb) (higher bin = larger keys): the bin b where the
+// count of keys in bins >= b first reaches krem (1 <= krem <= total), and the
+// count of keys in bins > b, to S.sel_bin / S.above.  Synchronises the CTA.
+template <int NT>
+__device__ void find_bin(const int* h, int nb, int krem, TopkSmem& S) {
+  constexpr int NW = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int per = (nb + NT - 1) / NT;            // bins per thread, highest first
+  int sum = 0;
+  for (int q = 0; q < per; ++q) {
+    const int b = nb - 1 - tid * per - q;
+    sum += b >= 0 ? h[b] : 0;
+  }
+  int x = sum;                                   // inclusive scan within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) S.scan[w] = x;
+  __syncthreads();
+  int wt = lane < NW ? S.scan[lane] : 0;         // warp totals, scanned by every warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, wt, o);
+    if (lane >= o) wt += y;
+  }
+  const int wbase = __shfl_sync(0xffffffffu, wt, (w + 31) & 31);
+  int base = (w > 0 ? wbase : 0) + x - sum;
+  for (int q = 0; q < per; ++q) {
+    const int b = nb - 1 - tid * per - q;
+    const int c = b >= 0 ? h[b] : 0;
+    if (c > 0 && base < krem && base + c >= krem) { S.sel_bin = b; S.above = base; }
+    base += c;
+  }
+  __syncthreads();
+}
+
+// The kk-th largest of those keys[0..m) whose top `top` bits equal prefix0's
+// (1 <= kk <= their count), by radix passes of up to 11 bits over the bits
+// below; *take = how many keys equal to it belong to the top kk.
+template <int NT>
+__device__ uint32_t radix_select(const uint32_t* keys, int m, int kk, TopkSmem& S, int* take,
+                                 int top, uint32_t prefix0) {
   const int tid = threadIdx.x;
-  uint32_t prefix = 0, maskbits = 0;
+  uint32_t prefix = prefix0, maskbits = top > 0 ? (~0u << (32 - top)) : 0u;
   int krem = kk;
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const int nb = pass == 2 ? 1024 : 2048;
-    int* h = S.hist[pass & 1];
-    for (int i = tid; i < nb; i += kTopkThreads) h[i] = 0;
+  int low = 32 - top;                            // bits still open
+  while (low > 0) {
+    const int nbits = min(11, low);
+    const int shift = low - nbits;
+    const int nb = 1 << nbits;
+    int* h = S.hist[1];
+    for (int i = tid; i < nb; i += NT) h[i] = 0;
     __syncthreads();
-    for (int i0 = 0; i0 < m; i0 += kTopkThreads) {
-      const int i = i0 + tid;
-      const bool in = i < m;
-      const uint32_t key = in ? keys[i] : 0u;
-      const bool match = in && (key & maskbits) == prefix;
-      const unsigned act = __ballot_sync(0xffffffffu, match);
-      if (match) {
-        const int bin = (int)((key >> shift) & (uint32_t)(nb - 1));
-        const unsigned same = __match_any_sync(act, bin);
-        if ((same & lanemask_lt()) == 0) atomicAdd(&h[bin], __popc(same));
-      }
+    for (int i = tid; i < m; i += NT) {
+      const uint32_t key = keys[i];
+      if ((key & maskbits) == prefix) atomicAdd(&h[(key >> shift) & (uint32_t)(nb - 1)], 1);
     }
     __syncthreads();
-    const int per = nb / kTopkThreads;
-    const int loc0 = h[nb - 1 - tid * per];
-    const int loc1 = per == 2 ? h[nb - 2 - tid * per] : 0;
-    const int base = block_exclusive_scan<kTopkThreads>(loc0 + loc1, S.scan, nullptr);
-    const int b0 = nb - 1 - tid * per;
-    if (base < krem && base + loc0 >= krem) { S.sel_bin = b0; S.above = base; }
-    if (per == 2) {
-      const int before = base + loc0;
-      if (before < krem && before + loc1 >= krem) { S.sel_bin = b0 - 1; S.above = before; }
-    }
-    __syncthreads();
+    find_bin<NT>(h, nb, krem, S);
     krem -= S.above;
     prefix |= (uint32_t)S.sel_bin << shift;
     maskbits |= (uint32_t)(nb - 1) << shift;
+    low = shift;
     __syncthreads();
   }
   *take = krem;
   return prefix;
 }
 
-// Rounds of the list passes: each thread takes kKpt consecutive entries.
-constexpr int kKpt = 8;
-constexpr int kRound = kKpt * kTopkThreads;
-
-// keys[ib .. ib+7] by two 16-byte shared loads (entries past m read as 0 and
-// are masked by the callers).  Lists are 16-byte aligned and padded to a
-// multiple of 8 entries, so a group that starts below m is in bounds.
-__device__ __forceinline__ void load8(const uint32_t* keys, int ib, int m, uint32_t* kk) {
-  if (ib < m) {
-    const uint4 u0 = *reinterpret_cast<const uint4*>(keys + ib);
-    const uint4 u1 = *reinterpret_cast<const uint4*>(keys + ib + 4);
-    kk[0] = u0.x; kk[1] = u0.y; kk[2] = u0.z; kk[3] = u0.w;
-    kk[4] = u1.x; kk[5] = u1.y; kk[6] = u1.z; kk[7] = u1.w;
-  } else {
-#pragma unroll
-    for (int j = 0; j < kKpt; ++j) kk[j] = 0u;
-  }
-}
-
-// Write, in list order, the entries with key > T and the first `take` with
-// key == T: out[p] = idx_of(i) for the p-th such entry.  The counts of a
-// thread's entries (key > T in the high half, key == T in the low half of one
-// int) are prefix-summed over the CTA once per round.
-template <typename IdxOf>
-__device__ void emit_selected(const uint32_t* keys, int m, uint32_t T, int take, TopkSmem& S,
-                              int32_t* out, IdxOf idx_of) {
-  const int tid = threadIdx.x;
-  int run_gt = 0, run_eq = 0;
-  for (int i0 = 0; i0 < m; i0 += kRound) {
-    const int ib = i0 + tid * kKpt;
-    uint32_t kk[kKpt];
-    int ng = 0, ne = 0;
-    load8(keys, ib, m, kk);
-#pragma unroll
-    for (int j = 0; j < kKpt; ++j) {
-      ng += ib + j < m && kk[j] > T;
-      ne += ib + j < m && kk[j] == T;
-    }
-    int tot;
-    const int pre = block_exclusive_scan<kTopkThreads>((ng << 16) | ne, S.scan, &tot);
-    int g_lt = run_gt + (pre >> 16), e_lt = run_eq + (pre & 0xFFFF);
-#pragma unroll
-    for (int j = 0; j < kKpt; ++j) {
-      if (ib + j >= m) break;
-      if (kk[j] > T) {
-        out[g_lt + min(e_lt, take)] = idx_of(ib + j);
-        ++g_lt;
-      } else if (kk[j] == T) {
-        if (e_lt < take) out[g_lt + e_lt] = idx_of(ib + j);
-        ++e_lt;
-      }
-    }
-    run_gt += tot >> 16;
-    run_eq += tot & 0xFFFF;
-  }
-}
-
-// Min and max of v over the CTA, returned to every thread.
-__device__ __forceinline__ void block_minmax(uint32_t lo, uint32_t hi, uint32_t* mn, uint32_t* mx,
-                                             int* scratch /* >= 2 * kTopkWarps */) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  uint32_t a = lo, b = hi;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
-    b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
-  }
-  if (lane == 0) { scratch[2 * w] = (int)a; scratch[2 * w + 1] = (int)b; }
-  __syncthreads();
-  a = lane < kTopkWarps ? (uint32_t)scratch[2 * lane] : 0xffffffffu;
-  b = lane < kTopkWarps ? (uint32_t)scratch[2 * lane + 1] : 0u;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    a = min(a, __shfl_xor_sync(0xffffffffu, a, o));
-    b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
-  }
-  __syncthreads();
-  *mn = a;
-  *mx = b;
-}
-
-// A key Ts such that at least r of keys[0..m) are >= Ts (1 <= r <= m), close
-// to the r-th largest: the lower edge of the linear bin (2048 bins over
-// [min, max]) that holds the r-th largest key.
-__device__ uint32_t threshold_at_least(const uint32_t* keys, int m, int r, TopkSmem& S) {
-  const int tid = threadIdx.x;
-  uint32_t lo = 0xffffffffu, hi = 0u;
-  for (int i = tid; i < m; i += kTopkThreads) { lo = min(lo, keys[i]); hi = max(hi, keys[i]); }
-  uint32_t kmin, kmax;
-  block_minmax(lo, hi, &kmin, &kmax, S.wgt);
-  const uint64_t span = (uint64_t)(kmax - kmin) + 1;
-  int* h = S.hist[0];
-  for (int i = tid; i < kBins; i += kTopkThreads) h[i] = 0;
-  __syncthreads();
-  for (int i = tid; i < m; i += kTopkThreads)
-    atomicAdd(&h[(int)(((uint64_t)(keys[i] - kmin) * kBins) / span)], 1);
-  __syncthreads();
-  const int loc0 = h[kBins - 1 - 2 * tid], loc1 = h[kBins - 2 - 2 * tid];
-  const int base = block_exclusive_scan<kTopkThreads>(loc0 + loc1, S.scan, nullptr);
-  if (base < r && base + loc0 >= r) S.sel_bin = kBins - 1 - 2 * tid;
-  else if (base + loc0 < r && base + loc0 + loc1 >= r) S.sel_bin = kBins - 2 - 2 * tid;
-  __syncthreads();
-  const uint64_t b = (uint64_t)S.sel_bin;
-  __syncthreads();
-  // smallest key whose bin is >= b
-  return kmin + (uint32_t)((b * span + kBins - 1) / kBins);
-}
-
-__global__ void __launch_bounds__(kTopkThreads) topk_row_kernel(TopkArgs a, int n_pad) {
+template <int NT>
+__global__ void __launch_bounds__(NT, 1) topk_row_kernel(TopkArgs a) {
+  constexpr int NW = NT / 32;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   TopkSmem& S = *reinterpret_cast<TopkSmem*>(smem_raw);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + kTopkSmemBytes);   // [n_pad]
-  uint32_t* samp = keys + n_pad;                                             // [n_pad / 16]
-  uint32_t* ck = samp + n_pad / kSampleStride;                               // [kCandMax]
+  int* hist = reinterpret_cast<int*>(smem_raw + kTopkSmemBytes);            // [kFineBins]
+  uint32_t* keys = reinterpret_cast<uint32_t*>(hist + kFineBins);            // [NT * kKpl]
+  uint32_t* ck = keys + NT * kKpl;                                           // [kCandMax]
   int32_t* ci = reinterpret_cast<int32_t*>(ck + kCandMax);                   // [kCandMax]
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int64_t row = blockIdx.x;
   const int k = a.k;
   int32_t* out = a.idx + row * k;
   const int p = __ldg(a.q_pos + row);
-  int n = p < 0 ? 0 : (int)min64(((int64_t)p + 1) / a.m, a.N_cap);
+  const int n = p < 0 ? 0 : (int)min64(((int64_t)p + 1) / a.m, a.N_cap);
   if (p >= 0 && ((int64_t)p + 1) / a.m > a.N_cap && tid == 0) set_err(a.err, SA_ERR_BOUNDS);
   if (n <= k) {
-    for (int i = tid; i < k; i += kTopkThreads) out[i] = i < n ? i : -1;
+    for (int i = tid; i < k; i += NT) out[i] = i < n ? i : -1;
     return;
   }
+  // ---- A. keys and the 13-bit histogram.  Thread tid holds the 16-byte
+  // groups tid + q*NT; slots past n get key 0, below every real score's key
+  // (score_key(-inf) > 0).
   const float* src = a.scores + row * a.ld;
-  int nan_local = 0;
-  int n4 = 0;
-  if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {       // 16-byte loads, four in flight
-    n4 = n / 4;
-    const float4* src4 = reinterpret_cast<const float4*>(src);
-    uint4* keys4 = reinterpret_cast<uint4*>(keys);
-#pragma unroll 4
-    for (int i = tid; i < n4; i += kTopkThreads) {
-      const float4 f = src4[i];
-      nan_local |= is_nan_bits(f.x) | is_nan_bits(f.y) | is_nan_bits(f.z) | is_nan_bits(f.w);
-      keys4[i] = make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
+  const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+  const int n4 = vec ? n / 4 : 0;                // whole 16-byte groups read as vectors
+  float4 f[kKpl / 4];
+#pragma unroll
+  for (int q = 0; q < kKpl / 4; ++q) {
+    const int g = tid + q * NT;
+    if (g < n4) {
+      f[q] = reinterpret_cast<const float4*>(src)[g];
+    } else {
+      const int i = 4 * g;
+      f[q] = make_float4(i < n ? src[i] : 0.f, i + 1 < n ? src[i + 1] : 0.f,
+                         i + 2 < n ? src[i + 2] : 0.f, i + 3 < n ? src[i + 3] : 0.f);
     }
   }
-  for (int i = 4 * n4 + tid; i < n; i += kTopkThreads) {
-    const float f = src[i];
-    nan_local |= is_nan_bits(f);
-    keys[i] = score_key(f);
+  for (int i = tid; i < kFineBins; i += NT) hist[i] = 0;      // while the loads fly
+  __syncthreads();
+  int nan_local = 0;
+  auto put = [&](int i, float v) -> uint32_t {
+    if (i >= n) return 0u;
+    nan_local |= is_nan_bits(v);
+    const uint32_t key = score_key(v);
+    atomicAdd(&hist[key >> kFineShift], 1);
+    return key;
+  };
+#pragma unroll
+  for (int q = 0; q < kKpl / 4; ++q) {
+    const int g = tid + q * NT;
+    reinterpret_cast<uint4*>(keys)[g] =
+        make_uint4(put(4 * g, f[q].x), put(4 * g + 1, f[q].y), put(4 * g + 2, f[q].z),
+                   put(4 * g + 3, f[q].w));
   }
   if (__syncthreads_or(nan_local)) {
     if (tid == 0) set_err(a.err, SA_ERR_NAN);
-    for (int i = tid; i < k; i += kTopkThreads) out[i] = -1;
+    for (int i = tid; i < k; i += NT) out[i] = -1;
     return;
   }
-  const int ns = (n + kSampleStride - 1) / kSampleStride;
-  for (int i = tid; i < ns; i += kTopkThreads) samp[i] = keys[i * kSampleStride];
+  find_bin<NT>(hist, kFineBins, k, S);
+  const uint32_t sel = (uint32_t)S.sel_bin;
+  const int r = k - S.above;                     // 1 <= r <= keys in bin sel
+  // ---- B. the bin's keys and indices; per-warp counts of keys above the bin
+  const unsigned lt = lanemask_lt();
+  const uint32_t* wkeys = keys + w * 32 * kKpl + lane;   // this lane's keys, stride 32
+  const int i0 = w * 32 * kKpl + lane;
+  int above_w = 0, in_w = 0;
+  uint32_t mine = 0;                             // bit j: this lane's slot j is in bin sel
+#pragma unroll 4
+  for (int j = 0; j < kKpl; ++j) {
+    const uint32_t key = wkeys[32 * j];
+    const uint32_t hb = key >> kFineShift;       // slots past n: key 0, never above sel
+    above_w += __popc(__ballot_sync(0xffffffffu, hb > sel));
+    const bool in = key != 0u && hb == sel;
+    in_w += __popc(__ballot_sync(0xffffffffu, in));
+    mine |= (uint32_t)in << j;
+  }
+  if (lane == 0) { S.wg[w] = above_w; S.we[w] = 0; S.wc[w] = in_w; }
   __syncthreads();
-  int rs = (int)(((int64_t)k * ns * 13 + (int64_t)n * 10 - 1) / ((int64_t)n * 10));   // ~1.3 k/16
-  rs = max(1, min(rs, ns));
-  const uint32_t Ts = threshold_at_least(samp, ns, rs, S);
-  // ---- candidates: keys >= Ts, in index order
-  int count = 0;
-  for (int i0 = 0; i0 < n; i0 += kRound) {
-    const int ib = i0 + tid * kKpt;
-    uint32_t kk[kKpt];
-    int nc = 0;
-    load8(keys, ib, n, kk);
+  int cw = lane < NW ? S.wc[lane] : 0;           // list offset of this warp's bin keys
 #pragma unroll
-    for (int j = 0; j < kKpt; ++j) nc += ib + j < n && kk[j] >= Ts;
-    int tot;
-    int pos = count + block_exclusive_scan<kTopkThreads>(nc, S.scan, &tot);
-#pragma unroll
-    for (int j = 0; j < kKpt; ++j) {
-      if (ib + j < n && kk[j] >= Ts) {
-        if (pos < kCandMax) { ck[pos] = kk[j]; ci[pos] = ib + j; }
-        ++pos;
-      }
-    }
-    count += tot;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, cw, o);
+    if (lane >= o) cw += y;
+  }
+  const int c = __shfl_sync(0xffffffffu, cw, 31);
+  int pos = w > 0 ? __shfl_sync(0xffffffffu, cw, w - 1) : 0;
+  for (int j = 0; j < kKpl && __any_sync(0xffffffffu, mine >> j); ++j) {
+    const bool in = (mine >> j) & 1u;
+    const unsigned b = __ballot_sync(0xffffffffu, in);
+    const int at = pos + __popc(b & lt);
+    if (in && at < kCandMax) { ck[at] = wkeys[32 * j]; ci[at] = i0 + 32 * j; }
+    pos += __popc(b);
   }
   __syncthreads();
+  uint32_t T;
   int take;
-  if (count >= k && count <= kCandMax) {
-    const uint32_t T = radix_select(ck, count, k, S, &take);
-    emit_selected(ck, count, T, take, S, out, [&](int i) { return ci[i]; });
-  } else {
-    const uint32_t T = radix_select(keys, n, k, S, &take);
-    emit_selected(keys, n, T, take, S, out, [&](int i) { return (int32_t)i; });
+  if (c <= kCandMax) {
+    if (c <= kRankMax) {
+      if (tid < c) {
+        const uint32_t x = ck[tid];
+        int gt = 0, eq = 0;
+        for (int i = 0; i < c; ++i) {
+          const uint32_t y = ck[i];
+          gt += y > x;
+          eq += y == x;
+        }
+        if (gt < r && r <= gt + eq) { S.T = x; S.take = r - gt; }   // equal x: equal writes
+      }
+      __syncthreads();
+      T = S.T;
+      take = S.take;
+    } else {
+      T = radix_select<NT>(ck, c, r, S, &take, 32 - kFineShift, sel << kFineShift);
+    }
+    for (int i = tid; i < c; i += NT) {          // the bin's share of the per-warp counts
+      const int wi = ci[i] / (32 * kKpl);
+      if (ck[i] > T) atomicAdd(&S.wg[wi], 1);
+      else if (ck[i] == T) atomicAdd(&S.we[wi], 1);
+    }
+    __syncthreads();
+  } else {                                       // the bin overflowed the list: whole row
+    T = radix_select<NT>(keys, NT * kKpl, k, S, &take, 0, 0u);
+    int g = 0, e = 0;
+#pragma unroll 4
+    for (int j = 0; j < kKpl; ++j) {
+      const uint32_t key = wkeys[32 * j];
+      g += __popc(__ballot_sync(0xffffffffu, key > T));
+      e += __popc(__ballot_sync(0xffffffffu, key == T));
+    }
+    if (lane == 0) { S.wg[w] = g; S.we[w] = e; }
+    __syncthreads();
+  }
+  // ---- C. emission in index order
+  int incl = lane < NW ? (S.wg[lane] << 16) | S.we[lane] : 0;   // each count <= 32*kKpl
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int excl = __shfl_sync(0xffffffffu, incl, (w + 31) & 31);
+  int g_run = w > 0 ? excl >> 16 : 0, e_run = w > 0 ? excl & 0xFFFF : 0;
+#pragma unroll 4
+  for (int j = 0; j < kKpl; ++j) {
+    const uint32_t key = wkeys[32 * j];
+    const bool is_gt = key > T, is_eq = key == T;
+    const unsigned bg = __ballot_sync(0xffffffffu, is_gt);
+    const unsigned be = __ballot_sync(0xffffffffu, is_eq);
+    const int gb = g_run + __popc(bg & lt), eb = e_run + __popc(be & lt);
+    if (is_gt) out[gb + min(eb, take)] = i0 + 32 * j;
+    else if (is_eq && eb < take) out[gb + eb] = i0 + 32 * j;
+    g_run += __popc(bg);
+    e_run += __popc(be);
   }
 }
 
@@ -487,14 +487,18 @@ bool topk_supported(int N_cap) { return N_cap <= kMaxChunk * kMaxCluster; }
 cudaError_t launch_topk(const TopkArgs& a, int num_sms, cudaStream_t st) {
   if (a.rows <= 0) return cudaSuccess;
   if (a.N_cap <= kRowMax) {
-    const int n_pad = (a.N_cap + 63) & ~63;   // keeps every list 16-byte aligned
-    const size_t smem = kTopkSmemBytes + sizeof(uint32_t) * (size_t)(n_pad + n_pad / kSampleStride) +
-                        (sizeof(uint32_t) + sizeof(int32_t)) * (size_t)kCandMax;
-    cudaError_t e = cudaFuncSetAttribute(topk_row_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    topk_row_kernel<<<(unsigned)a.rows, kTopkThreads, smem, st>>>(a, n_pad);
-    return cudaGetLastError();
+    auto go = [&](auto kern, int nt) -> cudaError_t {
+      const size_t smem = kTopkSmemBytes +
+                          sizeof(uint32_t) * ((size_t)kFineBins + (size_t)nt * kKpl + 2 * kCandMax);
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+      if (e != cudaSuccess) return e;
+      kern<<<(unsigned)a.rows, nt, smem, st>>>(a);
+      return cudaGetLastError();
+    };
+    if (a.N_cap <= 256 * kKpl) return go(topk_row_kernel<256>, 256);
+    if (a.N_cap <= 512 * kKpl) return go(topk_row_kernel<512>, 512);
+    return go(topk_row_kernel<1024>, 1024);
   }
   // Cluster size: a power of two, enough CTAs to hold N_cap keys in shared
   // memory, doubled while there are too few rows to cover the SMs and each

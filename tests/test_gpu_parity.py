@@ -222,13 +222,19 @@ def _topk_case(kind: str, rows: int, ncap: int, seed: int):
         s[:, ::5] = 1.0
     elif kind == "relu":
         s = np.maximum(g.standard_normal((rows, ncap)), 0).astype(np.float32)
+    elif kind == "wide":        # magnitudes over 60 decades, with infinities
+        s = (g.standard_normal((rows, ncap)) * 10.0 ** g.uniform(-30, 30, (rows, ncap)))
+        s = s.astype(np.float32)
+        s[:, 3::97] = np.inf
+        s[:, 5::89] = -np.inf
     else:
         s = g.standard_normal((rows, ncap)).astype(np.float32)
     return s
 
 
-@pytest.mark.parametrize("kind", ["random", "ties", "negzero", "relu"])
-@pytest.mark.parametrize("ncap,k", [(1024, 64), (32768, 2048), (262144, 2048), (5000, 4999)])
+@pytest.mark.parametrize("kind", ["random", "ties", "negzero", "relu", "wide"])
+@pytest.mark.parametrize("ncap,k", [(1024, 64), (32768, 2048), (262144, 2048), (5000, 4999),
+                                    (16384, 2048), (12000, 1000)])
 def test_topk_bit_exact_same_scores(kind, ncap, k):
     m = 4
     rows = 6
