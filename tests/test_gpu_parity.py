@@ -253,6 +253,24 @@ def test_topk_bit_exact_same_scores(kind, ncap, k):
     np.testing.assert_array_equal(host(idx), want)
 
 
+@pytest.mark.parametrize("kind", ["random", "ties", "wide"])
+def test_topk_bit_exact_many_long_rows(kind):
+    """More rows than fit one cluster per SM pair: one CTA per row of 20000."""
+    m, rows, ncap, k = 4, 100, 20000, 2048
+    s = _topk_case(kind, rows, ncap, 7)
+    nv = np.random.default_rng(8).integers(k - 5, ncap + 1, rows)
+    q_pos = (nv * m - 1).astype(np.int32)
+    idx = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sa().csa_index_topk(sa().SA_F32, rows, 1, 1, 1, m, k, None, None, None, None, None, ncap,
+                        dev(q_pos), idx, scores_in=dev(s), err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want, bad = oracle.topk(s.astype(np.float64), nv, k)
+    assert bad == 0
+    np.testing.assert_array_equal(host(idx), want)
+
+
 def test_topk_nan_row_rejected():
     rows, ncap, k = 3, 4096, 100
     s = np.random.default_rng(1).standard_normal((rows, ncap)).astype(np.float32)
