@@ -31,7 +31,7 @@
 //    TMEM lanes 32q..32q+15; the 16x256b load shape spreads those 16 rows
 //    over all 32 lanes (two heads and a quarter of the keys per lane), fp32
 //    exp2 of the scaled logits, P to shared memory in bf16; the running max
-//    is raised only when it grows by more than 8 (log2 units), and then O is
+//    is raised only when it grows by more than 32 (log2 units), and then O is
 //    rescaled in TMEM.
 //    At the end of an item it writes the normalised O and the LSE (or a
 //    normalised split partial, merged by merge_splits_kernel).
@@ -57,7 +57,7 @@ constexpr int kQBytes = kHeads * kD * 2;       // 16 KB: two 64-column halves
 constexpr int kStageBytes = 4 * kHalf;         // K (2 halves) + V (2 halves) = 32 KB
 constexpr int kPBytes = kHeads * kKeys * 2;    // 8 KB
 constexpr int kTmemCols = 512;                 // S: 2 x 64 at 0; O: 2 x 128 at 128
-constexpr float kRescaleThreshold = 8.f;       // log2 units
+constexpr float kRescaleThreshold = 32.f;      // log2 units: P <= 2^32, far inside fp32 and bf16
 
 struct Ctl {
   uint64_t full[kStages], empty[kStages];

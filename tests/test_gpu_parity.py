@@ -205,6 +205,23 @@ def test_decode_bf16_fewer_heads(H):
     run_staged(w, synth.make_inputs(w))
 
 
+def test_decode_bf16_logit_bands_force_rescales():
+    """Compressed key rows are scaled by 2^band over 8 bands of cache index, so
+    logits grow along every key list: an item whose tiles cross a band boundary
+    from band 4 up must raise its running max by more than the online softmax's
+    rescale threshold (32 log2 units) mid-item and rescale O.  The shape keeps
+    items several tiles long (16 rows, 34 CSA tiles and 65 HCA tiles per row)."""
+    w = synth.Workload("decB", "decode", B=16, L=65536, T=1, R=256, k=2048, W=128, m2=16)
+    x = synth.make_inputs(w)
+    for b in range(w.B):
+        for band in range(1, 8):
+            rows = np.arange(band * w.ncap // 8, (band + 1) * w.ncap // 8)
+            synth.scale_rows(x["k_c"][b], rows, float(2 ** band), w.dtype)
+            rows2 = np.arange(band * w.ncap2 // 8, (band + 1) * w.ncap2 // 8)
+            synth.scale_rows(x["hk_c"][b], rows2, float(2 ** band), w.dtype)
+    run_staged(w, x)
+
+
 def test_prefill_f32_multi_sequence_ragged():
     w = synth.Workload("pre32", "prefill", B=2, L=301, T=150, H=5, HI=3, dI=32, d=64, m=4, k=7,
                        W=9, m2=16, dtype="f32", indexer="f32")
