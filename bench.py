@@ -21,6 +21,7 @@ Prints one JSON line.  Multi-GPU (torchrun): every rank runs its own batch of
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -74,6 +75,36 @@ def recorded_traffic(kernel: str, files):
     except OSError:
         pass
     return None, "no ncu capture recorded"
+
+
+def graph_kernels(graph, cudart) -> list:
+    """Function names of the kernel nodes of a captured (not yet instantiated)
+    CUDA graph, read back through the runtime's graph API."""
+    ct = ctypes
+
+    class KernelNodeParams(ct.Structure):
+        _fields_ = [("func", ct.c_void_p), ("grid", ct.c_uint * 3), ("block", ct.c_uint * 3),
+                    ("smem", ct.c_uint), ("params", ct.c_void_p), ("extra", ct.c_void_p)]
+
+    n = ct.c_size_t(0)
+    if cudart.cudaGraphGetNodes(ct.c_void_p(graph), None, ct.byref(n)) != 0:
+        raise RuntimeError("cudaGraphGetNodes failed")
+    nodes = (ct.c_void_p * n.value)()
+    cudart.cudaGraphGetNodes(ct.c_void_p(graph), nodes, ct.byref(n))
+    names = []
+    for nd in nodes:
+        kind = ct.c_int(-1)
+        cudart.cudaGraphNodeGetType(ct.c_void_p(nd), ct.byref(kind))
+        if kind.value != 0:                      # cudaGraphNodeTypeKernel
+            continue
+        prm = KernelNodeParams()
+        name = ct.c_char_p()
+        if (cudart.cudaGraphKernelNodeGetParams(ct.c_void_p(nd), ct.byref(prm)) == 0 and
+                cudart.cudaFuncGetName(ct.byref(name), ct.c_void_p(prm.func)) == 0 and name.value):
+            names.append(name.value.decode(errors="replace"))
+        else:
+            names.append("?")
+    return names
 
 
 def algorithmic_bytes(w) -> dict:
@@ -313,17 +344,21 @@ def main() -> None:
     x = synth.make_inputs(w)
     step = make_step(w, x)
     io = StepIO(step, x, w)         # packs per-step inputs and outputs (before capture)
-    launches = step.kernel_launches()
     s_csa, s_hca = torch.cuda.Stream(), torch.cuda.Stream()
     main_s = torch.cuda.current_stream()
     # warm-up outside the graph (sets kernel attributes, loads modules)
     for _ in range(2):
         step.run_two_streams(s_csa, s_hca)
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
+    g = torch.cuda.CUDAGraph(keep_graph=True)
     cap = torch.cuda.Stream()
     with torch.cuda.graph(g, stream=cap):
         step.run_two_streams(s_csa, s_hca)
+    # the step's kernel launches: the captured graph's kernel nodes (the step
+    # issues only library calls and event edges, so every kernel node is ours)
+    kernels = graph_kernels(g.raw_cuda_graph(), io.cudart)
+    launches = len(kernels)
+    g.instantiate()
     torch.cuda.synchronize()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     sweep = torch.zeros(256 << 20, dtype=torch.uint8, device="cuda")
@@ -423,6 +458,7 @@ def main() -> None:
                          "avg_launch_ms": k_avg,
                          "algorithmic_bytes_per_launch": ab["index"]},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * args.steps,
+            "kernels_per_step": launches,
             "device_errors": errs, "clocks": clk.summary(),
         }), flush=True)
     if world > 1:

@@ -144,15 +144,5 @@ class HybridStep:
         cur.wait_event(e1)
         cur.wait_event(e2)
 
-    def kernel_launches(self) -> int:
-        """Kernels one ``run`` launches: compress, (MXFP4: query quantiser),
-        score, top-k, attend (+ split merge), HCA compress (if any block
-        closes), HCA attend (+ split merge)."""
-        D = self.D
-        n = (1 if D.max_blocks > 0 else 0) + 2 + 1 + (1 if self.ws_attend > 0 else 0)
-        n += 1 if D.indexer == "mxfp4" else 0
-        n += (1 if D.max_blocks2 > 0 else 0) + 1 + (1 if self.ws_hca > 0 else 0)
-        return n
-
     def device_errors(self) -> int:
         return int(self.err.item())

@@ -222,6 +222,18 @@ def test_decode_bf16_logit_bands_force_rescales():
     run_staged(w, x)
 
 
+def test_decode_bf16_one_row_many_splits():
+    """One query row: the HCA list (4375 rows + window, 71 tiles) is split one
+    tile per CTA, 71 partials merged by merge_splits_kernel in one row; the
+    staged check runs the CSA attention twice on one workspace.  Two runs
+    agree exactly."""
+    w = synth.Workload("dec1", "decode", B=1, L=70000, T=1, R=128, k=64, W=128, m2=16)
+    x = synth.make_inputs(w)
+    r1 = run_staged(w, x)
+    r2 = run_staged(w, x)
+    assert r1["o_err"] == r2["o_err"] and r1["ho_err"] == r2["ho_err"], (r1, r2)
+
+
 def test_prefill_f32_multi_sequence_ragged():
     w = synth.Workload("pre32", "prefill", B=2, L=301, T=150, H=5, HI=3, dI=32, d=64, m=4, k=7,
                        W=9, m2=16, dtype="f32", indexer="f32")
