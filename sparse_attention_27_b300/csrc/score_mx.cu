@@ -19,13 +19,18 @@
 // the nearest e4m3 value).
 //
 // Warp roles (448 threads): warp 0 = bulk-copy producer (raw codes + scales of
-// 128 entries per tile, 4352 bytes, into a ring of raw stages that the
-// converters and the epilogue both release), warp 1 = MMA issuer and TMEM owner,
-// warps 2..5 = converters (one entry row per thread: e2m1 -> e4m3 into a
-// 128B-swizzled K-major tile; they also convert each query group's B tile),
-// warps 6..13 = two epilogue warpgroups taking alternate tiles (weighted ReLU
-// head sum as in the bf16 kernel; each warp keeps its query weights, with the
-// row exponents folded in, in shared memory).
+// 128 entries per tile, 4352 bytes, into a ring of raw stages), warp 1 = MMA
+// issuer and TMEM owner, warps 2..9 = two converter warpgroups taking
+// alternate tiles (one entry row per thread: e2m1 -> e4m3 into a
+// 128B-swizzled K-major tile, the row's factor 2^(e_row) into a ring the
+// epilogue reads, so a raw stage is free as soon as it is converted; the
+// first group also converts each query group's B tile), warps 10..13 = the
+// epilogue (weighted ReLU head sum as in the bf16 kernel; each warp keeps its
+// query weights, with the row exponents folded in, in shared memory).
+// Conversion is the longest per-tile chain, so it gets two warpgroups.  Every
+// ring (16 raw stages, 4 A stages, 16 factor slots) has an even length: the
+// previous user of a tile's slot is the tile of the same parity, handled by
+// the same converter group, so each parity wait is at most one phase away.
 // Every wait is bounded; on a timeout the CTA records SA_ERR_DEVICE_TIMEOUT,
 // stops and still frees its TMEM.
 #include <cuda_fp8.h>
@@ -38,7 +43,8 @@ namespace sa {
 namespace {
 
 constexpr int kMxThreads = 448;
-constexpr int kMxEpiWarps = 8;     // two epilogue warpgroups
+constexpr int kMxConvWarps = 8;    // two converter warpgroups
+constexpr int kMxEpiWarps = 4;     // one epilogue warpgroup
 constexpr int kAStages = 4;
 constexpr int kCodeRowBytes = kIdxDim / 2;                       // 32
 constexpr int kScaleRowBytes = kIdxDim / 32;                     // 2
@@ -47,19 +53,24 @@ constexpr int kRawBytes = kTileEntries * (kCodeRowBytes + kScaleRowBytes);  // 4
 constexpr int kARowBytes = 128;                                  // swizzle row (64 used)
 constexpr int kABytes = kTileEntries * kARowBytes;               // 16 KB
 
+// Key-row factors 2^(e_row) pass from the converters to the epilogue through a
+// ring of kKsSlots tiles.  A converter is at most kAStages + kAccBufs (<= 8)
+// tiles ahead of the epilogue, so a slot is rewritten only after the epilogue
+// has read it.
+constexpr int kKsSlots = 16;
+
 template <int QG>
 struct MxCfg {
-  // raw stages are released by the converters and the epilogue, which trails
-  // the converters by up to kAStages + kAccBufs tiles
   static constexpr int kRawStages = QG == 1 ? 16 : 12;
   static constexpr int kAccCols = QG * kIdxHeads;
   static constexpr int kAccBufs = QG == 1 ? 4 : 2;
   static constexpr int kTmemCols = kAccBufs * kAccCols;          // 256 or 512
   static constexpr int kBBytes = QG * kIdxHeads * kARowBytes;    // 8 KB per query
   static constexpr size_t kWqBytes = kMxEpiWarps * QG * kIdxHeads * sizeof(float);
+  static constexpr size_t kKsBytes = kKsSlots * kTileEntries * sizeof(float);
   static constexpr size_t kSmem = 1024 + kAStages * kABytes + 2 * kBBytes +
                                   kRawStages * kRawBytes + 1024 /* LUT + barriers */ +
-                                  kMaxJobsPerCta * sizeof(JobRec<QG>) + kWqBytes;
+                                  kMaxJobsPerCta * sizeof(JobRec<QG>) + kWqBytes + kKsBytes;
 };
 
 struct MxPtrs {
@@ -164,10 +175,12 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
   uint64_t* b_empty = b_full + 2;
   uint64_t* t_full = b_empty + 2;
   uint64_t* t_empty = t_full + Cfg::kAccBufs;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(t_empty + Cfg::kAccBufs);
+  uint64_t* ks_full = t_empty + Cfg::kAccBufs;                     // [kKsSlots]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(ks_full + kKsSlots);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   JobRec<QG>* jobs = reinterpret_cast<JobRec<QG>*>(reinterpret_cast<unsigned char*>(lut) + 1024);
   float* s_wq = reinterpret_cast<float*>(jobs + kMaxJobsPerCta);   // [kMxEpiWarps][QG][64]
+  float* s_ks = s_wq + kMxEpiWarps * QG * kIdxHeads;                // [kKsSlots][128]
 
   const int n_my = fill_job_table<QG>(p, jobs);
   const int warp = (int)warp_id(), lane = (int)lane_id();
@@ -176,7 +189,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
     reinterpret_cast<uint8_t*>(lut)[s * 8 + c] = e4m3_of(c, s);
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kRawStages; ++s) { mbar_init(&raw_full[s], 1); mbar_init(&raw_empty[s], 256); }
+    for (int s = 0; s < kRawStages; ++s) { mbar_init(&raw_full[s], 1); mbar_init(&raw_empty[s], 128); }
+    for (int s = 0; s < kKsSlots; ++s) mbar_init(&ks_full[s], 128);
     for (int s = 0; s < kAStages; ++s) { mbar_init(&a_full[s], 128); mbar_init(&a_empty[s], 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(&b_full[s], 128); mbar_init(&b_empty[s], 1); }
     for (int s = 0; s < Cfg::kAccBufs; ++s) { mbar_init(&t_full[s], 1); mbar_init(&t_empty[s], 128); }
@@ -245,17 +259,18 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
       }
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 2 + kMxConvWarps) {
     // ---------------------------------------------------------- converters
-    const int c = (int)threadIdx.x - 64;        // entry row of the tile, 0..127
-    int rstage = 0, astage = 0, nsw = 0;
-    uint32_t rph = 0, aph = 0;
+    const int cgrp = (warp - 2) >> 2;           // converts the tiles with ordinal parity cgrp
+    const int c = ((int)threadIdx.x - 64) & 127;  // entry row of the tile, 0..127
+    int nsw = 0;
+    int64_t ko = 0;                             // tile ordinal: raw stage, A stage, factor slot
     int64_t prev_g = -1;
     for (int ji = 0; ji < n_my && !*s_abort; ++ji) {
       const JobRec<QG>& J = jobs[ji];
       if (J.t_lo >= J.t_hi) continue;
       bool stop = false;
-      if (J.g != prev_g) {
+      if (J.g != prev_g && cgrp == 0) {
         // the query group's B tile: QG*64 rows (query q, head h), zero past nq
         const int slot = nsw & 1;
         if (!mbar_wait(&b_empty[slot], ((nsw >> 1) & 1) ^ 1, p.err)) { *s_abort = 1; break; }
@@ -276,60 +291,63 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
         }
         fence_proxy_async_smem();
         mbar_arrive(&b_full[slot]);
-        prev_g = J.g;
         ++nsw;
       }
-      for (int t = J.t_lo; t < J.t_hi; ++t) {
+      prev_g = J.g;
+      for (int t = J.t_lo; t < J.t_hi; ++t, ++ko) {
+        if ((int)(ko & 1) != cgrp) continue;
+        const int rstage = (int)(ko % kRawStages), astage = (int)(ko % kAStages);
+        const uint32_t rph = (uint32_t)((ko / kRawStages) & 1), aph = (uint32_t)((ko / kAStages) & 1);
         if (!mbar_wait(&raw_full[rstage], rph, p.err)) { *s_abort = 1; stop = true; break; }
         const unsigned char* raw = sRaw + rstage * kRawBytes;
         const uint4 c0 = *reinterpret_cast<const uint4*>(raw + c * kCodeRowBytes);
         const uint4 c1 = *reinterpret_cast<const uint4*>(raw + c * kCodeRowBytes + 16);
         const uint32_t sc0 = raw[kRawCodeBytes + 2 * c], sc1 = raw[kRawCodeBytes + 2 * c + 1];
         mbar_arrive(&raw_empty[rstage]);
-        if (++rstage == kRawStages) { rstage = 0; rph ^= 1; }
         if (!mbar_wait(&a_empty[astage], aph ^ 1, p.err)) { *s_abort = 1; stop = true; break; }
-        convert_row(c0, c1, sc0, sc1, lut, sA + astage * kABytes, c);
+        const int er = convert_row(c0, c1, sc0, sc1, lut, sA + astage * kABytes, c);
         fence_proxy_async_smem();
         mbar_arrive(&a_full[astage]);
-        if (++astage == kAStages) { astage = 0; aph ^= 1; }
+        const int ks = (int)(ko % kKsSlots);
+        s_ks[ks * kTileEntries + c] = pow2i(er);
+        mbar_arrive(&ks_full[ks]);
       }
       if (stop) break;
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Two warpgroups take alternate tiles: tile ordinal o goes to group o % 2,
-    // accumulator o % kAccBufs.
-    const int grp = (warp - 6) >> 2;
+    // Tile ordinal o uses accumulator o % kAccBufs.
     const int quad = warp & 3;
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    float* wq = s_wq + (warp - 6) * QG * kIdxHeads;     // this warp's weights, per query
-    int64_t o = 0;                // tile ordinal (raw stage o % kRawStages)
+    float* wq = s_wq + (warp - 2 - kMxConvWarps) * QG * kIdxHeads;   // this warp's weights
+    int64_t o = 0;                // tile ordinal (factor slot o % kKsSlots)
+    int64_t wq_g = -1;            // query group whose weights are in wq
     for (int ji = 0; ji < n_my && !*s_abort; ++ji) {
       const JobRec<QG>& J = jobs[ji];
       if (J.t_lo >= J.t_hi) continue;
-      __syncwarp();                                      // previous job's weights are consumed
-      for (int q = 0; q < J.nq; ++q) store_wq(p, x, (int64_t)J.b * p.T + J.t0 + q, wq + q * kIdxHeads);
+      if (J.g != wq_g) {          // consecutive jobs of one group reuse its weights
+        __syncwarp();                                    // previous group's weights are consumed
+        for (int q = 0; q < J.nq; ++q)
+          store_wq(p, x, (int64_t)J.b * p.T + J.t0 + q, wq + q * kIdxHeads);
+        wq_g = J.g;
+      }
       bool stop = false;
       for (int t = J.t_lo; t < J.t_hi; ++t, ++o) {
-        if ((int)(o & 1) != grp) continue;
         const int acc = (int)(o % Cfg::kAccBufs);
         if (!mbar_wait(&t_full[acc], (uint32_t)((o / Cfg::kAccBufs) & 1), p.err)) {
           *s_abort = 1;
           stop = true;
           break;
         }
-        // this entry row's key scales, from the raw stage of tile o (held until
-        // the epilogue has read them)
-        const int rs = (int)(o % kRawStages);
-        if (!mbar_wait(&raw_full[rs], (uint32_t)((o / kRawStages) & 1), p.err)) {
+        // this entry row's factor 2^(e_row), from the converters' ring
+        const int ks = (int)(o % kKsSlots);
+        if (!mbar_wait(&ks_full[ks], (uint32_t)((o / kKsSlots) & 1), p.err)) {
           *s_abort = 1;
           stop = true;
           break;
         }
-        const unsigned char* rsc = sRaw + rs * kRawBytes + kRawCodeBytes + 2 * row_in_tile;
-        const float kscale = pow2i(max((int)rsc[0], (int)rsc[1]) - 127);
-        mbar_arrive(&raw_empty[rs]);
+        const float kscale = s_ks[ks * kTileEntries + row_in_tile];
         tc_fence_after();
         const int64_t j = (int64_t)t * kTileEntries + row_in_tile;
 #pragma unroll 1
