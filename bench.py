@@ -272,15 +272,32 @@ def cpu_baseline(w, x, seqs: int) -> dict:
     import numpy as np
     import oracle
     import synth
-    sub = synth.Workload(w.name, w.mode, B=seqs, L=w.L, T=w.T, R=w.R, k=w.k, x8=w.x8)
+    import dataclasses
+    sub = dataclasses.replace(w, B=seqs)
     xs = {k: (v[:seqs] if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == w.B else v)
           for k, v in x.items()}
     t0 = time.perf_counter()
     oracle.reference(sub, xs)
     dt = time.perf_counter() - t0
-    return {"value": seqs * sub.T / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{seqs} of {w.B} sequences of one {w.name} step (full CSA+HCA path, "
-                      f"float64, OpenMP over query rows), {dt:.2f} s"}
+    out = {"value": seqs * sub.T / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+           "sample": f"{seqs} of {w.B} sequences of one {w.name} step (full CSA+HCA path, "
+                     f"float64, OpenMP over query rows), {dt:.2f} s"}
+    # the same on one core, on a smaller sample (OpenMP of the loaded oracle)
+    try:
+        gomp = ctypes.CDLL("libgomp.so.1")
+        n1 = max(1, seqs // 16)
+        sub1 = dataclasses.replace(w, B=n1)
+        xs1 = {k: (v[:n1] if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == w.B
+                   else v) for k, v in x.items()}
+        gomp.omp_set_num_threads(1)
+        t0 = time.perf_counter()
+        oracle.reference(sub1, xs1)
+        dt1 = time.perf_counter() - t0
+        gomp.omp_set_num_threads(os.cpu_count())
+        out["one_core"] = {"value": n1 * sub1.T / dt1, "sample": f"{n1} sequences, {dt1:.2f} s"}
+    except OSError:
+        pass
+    return out
 
 
 def run_reference(args) -> None:
@@ -388,6 +405,8 @@ def main() -> None:
         dist.barrier()
     torch.cuda.synchronize()
     total_ms = sum(ms)
+    ms_sorted = sorted(ms)
+    pct = lambda q: ms_sorted[min(len(ms_sorted) - 1, int(q * len(ms_sorted)))]
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -458,6 +477,7 @@ def main() -> None:
                          "avg_launch_ms": k_avg,
                          "algorithmic_bytes_per_launch": ab["index"]},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * args.steps,
+            "step_ms": {"p10": pct(0.10), "median": statistics.median(ms), "p90": pct(0.90)},
             "kernels_per_step": launches,
             "device_errors": errs, "clocks": clk.summary(),
         }), flush=True)
