@@ -9,24 +9,27 @@
 // "EP 95. DeepSeek-V4 논문 읽기 — 노정석", section IDEAS (one shared KV head).
 //
 // Work: an item is (query row, split of the row's key list); a persistent grid
-// of at most one CTA per SM takes items c, c+G, ...  A row's key list is the
+// of at most two CTAs per SM takes items c, c+G, ...  Two resident CTAs give
+// each SM two independent pipelines (each CTA: two K/V stages, one Q tile,
+// 256 TMEM columns).  A row's key list is the
 // compressed part (rows idx[r, i] for CSA, rows 0.. for HCA), padded to a
 // multiple of 4 keys, then the window rows (ring slot u mod R); it is
 // processed in tiles of 64 keys.
 //
 // Warp roles (288 threads):
-//  * warps 0-3, producers: warp w issues the tiles with ordinal n = w (mod 4).
+//  * warps 0-3, producers: warp w < kProducers issues the tiles with ordinal
+//    n = w (mod kProducers) (warps past kProducers only wait).
 //    Lane l gathers keys 2l and 2l+1 -- sixteen 16-byte chunks of the K row
 //    and of the V row each, by cp.async, straight into the 128B-swizzled
 //    layout the tensor core reads (keys past the list are zero-filled) --
 //    waits for its copies, fences them to the async proxy and arrives on the
-//    stage's mbarrier, so four tiles are in flight per SM without coupling.
+//    stage's mbarrier, so two tiles are in flight per CTA (four per SM).
 //    Warp 0 also brings the item's 64 query heads by one TMA tiled load per
-//    64-column half into a double-buffered Q tile.
+//    64-column half into the Q tile.
 //  * warp 4, MMA: S(n) = Q . K(n)^T (M = 64 heads, N = 64 keys, K = 128) into
 //    one of two TMEM S buffers, issued before PV(n-1) so that the softmax of
 //    tile n overlaps the tensor core; O += P(n) . V(n) (M = 64, N = 128,
-//    K = 64) into one of two TMEM O buffers (one per item in flight).
+//    K = 64) into the TMEM O accumulator (freed by the softmax after each item).
 //  * warps 5-8, softmax: the M = 64 accumulator puts rows 16q..16q+15 in
 //    TMEM lanes 32q..32q+15; the 16x256b load shape spreads those 16 rows
 //    over all 32 lanes (two heads and a quarter of the keys per lane), fp32
@@ -49,22 +52,31 @@ namespace {
 
 constexpr int kThreads = 288;
 constexpr int kKeys = 64;                      // keys per tile
-constexpr int kStages = 5;
+constexpr int kCtasPerSm = 2;                  // two independent pipelines per SM
+constexpr int kStages = 2;                     // K/V tiles in flight per CTA
+// Producer warps 0 .. kProducers-1 issue tile n in warp n % kProducers.  A
+// producer's wait for stage n % kStages is sound by parity only while that
+// barrier is at most one phase behind: the warp's own previous tile n -
+// kProducers waited for the release of tile n - kProducers - kStages, which
+// covers tile n - 2 * kStages as long as kProducers <= kStages.
+constexpr int kProducers = kStages;
+constexpr int kQBufs = 1;                      // query tiles per CTA
+constexpr int kOBufs = 1;                      // TMEM O accumulators per CTA
 constexpr int kD = 128;                        // head dim
 constexpr int kHeads = 64;                     // MMA M
 constexpr int kHalf = kKeys * 128;             // 8 KB: a 64-dim half of a K or V tile
 constexpr int kQBytes = kHeads * kD * 2;       // 16 KB: two 64-column halves
 constexpr int kStageBytes = 4 * kHalf;         // K (2 halves) + V (2 halves) = 32 KB
 constexpr int kPBytes = kHeads * kKeys * 2;    // 8 KB
-constexpr int kTmemCols = 512;                 // S: 2 x 64 at 0; O: 2 x 128 at 128
+constexpr int kTmemCols = 256;                 // S: 2 x 64 at 0; O: 128 at 128 (half of TMEM)
 constexpr float kRescaleThreshold = 32.f;      // log2 units: P <= 2^32, far inside fp32 and bf16
 
 struct Ctl {
   uint64_t full[kStages], empty[kStages];
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[kQBufs], q_empty[kQBufs];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], p_empty[2];
-  uint64_t o_empty[2];
+  uint64_t o_empty[kOBufs];
   uint32_t tmem;
   int abort;
 };
@@ -119,14 +131,14 @@ __device__ __forceinline__ Item make_item(const AttnArgs& a, int64_t it) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     attend_tc_kernel(const __grid_constant__ TMaps tm, AttnArgs a) {
   extern __shared__ unsigned char smem_raw[];
   Ctl& C = *reinterpret_cast<Ctl*>(smem_raw);
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + sizeof(Ctl) + 1023) & ~uintptr_t(1023));
   unsigned char* sQ = base;                          // [2][kQBytes]
-  unsigned char* sKV = sQ + 2 * kQBytes;             // [kStages][kStageBytes]
+  unsigned char* sKV = sQ + kQBufs * kQBytes;        // [kStages][kStageBytes]
   unsigned char* sP = sKV + kStages * kStageBytes;   // [2][kPBytes]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -138,15 +150,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&C.full[s], 32);
       mbar_init(&C.empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kQBufs; ++s) {
       mbar_init(&C.q_full[s], 1);
       mbar_init(&C.q_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&C.s_full[s], 1);
       mbar_init(&C.s_empty[s], 128);
       mbar_init(&C.p_full[s], 128);
       mbar_init(&C.p_empty[s], 1);
-      mbar_init(&C.o_empty[s], 128);
     }
+    for (int s = 0; s < kOBufs; ++s) mbar_init(&C.o_empty[s], 128);
     C.abort = 0;
     mbar_fence_init();
   }
@@ -159,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     // ============================================================ producer
-    // warp w issues the tiles with ordinal n = w (mod 4): lane l gathers keys
+    // warp w issues the tiles with ordinal n = w (mod kProducers): lane l gathers keys
     // 2l and 2l+1 (16 chunks of K and 16 of V each), waits for its copies,
     // fences them to the async proxy and arrives on the stage's barrier.
     const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(a.kc);
@@ -172,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item I = make_item(a, it);
       if (I.nt == 0) continue;
       if (warp == 0) {            // the item's query heads, once the MMA warp has let go of the buffer
-        const int qb = (int)(e & 1);
-        if (!mbar_wait(&C.q_empty[qb], (uint32_t)(((e >> 1) & 1) ^ 1), a.err)) { ok = false; break; }
+        const int qb = (int)(e % kQBufs);
+        if (!mbar_wait(&C.q_empty[qb], (uint32_t)(((e / kQBufs) & 1) ^ 1), a.err)) { ok = false; break; }
         if (lane == 0) {
           mbar_arrive_expect_tx(&C.q_full[qb], kQBytes);
           const int32_t qrow = (int32_t)(I.row * a.H);
@@ -182,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       for (int t = 0; t < I.nt; ++t, ++n) {
-        if ((int)(n & 3) != warp) continue;
+        if ((int)(n % kProducers) != warp) continue;
         if (*abort_flag) { ok = false; break; }
         const int st = (int)(n % kStages);
         if (!mbar_wait(&C.empty[st], (uint32_t)(((n / kStages) & 1) ^ 1), a.err)) {
@@ -240,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pb = (int)(m & 1);
         if (!mbar_wait(&C.p_full[pb], (uint32_t)((m >> 1) & 1), a.err)) return false;
         if (t == 0 &&
-            !mbar_wait(&C.o_empty[ob], (uint32_t)(((e_item >> 1) & 1) ^ 1), a.err))
+            !mbar_wait(&C.o_empty[ob], (uint32_t)(((e_item / kOBufs) & 1) ^ 1), a.err))
           return false;
         tc_fence_after();
         const uint32_t pa = smem_u32(sP + pb * kPBytes);
@@ -258,9 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         const Item I = make_item(a, it);
         if (I.nt == 0) continue;
-        const int qb = (int)(e & 1), ob = (int)(e & 1);
+        const int qb = (int)(e % kQBufs), ob = (int)(e % kOBufs);
         const uint32_t qa = smem_u32(sQ + qb * kQBytes);
-        if (!mbar_wait(&C.q_full[qb], (uint32_t)((e >> 1) & 1), a.err)) { ok = false; break; }
+        if (!mbar_wait(&C.q_full[qb], (uint32_t)((e / kQBufs) & 1), a.err)) { ok = false; break; }
         for (int t = 0; t < I.nt; ++t, ++n) {
           if (*abort_flag) { ok = false; break; }
           const int st = (int)(n % kStages), sb = (int)(n & 1);
@@ -320,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (l4 == 0 && ok1) out_l[h1] = -INFINITY;
         continue;
       }
-      const int ob = (int)(e & 1);
+      const int ob = (int)(e % kOBufs);
       float m0 = -INFINITY, m1 = -INFINITY;        // running max (log2 units), per head
       float l0 = 0.f, l1 = 0.f;                    // this lane's share of the running sums
       for (int t = 0; t < I.nt && ok; ++t, ++n) {
@@ -517,7 +531,7 @@ bool attend_tc_supported(const AttnArgs& a) {
 int attend_tc_items_per_sm() { return 2; }
 
 static size_t attend_tc_smem() {
-  return sizeof(Ctl) + 1024 + 2 * kQBytes + kStages * kStageBytes + 2 * kPBytes;
+  return sizeof(Ctl) + 1024 + kQBufs * kQBytes + kStages * kStageBytes + 2 * kPBytes;
 }
 
 cudaError_t launch_attend_tc(const AttnArgs& a, int num_sms, cudaStream_t st) {
@@ -530,7 +544,7 @@ cudaError_t launch_attend_tc(const AttnArgs& a, int num_sms, cudaStream_t st) {
   cudaError_t e =
       cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int grid = (int)min64(num_sms, items);
+  const int grid = (int)min64((int64_t)kCtasPerSm * num_sms, items);
   attend_tc_kernel<<<grid, kThreads, smem, st>>>(tm, a);
   return cudaGetLastError();
 }
