@@ -378,7 +378,7 @@ def main() -> None:
     g.instantiate()
     torch.cuda.synchronize()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
-    sweep = torch.zeros(256 << 20, dtype=torch.uint8, device="cuda")
+    sweep = torch.zeros(64 << 20, dtype=torch.float32, device="cuda")   # 256 MiB, summed in place
 
     def timed(fn, n):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))

@@ -177,11 +177,11 @@ cudaError_t launch_attend_simt(const AttnArgs& a, cudaStream_t st) {
 // heads of one query row.  All threads first fetch the split LSEs into shared
 // memory at once (one memory round trip rather than nsplit dependent loads);
 // kMergeHeads threads turn them into weights exp(LSE_s - LSE); then each
-// thread issues up to kMergeBatch independent 16-byte partial loads before it
+// thread issues up to kMergeBatch (16) independent 16-byte partial loads before it
 // accumulates them.  Grid: (rows, ceil(H / kMergeHeads)).
 constexpr int kMergeThreads = 256;
 constexpr int kMergeHeads = 8;
-constexpr int kMergeBatch = 8;
+constexpr int kMergeBatch = 16;
 
 __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(
     const float* __restrict__ part_o, const float* __restrict__ part_lse, int nsplit, int H,
