@@ -190,18 +190,18 @@ class Clocks:
 class StepIO:
     """Host <-> device traffic of one decode step for the end-to-end figure.
 
-    The new token's inputs (q, q_hca, q_I, w, positions) live in one device
-    buffer filled by one copy from one pinned host buffer; its raw rows (ring
-    slot t mod R of the seven per-token arrays of both layers) are written by
-    one strided 2-D copy per array; the step's outputs (O and LSE of both
-    layers) live in one device buffer read back by one copy."""
+    Each layer's share of the new token's inputs (CSA: q, q_I, w; HCA: q_hca
+    and the positions both layers read) lives in one device buffer filled by
+    one copy from one pinned host buffer; the new raw rows (ring slot t mod R
+    of the layer's per-token arrays) are written by one strided 2-D copy per
+    array; each layer's outputs (O and LSE) live in one device buffer read
+    back by one copy.  Every copy is issued on its layer's stream."""
 
-    IN = ["q", "q_hca", "q_idx", "w_idx", "q_pos"]
-    RING = ["k_raw", "v_raw", "ik_raw", "z", "hk_raw", "hv_raw", "hz"]
-    OUT = ["o", "lse", "ho", "hlse"]
+    IN = {"csa": ["q", "q_idx", "w_idx"], "hca": ["q_hca", "q_pos"]}
+    RING = {"csa": ["k_raw", "v_raw", "ik_raw", "z"], "hca": ["hk_raw", "hv_raw", "hz"]}
+    OUT = {"csa": ["o", "lse"], "hca": ["ho", "hlse"]}
 
     def __init__(self, step, x, w):
-        import ctypes
         import numpy as np
         import torch
         dev = step.o.device
@@ -216,29 +216,34 @@ class StepIO:
                      for o, t in zip(offs, tensors)]
             return buf, views
 
-        ins = [step.x[n] for n in self.IN]
-        self.d_in, views = carve(ins)
-        for n, t, v in zip(self.IN, ins, views):
-            v.copy_(t)
-            step.x[n] = v
-        self.h_in = torch.empty(self.d_in.numel(), dtype=torch.uint8, pin_memory=True)
-        self.h_in.copy_(self.d_in.cpu())
-        outs = [getattr(step, n) for n in self.OUT]
-        self.d_out, views = carve(outs)
-        for n, v in zip(self.OUT, views):
-            setattr(step, n, v)
-        self.h_out = torch.empty(self.d_out.numel(), dtype=torch.uint8, pin_memory=True)
+        self.d_in, self.h_in, self.d_out, self.h_out, self.rings = {}, {}, {}, {}, {}
         slot = (w.L - 1) % w.ring
-        self.rings = []
-        for n in self.RING:
-            d = step.x[n]
-            row = d[0, 0].numel() * d.element_size()
-            h = torch.from_numpy(np.ascontiguousarray(x[n][:, slot]).view(np.uint8).reshape(-1)).pin_memory()
-            self.rings.append((d.data_ptr() + slot * row, d.stride(0) * d.element_size(), h, row,
-                               d.shape[0]))
-        self.h2d_bytes = self.d_in.numel() + sum(r[3] * r[4] for r in self.rings)
-        self.d2h_bytes = self.d_out.numel()
-        self.copies = 2 + len(self.rings)
+        for g in ("csa", "hca"):
+            ins = [step.x[n] for n in self.IN[g]]
+            self.d_in[g], views = carve(ins)
+            for n, t, v in zip(self.IN[g], ins, views):
+                v.copy_(t)
+                step.x[n] = v
+            self.h_in[g] = torch.empty(self.d_in[g].numel(), dtype=torch.uint8, pin_memory=True)
+            self.h_in[g].copy_(self.d_in[g].cpu())
+            outs = [getattr(step, n) for n in self.OUT[g]]
+            self.d_out[g], views = carve(outs)
+            for n, v in zip(self.OUT[g], views):
+                setattr(step, n, v)
+            self.h_out[g] = torch.empty(self.d_out[g].numel(), dtype=torch.uint8,
+                                        pin_memory=True)
+            self.rings[g] = []
+            for n in self.RING[g]:
+                d = step.x[n]
+                row = d[0, 0].numel() * d.element_size()
+                h = torch.from_numpy(np.ascontiguousarray(x[n][:, slot]).view(np.uint8)
+                                     .reshape(-1)).pin_memory()
+                self.rings[g].append((d.data_ptr() + slot * row, d.stride(0) * d.element_size(),
+                                      h, row, d.shape[0]))
+        self.h2d_bytes = sum(self.d_in[g].numel() + sum(r[3] * r[4] for r in self.rings[g])
+                             for g in ("csa", "hca"))
+        self.d2h_bytes = sum(self.d_out[g].numel() for g in ("csa", "hca"))
+        self.copies = sum(2 + len(self.rings[g]) for g in ("csa", "hca"))
         self.cudart = None
         for name in ("libcudart.so.13", "libcudart.so"):
             try:
@@ -248,23 +253,26 @@ class StepIO:
                 continue
         if self.cudart is None:
             raise RuntimeError("libcudart not found for the strided host-to-device copies")
-        self.ct = ctypes
 
-    def h2d(self):
+    def h2d(self, g, stream):
+        """Layer g's inputs, host to device, on ``stream``."""
         import torch
-        stream = torch.cuda.current_stream().cuda_stream
-        self.d_in.copy_(self.h_in, non_blocking=True)
-        ct = self.ct
-        for dst, pitch, h, row, nrows in self.rings:
+        with torch.cuda.stream(stream):
+            self.d_in[g].copy_(self.h_in[g], non_blocking=True)
+        ct = ctypes
+        for dst, pitch, h, row, nrows in self.rings[g]:
             rc = self.cudart.cudaMemcpy2DAsync(ct.c_void_p(dst), ct.c_size_t(pitch),
                                                ct.c_void_p(h.data_ptr()), ct.c_size_t(row),
                                                ct.c_size_t(row), ct.c_size_t(nrows), 1,
-                                               ct.c_void_p(stream))
+                                               ct.c_void_p(stream.cuda_stream))
             if rc != 0:
                 raise RuntimeError(f"cudaMemcpy2DAsync failed: {rc}")
 
-    def d2h(self):
-        self.h_out.copy_(self.d_out, non_blocking=True)
+    def d2h(self, g, stream):
+        """Layer g's outputs, device to host, on ``stream``."""
+        import torch
+        with torch.cuda.stream(stream):
+            self.h_out[g].copy_(self.d_out[g], non_blocking=True)
 
 
 def cpu_baseline(w, x, seqs: int) -> dict:
@@ -442,16 +450,40 @@ def main() -> None:
     # ---- end to end: host (pinned) inputs of the new token in, outputs out
     e2e = None
     if rank == 0 or world > 1:
-        def e2e_step():
-            io.h2d()
-            g.replay()
-            io.d2h()
+        def e2e_body():
+            # each layer: its inputs in, its kernels, its outputs out, on its own
+            # stream; the CSA layer also waits for the positions (HCA's copy)
+            cur = torch.cuda.current_stream()
+            fork = torch.cuda.Event()
+            fork.record(cur)
+            s_csa.wait_event(fork)
+            s_hca.wait_event(fork)
+            io.h2d("hca", s_hca)
+            pos_in = torch.cuda.Event()
+            pos_in.record(s_hca)
+            step.hca(s_hca)
+            io.d2h("hca", s_hca)
+            io.h2d("csa", s_csa)
+            s_csa.wait_event(pos_in)
+            step.csa(s_csa)
+            io.d2h("csa", s_csa)
+            e1, e2 = torch.cuda.Event(), torch.cuda.Event()
+            e1.record(s_csa)
+            e2.record(s_hca)
+            cur.wait_event(e1)
+            cur.wait_event(e2)
+        e2e_body()
+        torch.cuda.synchronize()
+        g_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_e2e, stream=cap):
+            e2e_body()
         for _ in range(3):
-            e2e_step()
-        e_ms = timed(e2e_step, args.steps)
+            g_e2e.replay()
+        e_ms = timed(g_e2e.replay, args.steps)
         e2e = {"value": world * w.B * w.T * args.steps / (sum(e_ms) / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": io.h2d_bytes, "d2h_bytes_per_step": io.d2h_bytes,
-               "copies_per_step": io.copies}
+               "copies_per_step": io.copies,
+               "note": "one graph per step: each layer's copies on its own stream"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
