@@ -77,6 +77,19 @@ def recorded_traffic(kernel: str, files):
     return None, "no ncu capture recorded"
 
 
+def max_over_ranks(v: float, device=None) -> float:
+    """The largest v over the ranks of the default process group (v itself
+    without one): the only collective of a multi-GPU run, which shards the
+    decode batch with no exchange on the data path."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def graph_kernels(graph, cudart) -> list:
     """Function names of the kernel nodes of a captured (not yet instantiated)
     CUDA graph, read back through the runtime's graph API."""
@@ -366,6 +379,9 @@ def main() -> None:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     w = synth.WORKLOADS[WORKLOAD]
+    if world > 1:                   # every rank decodes its own sequences (seeded by rank)
+        import dataclasses
+        w = dataclasses.replace(w, seed=rank)
     x = synth.make_inputs(w)
     step = make_step(w, x)
     io = StepIO(step, x, w)         # packs per-step inputs and outputs (before capture)
@@ -415,10 +431,7 @@ def main() -> None:
     total_ms = sum(ms)
     ms_sorted = sorted(ms)
     pct = lambda q: ms_sorted[min(len(ms_sorted) - 1, int(q * len(ms_sorted)))]
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, device="cuda")
     errs = step.device_errors()
     value = world * w.B * w.T * args.steps / (total_ms / 1e3)
 
@@ -480,7 +493,8 @@ def main() -> None:
         for _ in range(3):
             g_e2e.replay()
         e_ms = timed(g_e2e.replay, args.steps)
-        e2e = {"value": world * w.B * w.T * args.steps / (sum(e_ms) / 1e3), "unit": UNIT,
+        e_total = max_over_ranks(sum(e_ms), device="cuda")
+        e2e = {"value": world * w.B * w.T * args.steps / (e_total / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": io.h2d_bytes, "d2h_bytes_per_step": io.d2h_bytes,
                "copies_per_step": io.copies,
                "note": "one graph per step: each layer's copies on its own stream"}
