@@ -465,7 +465,10 @@ def main() -> None:
     if rank == 0 or world > 1:
         def e2e_body():
             # each layer: its inputs in, its kernels, its outputs out, on its own
-            # stream; the CSA layer also waits for the positions (HCA's copy)
+            # stream; the CSA layer also waits for the positions (HCA's copy).
+            # HCA starts at once here: its readback then overlaps the CSA chain
+            # (starting it after the CSA scores, as the device-only graph does,
+            # leaves both readbacks at the end of the step)
             cur = torch.cuda.current_stream()
             fork = torch.cuda.Event()
             fork.record(cur)
@@ -513,7 +516,7 @@ def main() -> None:
                        "head_dim": w.d, "m": w.m, "top_k": w.k, "window": w.W, "m2": w.m2,
                        "indexer_heads": w.HI, "parallelism": f"replicas x{world}",
                        "l2": "flushed before every timed step: a 512 MiB write, then a 256 MiB read",
-                       "graph": "one CUDA graph per step, CSA and HCA on two streams"},
+                       "graph": "one CUDA graph per step, CSA and HCA on two streams, HCA after the CSA scores"},
             "step_algorithmic_bytes": ab["step"], "step_gbs": step_gbs,
             "step_frac_of_hbm": step_gbs / peak,
             "roofline": {"kernel": "score_tc_kernel (csa_index_topk scores, k=0, one-node graph)",

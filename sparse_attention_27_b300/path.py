@@ -104,6 +104,25 @@ class HybridStep:
                        x["q_pos"], self.idx, scores_out=scores_out, scores_in=scores_in,
                        ws=self.ws_a, ws_bytes=self.ws_a.numel(), err=self.err, stream=stream)
 
+    def index_topk_split(self, stream, scored):
+        """index_topk as two calls on ``stream``: the indexer scores into the
+        workspace (top-k size 0), event ``scored``, then the top-k from those
+        scores -- the same two kernels, with a point in between that another
+        stream can wait for."""
+        D, x = self.D, self.x
+        sc = self.ws_a[: D.B * D.T * D.ncap * 4].view(torch.float32)
+        q, q_scales = x["q_idx"], None
+        if D.indexer == "mxfp4":
+            sa_mxfp4_quantize(x["q_idx"], self.q_codes, self.q_scales, stream=stream)
+            q, q_scales = self.q_codes, self.q_scales
+        csa_index_topk(_CODES[D.indexer], D.B, D.T, D.HI, D.dI, D.m, 0, q, q_scales, x["w_idx"],
+                       x["ik_c"], x.get("ik_c_scales"), D.ncap, x["q_pos"], None,
+                       scores_out=sc, err=self.err, stream=stream)
+        scored.record(stream)
+        csa_index_topk(_CODES[D.indexer], D.B, D.T, D.HI, D.dI, D.m, D.k, None, None, None, None,
+                       None, D.ncap, x["q_pos"], self.idx, scores_in=sc, err=self.err,
+                       stream=stream)
+
     def attend_csa(self, stream=None, idx=None):
         D, x = self.D, self.x
         csa_attend(_CODES[D.dtype], D.B, D.T, D.H, D.d, D.m, D.k, D.W, D.sm_scale, x["q"],
@@ -130,13 +149,20 @@ class HybridStep:
         self.hca(stream)
 
     def run_two_streams(self, s_csa: torch.cuda.Stream, s_hca: torch.cuda.Stream):
-        """The CSA and HCA layers on two streams (they share no buffer)."""
+        """The CSA and HCA layers on two streams (they share no buffer).  The
+        HCA layer starts once the CSA indexer's scores are written: the score
+        kernel, the step's largest HBM stream, then has the GPU to itself, and
+        HCA overlaps the top-k and the CSA attention."""
         cur = torch.cuda.current_stream()
         ev = torch.cuda.Event()
         ev.record(cur)
         s_csa.wait_event(ev)
         s_hca.wait_event(ev)
-        self.csa(s_csa)
+        self.compress_csa(s_csa)
+        scored = torch.cuda.Event()
+        self.index_topk_split(s_csa, scored)
+        self.attend_csa(s_csa)
+        s_hca.wait_event(scored)
         self.hca(s_hca)
         e1, e2 = torch.cuda.Event(), torch.cuda.Event()
         e1.record(s_csa)

@@ -363,6 +363,24 @@ def test_host_validation_rejects_bad_arguments():
                      x, x)
 
 
+def test_two_stream_schedule_matches_one_stream():
+    """HybridStep.run_two_streams (the bench's schedule: the indexer split into a
+    score call and a top-k call, the HCA layer on a second stream after the
+    scores) gives bit-identical outputs to HybridStep.run on one stream."""
+    w = synth.Workload("sched", "decode", B=8, L=20003, T=1, R=128, k=256, W=128, x8=True)
+    x = synth.make_inputs(w)
+    one = make_step(w, x)
+    one.run()
+    two = make_step(w, x)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    two.run_two_streams(s1, s2)
+    torch.cuda.synchronize()
+    assert one.device_errors() == 0 and two.device_errors() == 0
+    for name in ("idx", "o", "lse", "ho", "hlse"):
+        np.testing.assert_array_equal(host(getattr(two, name)), host(getattr(one, name)),
+                                      err_msg=name)
+
+
 # ----------------------------------------------------------- full-size cases
 
 def test_decode128k_full_size():
