@@ -61,17 +61,25 @@ def source_hash(files) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, files):
-    """(bytes per launch, capture note) from profiles/traffic.txt, or (None, why)."""
+def recorded_traffic(kernel: str, files, alg_bytes: int):
+    """(bytes per launch, capture note) from profiles/traffic.txt, or (None, why).
+
+    A capture of another workload of the same kernel is scaled to this one by
+    the algorithmic bytes the two launches move (the kernel reads each byte
+    once, so its traffic grows in proportion)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     cur = source_hash(files)
     try:
         for line in open(path):
             f = line.split()
-            if len(f) >= 3 and not line.startswith("#") and f[0] == kernel:
-                if f[1] == cur:
-                    return int(f[2]), " ".join(f[3:])
-                return None, "kernel changed since the ncu capture"
+            if len(f) >= 4 and not line.startswith("#") and f[0] == kernel:
+                if f[1] != cur:
+                    return None, "kernel changed since the ncu capture"
+                dram, cap_alg, note = int(f[2]), int(f[3]), " ".join(f[4:])
+                if cap_alg == alg_bytes:
+                    return dram, note
+                return (round(dram * alg_bytes / cap_alg),
+                        f"scaled by algorithmic bytes {alg_bytes}/{cap_alg} from: {note}")
     except OSError:
         pass
     return None, "no ncu capture recorded"
@@ -457,7 +465,7 @@ def main() -> None:
     ab = algorithmic_bytes(w)
     peak, peak_kind = peaks()
     achieved = ab["index"] / (k_avg / 1e3) / 1e9
-    traffic, traffic_note = recorded_traffic("score_tc_kernel", SCORE_SOURCES)
+    traffic, traffic_note = recorded_traffic("score_tc_kernel", SCORE_SOURCES, ab["index"])
     step_gbs = ab["step"] / (total_ms / args.steps / 1e3) / 1e9
 
     # ---- end to end: host (pinned) inputs of the new token in, outputs out
