@@ -82,14 +82,17 @@ __device__ __forceinline__ int fill_job_table(const ScoreJobs& p, JobRec<QG>* jo
 }
 
 // Host: choose the chunking (about 16 jobs per CTA, never more than the job
-// table holds) and the job order.  Returns the grid size, 0 if there is no
-// work, or -1 if the shape cannot be split into the job table.
-inline int plan_score_jobs(ScoreJobs& p, int QG, int num_sms) {
+// table holds; chunks a multiple of `step_tiles` where the shape allows, for
+// kernels that take that many tiles at a time) and the job order.  Returns the
+// grid size, 0 if there is no work, or -1 if the shape cannot be split into
+// the job table.
+inline int plan_score_jobs(ScoreJobs& p, int QG, int num_sms, int step_tiles = 1) {
   const int64_t ngroups = (int64_t)p.B * ((p.T + QG - 1) / QG);
   const int ntiles_max = (p.N_cap + kTileEntries - 1) / kTileEntries;
   if (ngroups == 0 || ntiles_max == 0) return 0;
   int64_t ct = (ngroups * ntiles_max) / (16LL * num_sms);
   if (ct < 1) ct = 1;
+  ct = (ct + step_tiles - 1) / step_tiles * step_tiles;
   if (ct > ntiles_max) ct = ntiles_max;
   while (ct < ntiles_max &&
          ngroups * ((ntiles_max + ct - 1) / ct) > (int64_t)kMaxJobsPerCta * num_sms)

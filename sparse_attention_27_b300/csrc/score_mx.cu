@@ -18,21 +18,30 @@
 // (rows whose blocks differ by more than 8 exponents round the small block to
 // the nearest e4m3 value).
 //
-// Warp roles (448 threads): warp 0 = bulk-copy producer (raw codes + scales of
-// 128 entries per tile, 4352 bytes, into a ring of raw stages), warp 1 = MMA
-// issuer and TMEM owner, warps 2..9 = two converter warpgroups taking
-// alternate tiles (one entry row per thread: e2m1 -> e4m3 into a
-// 128B-swizzled K-major tile, the row's factor 2^(e_row) into a ring the
-// epilogue reads, so a raw stage is free as soon as it is converted; the
-// first group also converts each query group's B tile), warps 10..13 = the
-// epilogue (weighted ReLU head sum as in the bf16 kernel; each warp keeps its
-// query weights, with the row exponents folded in, in shared memory).
-// Conversion is the longest per-tile chain, so it gets two warpgroups.  Every
-// ring (16 raw stages, 4 A stages, 16 factor slots) has an even length: the
-// previous user of a tile's slot is the tile of the same parity, handled by
-// the same converter group, so each parity wait is at most one phase away.
-// Every wait is bounded; on a timeout the CTA records SA_ERR_DEVICE_TIMEOUT,
-// stops and still frees its TMEM.
+// Work moves through the CTA in steps of kS consecutive 128-entry tiles of
+// one job (kS = 4 for one query per group, 1 for four): one bulk load, one A
+// stage, kS MMAs into one accumulator, one epilogue pass.  Every hand-off
+// between roles costs a barrier round trip, so at decode, where a tile is only
+// 4.3 KB of MXFP4, steps of four tiles spread those round trips over 17 KB
+// (measured: 45 -> 33 us at the 128K decode shape).
+//
+// Warp roles (448 threads): warp 0 = bulk-copy producer (raw codes + scales
+// of a step, 34 bytes per entry, into a ring of raw stages), warp 1 = MMA
+// issuer and TMEM owner, then 12 worker warps:
+//   converters -- one warpgroup at decode (a thread turns entry row c of each
+//     tile of the step from e2m1 into e4m3), two warpgroups at prefill (each
+//     takes one 32-element block of the row); the output is a K-major tile
+//     with 64-byte swizzled rows; the row's factor 2^(e_row) goes to the
+//     epilogue through a ring, so a raw stage is free as soon as it is
+//     converted; together they also convert each query group's B tile;
+//   epilogue -- two warpgroups at decode, taking alternate tiles of a step,
+//     one at prefill: one entry row per thread, weighted ReLU head sum as in
+//     the bf16 kernel; each warp keeps its query weights, with the row
+//     exponents folded in, in shared memory.
+// Every role takes the steps in order, so each ring slot's previous user is
+// the same role one lap earlier and every parity wait is at most one phase
+// away.  Every wait is bounded; on a timeout the CTA records
+// SA_ERR_DEVICE_TIMEOUT, stops and still frees its TMEM.
 #include <cuda_fp8.h>
 
 #include "kernels.cuh"
@@ -43,34 +52,44 @@ namespace sa {
 namespace {
 
 constexpr int kMxThreads = 448;
-constexpr int kMxConvWarps = 8;    // two converter warpgroups
-constexpr int kMxEpiWarps = 4;     // one epilogue warpgroup
-constexpr int kAStages = 4;
 constexpr int kCodeRowBytes = kIdxDim / 2;                       // 32
 constexpr int kScaleRowBytes = kIdxDim / 32;                     // 2
-constexpr int kRawCodeBytes = kTileEntries * kCodeRowBytes;      // 4096
-constexpr int kRawBytes = kTileEntries * (kCodeRowBytes + kScaleRowBytes);  // 4352
-constexpr int kARowBytes = 128;                                  // swizzle row (64 used)
-constexpr int kABytes = kTileEntries * kARowBytes;               // 16 KB
-
-// Key-row factors 2^(e_row) pass from the converters to the epilogue through a
-// ring of kKsSlots tiles.  A converter is at most kAStages + kAccBufs (<= 8)
-// tiles ahead of the epilogue, so a slot is rewritten only after the epilogue
-// has read it.
-constexpr int kKsSlots = 16;
+constexpr int kARowBytes = 64;                                   // A: 64B-swizzled rows
+constexpr int kABytes = kTileEntries * kARowBytes;               // 8 KB per tile
+constexpr int kBRowBytes = 128;                                  // B: 128B-swizzled (64 used)
 
 template <int QG>
 struct MxCfg {
-  static constexpr int kRawStages = QG == 1 ? 16 : 12;
-  static constexpr int kAccCols = QG * kIdxHeads;
-  static constexpr int kAccBufs = QG == 1 ? 4 : 2;
-  static constexpr int kTmemCols = kAccBufs * kAccCols;          // 256 or 512
-  static constexpr int kBBytes = QG * kIdxHeads * kARowBytes;    // 8 KB per query
-  static constexpr size_t kWqBytes = kMxEpiWarps * QG * kIdxHeads * sizeof(float);
-  static constexpr size_t kKsBytes = kKsSlots * kTileEntries * sizeof(float);
-  static constexpr size_t kSmem = 1024 + kAStages * kABytes + 2 * kBBytes +
-                                  kRawStages * kRawBytes + 1024 /* LUT + barriers */ +
+  static constexpr int kS = QG == 1 ? 4 : 1;                      // tiles per step
+  // 12 worker warps: converters (whole rows with one warpgroup, one block of
+  // each row per warpgroup with two) and epilogue warpgroups (each taking
+  // every kEpiGroups-th tile of a step)
+  static constexpr int kConvWarps = QG == 1 ? 4 : 8;
+  static constexpr int kEpiWarps = 12 - kConvWarps;
+  static constexpr int kStepEntries = kS * kTileEntries;
+  static constexpr int kRawCodeBytes = kStepEntries * kCodeRowBytes;
+  static constexpr int kRawBytes = kStepEntries * (kCodeRowBytes + kScaleRowBytes);
+  static constexpr int kRawStages = QG == 1 ? 6 : 12;
+  static constexpr int kAStages = QG == 1 ? 2 : 4;
+  static constexpr int kAStepBytes = kS * kABytes;
+  static constexpr int kAccCols = QG * kIdxHeads;                 // one tile's accumulator
+  static constexpr int kAccBufs = 2;
+  static constexpr int kTmemCols = kAccBufs * kS * kAccCols;      // 512
+  // Key-row factors 2^(e_row) pass from the converters to the epilogue through
+  // a ring of kKsSlots steps.  The converters reach step k only after the MMA
+  // of step k - kAStages, which waited for the epilogue to finish step
+  // k - kAStages - kAccBufs, so that many slots are never overwritten unread.
+  static constexpr int kKsSlots = kAStages + kAccBufs;
+  static constexpr int kBBytes = QG * kIdxHeads * kBRowBytes;    // 8 KB per query
+  static constexpr size_t kWqBytes = kEpiWarps * QG * kIdxHeads * sizeof(float);
+  static constexpr size_t kKsBytes = (size_t)kKsSlots * kStepEntries * sizeof(float);
+  static constexpr size_t kSmem = 1024 + (size_t)kAStages * kAStepBytes + 2 * kBBytes +
+                                  (size_t)kRawStages * kRawBytes + 1024 /* LUT + barriers */ +
                                   kMaxJobsPerCta * sizeof(JobRec<QG>) + kWqBytes + kKsBytes;
+  static_assert(kRawBytes % 16 == 0 && kRawCodeBytes % 16 == 0, "bulk copies need 16 B");
+  static_assert(kABytes % 512 == 0 && kBBytes % 1024 == 0, "swizzle atoms: 512 B (A), 1 KB (B)");
+  static_assert(kTmemCols <= 512, "TMEM");
+  static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 };
 
 struct MxPtrs {
@@ -79,6 +98,19 @@ struct MxPtrs {
   const uint8_t* k_codes;    // [B, N_cap, 32]
   const uint8_t* k_scales;   // [B, N_cap, 2]
 };
+
+// Shared-memory descriptor of a K-major operand with 64-byte swizzle: rows of
+// 64 bytes (K = 64 8-bit values), the 16-byte chunk c of row r stored at chunk
+// c ^ ((r >> 1) & 3), 8-row groups 512 B apart; the tile is 512-byte aligned.
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw64(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);        // start address
+  d |= (uint64_t)1u << 16;                        // leading byte offset (unused here)
+  d |= (uint64_t)(512u >> 4) << 32;               // stride byte offset: 8 rows * 64 B
+  d |= (uint64_t)1u << 46;                        // descriptor version (sm_100 family)
+  d |= (uint64_t)4u << 61;                        // swizzle: 64 B
+  return d;
+}
 
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
                                          uint64_t* bar) {
@@ -110,27 +142,40 @@ __device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lut_lo, uin
   return make_uint2(mag_lo | s_lo, mag_hi | s_hi);
 }
 
-// Convert one 64-element MXFP4 row (32 code bytes as two uint4, 2 scale bytes)
-// into 64 e4m3 bytes at row `r` of a 128B-swizzled tile; returns e_row.
-__device__ __forceinline__ int convert_row(uint4 c0, uint4 c1, uint32_t sc0, uint32_t sc1,
-                                           const uint32_t* lut, unsigned char* tile, int r) {
+// Convert block h (elements 32h..32h+31, code bytes 16h..16h+15) of one
+// 64-element MXFP4 row, given both of the row's scale bytes, into e4m3 bytes
+// 32h..32h+31 of row r of a K-major tile with kRowBytes-byte swizzled rows
+// (128: chunk c at c ^ (r & 7); 64: chunk c at c ^ ((r >> 1) & 3)); returns
+// e_row.
+template <int kRowBytes>
+__device__ __forceinline__ int convert_half(uint4 cw, uint32_t sc0, uint32_t sc1, int h,
+                                            const uint32_t* lut, unsigned char* tile, int r) {
   const int e0 = (int)sc0 - 127, e1 = (int)sc1 - 127;
   const int er = max(e0, e1);
-  const int s0 = min(er - e0, 15), s1 = min(er - e1, 15);
-  const uint32_t l0a = lut[2 * s0], l0b = lut[2 * s0 + 1];
-  const uint32_t l1a = lut[2 * s1], l1b = lut[2 * s1 + 1];
-  // block 0 = elements 0..31 = code bytes 0..15 = c0; block 1 = c1
-  const uint2 a0 = e2m1x8_to_e4m3(c0.x, l0a, l0b), a1 = e2m1x8_to_e4m3(c0.y, l0a, l0b);
-  const uint2 a2 = e2m1x8_to_e4m3(c0.z, l0a, l0b), a3 = e2m1x8_to_e4m3(c0.w, l0a, l0b);
-  const uint2 b0 = e2m1x8_to_e4m3(c1.x, l1a, l1b), b1 = e2m1x8_to_e4m3(c1.y, l1a, l1b);
-  const uint2 b2 = e2m1x8_to_e4m3(c1.z, l1a, l1b), b3 = e2m1x8_to_e4m3(c1.w, l1a, l1b);
-  unsigned char* row = tile + r * kARowBytes;
-  const int x = r & 7;
-  *reinterpret_cast<uint4*>(row + ((0 ^ x) << 4)) = make_uint4(a0.x, a0.y, a1.x, a1.y);
-  *reinterpret_cast<uint4*>(row + ((1 ^ x) << 4)) = make_uint4(a2.x, a2.y, a3.x, a3.y);
-  *reinterpret_cast<uint4*>(row + ((2 ^ x) << 4)) = make_uint4(b0.x, b0.y, b1.x, b1.y);
-  *reinterpret_cast<uint4*>(row + ((3 ^ x) << 4)) = make_uint4(b2.x, b2.y, b3.x, b3.y);
+  const int sh = min(er - (h ? e1 : e0), 15);
+  const uint32_t la = lut[2 * sh], lb = lut[2 * sh + 1];
+  const uint2 a0 = e2m1x8_to_e4m3(cw.x, la, lb), a1 = e2m1x8_to_e4m3(cw.y, la, lb);
+  const uint2 a2 = e2m1x8_to_e4m3(cw.z, la, lb), a3 = e2m1x8_to_e4m3(cw.w, la, lb);
+  unsigned char* row = tile + r * kRowBytes;
+  const int x = kRowBytes == 128 ? (r & 7) : ((r >> 1) & 3);
+  *reinterpret_cast<uint4*>(row + (((2 * h) ^ x) << 4)) = make_uint4(a0.x, a0.y, a1.x, a1.y);
+  *reinterpret_cast<uint4*>(row + (((2 * h + 1) ^ x) << 4)) = make_uint4(a2.x, a2.y, a3.x, a3.y);
   return er;
+}
+
+// sum_i w[i] * ReLU(v[i]) over 32 columns of fp32 accumulators.
+__device__ __forceinline__ float relu_dot32(const uint32_t* v, const float* w) {
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 wv = w4[i];
+    s0 = fmaf(wv.x, fmaxf(__uint_as_float(v[4 * i + 0]), 0.f), s0);
+    s1 = fmaf(wv.y, fmaxf(__uint_as_float(v[4 * i + 1]), 0.f), s1);
+    s2 = fmaf(wv.z, fmaxf(__uint_as_float(v[4 * i + 2]), 0.f), s2);
+    s3 = fmaf(wv.w, fmaxf(__uint_as_float(v[4 * i + 3]), 0.f), s3);
+  }
+  return (s0 + s1) + (s2 + s3);
 }
 
 __device__ __forceinline__ float pow2i(int e) {
@@ -158,14 +203,23 @@ __device__ __forceinline__ void store_wq(const ScoreJobs& p, const MxPtrs& x, in
 template <int QG>
 __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, MxPtrs x) {
   using Cfg = MxCfg<QG>;
+  constexpr int kS = Cfg::kS;
+  constexpr int kRawStages = Cfg::kRawStages;
+  constexpr int kAStages = Cfg::kAStages;
+  constexpr int kAccBufs = Cfg::kAccBufs;
+  constexpr int kKsSlots = Cfg::kKsSlots;
+  constexpr int kConvWarps = Cfg::kConvWarps;
+  constexpr int kConvThreads = 32 * kConvWarps;
+  constexpr int kEpiThreads = 32 * Cfg::kEpiWarps;
+  constexpr int kHalves = 8 / kConvWarps;                          // blocks per row per thread
+  constexpr int kEpiGroups = Cfg::kEpiWarps / 4;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* sA = smem;
-  unsigned char* sB = sA + kAStages * kABytes;
-  unsigned char* sRaw = sB + 2 * Cfg::kBBytes;
-  constexpr int kRawStages = Cfg::kRawStages;
-  uint32_t* lut = reinterpret_cast<uint32_t*>(sRaw + kRawStages * kRawBytes);   // [16][2]
+  unsigned char* sA = smem;                                        // [kAStages][kS][128][128]
+  unsigned char* sB = sA + kAStages * Cfg::kAStepBytes;            // [2][QG*64][128]
+  unsigned char* sRaw = sB + 2 * Cfg::kBBytes;                     // [kRawStages] codes, scales
+  uint32_t* lut = reinterpret_cast<uint32_t*>(sRaw + kRawStages * Cfg::kRawBytes);   // [16][2]
   uint64_t* bars = reinterpret_cast<uint64_t*>(lut + 32);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + kRawStages;
@@ -174,13 +228,13 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
   uint64_t* b_full = a_empty + kAStages;
   uint64_t* b_empty = b_full + 2;
   uint64_t* t_full = b_empty + 2;
-  uint64_t* t_empty = t_full + Cfg::kAccBufs;
-  uint64_t* ks_full = t_empty + Cfg::kAccBufs;                     // [kKsSlots]
+  uint64_t* t_empty = t_full + kAccBufs;
+  uint64_t* ks_full = t_empty + kAccBufs;                          // [kKsSlots]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(ks_full + kKsSlots);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   JobRec<QG>* jobs = reinterpret_cast<JobRec<QG>*>(reinterpret_cast<unsigned char*>(lut) + 1024);
-  float* s_wq = reinterpret_cast<float*>(jobs + kMaxJobsPerCta);   // [kMxEpiWarps][QG][64]
-  float* s_ks = s_wq + kMxEpiWarps * QG * kIdxHeads;                // [kKsSlots][128]
+  float* s_wq = reinterpret_cast<float*>(jobs + kMaxJobsPerCta);   // [kEpiWarps][QG][64]
+  float* s_ks = s_wq + Cfg::kEpiWarps * QG * kIdxHeads;             // [kKsSlots][kS*128]
 
   const int n_my = fill_job_table<QG>(p, jobs);
   const int warp = (int)warp_id(), lane = (int)lane_id();
@@ -189,11 +243,17 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
     reinterpret_cast<uint8_t*>(lut)[s * 8 + c] = e4m3_of(c, s);
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kRawStages; ++s) { mbar_init(&raw_full[s], 1); mbar_init(&raw_empty[s], 128); }
-    for (int s = 0; s < kKsSlots; ++s) mbar_init(&ks_full[s], 128);
-    for (int s = 0; s < kAStages; ++s) { mbar_init(&a_full[s], 128); mbar_init(&a_empty[s], 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(&b_full[s], 128); mbar_init(&b_empty[s], 1); }
-    for (int s = 0; s < Cfg::kAccBufs; ++s) { mbar_init(&t_full[s], 1); mbar_init(&t_empty[s], 128); }
+    for (int s = 0; s < kRawStages; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], kConvThreads);
+    }
+    for (int s = 0; s < kKsSlots; ++s) mbar_init(&ks_full[s], kConvThreads);
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(&a_full[s], kConvThreads);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) { mbar_init(&b_full[s], kConvThreads); mbar_init(&b_empty[s], 1); }
+    for (int s = 0; s < kAccBufs; ++s) { mbar_init(&t_full[s], 1); mbar_init(&t_empty[s], kEpiThreads); }
     *s_abort = 0;
     mbar_fence_init();
   }
@@ -203,6 +263,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
+  // Every role walks the same steps: job by job, kS tiles at a time (fewer
+  // at the end of a job).
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -210,15 +272,20 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
       uint32_t ph = 0;
       for (int ji = 0; ji < n_my && !*s_abort; ++ji) {
         const JobRec<QG>& J = jobs[ji];
-        for (int t = J.t_lo; t < J.t_hi; ++t) {
+        for (int t = J.t_lo; t < J.t_hi; t += kS) {
           if (!mbar_wait(&raw_empty[stage], ph ^ 1, p.err)) { *s_abort = 1; break; }
+          // the step's tiles are consecutive entries of sequence b; the last
+          // tile of a sequence may be partial (N_cap is a multiple of 8, so
+          // every copy stays a multiple of 16 bytes)
+          const int nsub = min(kS, J.t_hi - t);
           const int64_t e0 = (int64_t)J.b * p.N_cap + (int64_t)t * kTileEntries;
-          const uint32_t rows = (uint32_t)min64(kTileEntries, (int64_t)p.N_cap - (int64_t)t * kTileEntries);
-          unsigned char* dst = sRaw + stage * kRawBytes;
+          const uint32_t rows = (uint32_t)min64((int64_t)nsub * kTileEntries,
+                                                (int64_t)p.N_cap - (int64_t)t * kTileEntries);
+          unsigned char* dst = sRaw + stage * Cfg::kRawBytes;
           mbar_arrive_expect_tx(&raw_full[stage], rows * (kCodeRowBytes + kScaleRowBytes));
           bulk_g2s(dst, x.k_codes + e0 * kCodeRowBytes, rows * kCodeRowBytes, &raw_full[stage]);
-          bulk_g2s(dst + kRawCodeBytes, x.k_scales + e0 * kScaleRowBytes, rows * kScaleRowBytes,
-                   &raw_full[stage]);
+          bulk_g2s(dst + Cfg::kRawCodeBytes, x.k_scales + e0 * kScaleRowBytes,
+                   rows * kScaleRowBytes, &raw_full[stage]);
           if (++stage == kRawStages) { stage = 0; ph ^= 1; }
         }
       }
@@ -242,86 +309,119 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
           ++nsw;
         }
         const uint32_t b_base = smem_u32(sB + slot * Cfg::kBBytes);
-        for (int t = J.t_lo; t < J.t_hi; ++t) {
+        for (int t = J.t_lo; t < J.t_hi; t += kS) {
+          const int nsub = min(kS, J.t_hi - t);
           if (!mbar_wait(&a_full[stage], ph, p.err)) { *s_abort = 1; break; }
           if (!mbar_wait(&t_empty[acc], acc_ph ^ 1, p.err)) { *s_abort = 1; break; }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + stage * kABytes);
+          const uint32_t a_base = smem_u32(sA + stage * Cfg::kAStepBytes);
+          const uint32_t d_base = tmem + (uint32_t)(acc * kS * Cfg::kAccCols);
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk)          // K = 64 e4m3 = two MMAs of K = 32
-            tc_mma_f8f6f4(tmem + acc * Cfg::kAccCols, sdesc_kmajor_sw128(a_base + kk * 32),
-                          sdesc_kmajor_sw128(b_base + kk * 32), idesc, kk > 0 ? 1u : 0u);
+          for (int s = 0; s < kS; ++s) {
+            if (s >= nsub) break;
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)        // K = 64 e4m3 = two MMAs of K = 32
+              tc_mma_f8f6f4(d_base + (uint32_t)(s * Cfg::kAccCols),
+                            sdesc_kmajor_sw64(a_base + s * kABytes + kk * 32),
+                            sdesc_kmajor_sw128(b_base + kk * 32), idesc, kk > 0 ? 1u : 0u);
+          }
           tc_commit(&a_empty[stage]);
           tc_commit(&t_full[acc]);
           if (++stage == kAStages) { stage = 0; ph ^= 1; }
-          if (++acc == Cfg::kAccBufs) { acc = 0; acc_ph ^= 1; }
+          if (++acc == kAccBufs) { acc = 0; acc_ph ^= 1; }
         }
       }
     }
     __syncwarp();
-  } else if (warp < 2 + kMxConvWarps) {
+  } else if (warp < 2 + kConvWarps) {
     // ---------------------------------------------------------- converters
-    const int cgrp = (warp - 2) >> 2;           // converts the tiles with ordinal parity cgrp
-    const int c = ((int)threadIdx.x - 64) & 127;  // entry row of the tile, 0..127
+    const int tc = (int)threadIdx.x - 64;       // 0 .. kConvThreads - 1
+    const int c = tc & 127;                     // entry row within a tile
+    const int h0 = tc >> 7;                     // first block of the row taken: 32*h0 ..
     int nsw = 0;
-    int64_t ko = 0;                             // tile ordinal: raw stage, A stage, factor slot
+    int64_t k = 0;                              // step ordinal
     int64_t prev_g = -1;
     for (int ji = 0; ji < n_my && !*s_abort; ++ji) {
       const JobRec<QG>& J = jobs[ji];
       if (J.t_lo >= J.t_hi) continue;
       bool stop = false;
-      if (J.g != prev_g && cgrp == 0) {
-        // the query group's B tile: QG*64 rows (query q, head h), zero past nq
+      if (J.g != prev_g) {
+        // the query group's B tile: QG*64 rows (query q, head h), two blocks
+        // each, zero past nq
         const int slot = nsw & 1;
         if (!mbar_wait(&b_empty[slot], ((nsw >> 1) & 1) ^ 1, p.err)) { *s_abort = 1; break; }
         unsigned char* tile = sB + slot * Cfg::kBBytes;
-        for (int rr = c; rr < QG * kIdxHeads; rr += 128) {
+        for (int it = tc; it < QG * kIdxHeads * 2; it += kConvThreads) {
+          const int rr = it >> 1, hh = it & 1;
           const int q = rr / kIdxHeads;
           if (q < J.nq) {
             const int64_t qrow = ((int64_t)J.b * p.T + J.t0 + q) * kIdxHeads + (rr % kIdxHeads);
             const uint4* src = reinterpret_cast<const uint4*>(x.q_codes + qrow * kCodeRowBytes);
-            convert_row(__ldg(src), __ldg(src + 1), x.q_scales[qrow * 2], x.q_scales[qrow * 2 + 1],
-                        lut, tile, rr);
+            convert_half<kBRowBytes>(__ldg(src + hh), x.q_scales[qrow * 2],
+                                     x.q_scales[qrow * 2 + 1], hh, lut, tile, rr);
           } else {
-            unsigned char* row = tile + rr * kARowBytes;
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch)
-              *reinterpret_cast<uint4*>(row + ((ch ^ (rr & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+            unsigned char* row = tile + rr * kBRowBytes;
+            *reinterpret_cast<uint4*>(row + (((2 * hh) ^ (rr & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(row + (((2 * hh + 1) ^ (rr & 7)) << 4)) =
+                make_uint4(0, 0, 0, 0);
           }
         }
         fence_proxy_async_smem();
         mbar_arrive(&b_full[slot]);
         ++nsw;
+        prev_g = J.g;
       }
-      prev_g = J.g;
-      for (int t = J.t_lo; t < J.t_hi; ++t, ++ko) {
-        if ((int)(ko & 1) != cgrp) continue;
-        const int rstage = (int)(ko % kRawStages), astage = (int)(ko % kAStages);
-        const uint32_t rph = (uint32_t)((ko / kRawStages) & 1), aph = (uint32_t)((ko / kAStages) & 1);
+      for (int t = J.t_lo; t < J.t_hi; t += kS, ++k) {
+        const int nsub = min(kS, J.t_hi - t);
+        const int rstage = (int)(k % kRawStages), astage = (int)(k % kAStages);
+        const uint32_t rph = (uint32_t)((k / kRawStages) & 1), aph = (uint32_t)((k / kAStages) & 1);
         if (!mbar_wait(&raw_full[rstage], rph, p.err)) { *s_abort = 1; stop = true; break; }
-        const unsigned char* raw = sRaw + rstage * kRawBytes;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(raw + c * kCodeRowBytes);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(raw + c * kCodeRowBytes + 16);
-        const uint32_t sc0 = raw[kRawCodeBytes + 2 * c], sc1 = raw[kRawCodeBytes + 2 * c + 1];
+        // all of the step's loads first, then the stage is released
+        const unsigned char* raw = sRaw + rstage * Cfg::kRawBytes;
+        uint4 cw[kS][kHalves];
+        uint32_t sc0[kS], sc1[kS];
+#pragma unroll
+        for (int s = 0; s < kS; ++s) {
+          if (s < nsub) {
+            const int e = s * kTileEntries + c;
+#pragma unroll
+            for (int i = 0; i < kHalves; ++i)
+              cw[s][i] = *reinterpret_cast<const uint4*>(raw + e * kCodeRowBytes + (h0 + i) * 16);
+            sc0[s] = raw[Cfg::kRawCodeBytes + 2 * e];
+            sc1[s] = raw[Cfg::kRawCodeBytes + 2 * e + 1];
+          }
+        }
         mbar_arrive(&raw_empty[rstage]);
         if (!mbar_wait(&a_empty[astage], aph ^ 1, p.err)) { *s_abort = 1; stop = true; break; }
-        const int er = convert_row(c0, c1, sc0, sc1, lut, sA + astage * kABytes, c);
+        unsigned char* a = sA + astage * Cfg::kAStepBytes;
+        float* ksd = s_ks + (int)(k % kKsSlots) * Cfg::kStepEntries;
+#pragma unroll
+        for (int s = 0; s < kS; ++s) {
+          if (s < nsub) {
+            int er = 0;
+#pragma unroll
+            for (int i = 0; i < kHalves; ++i)
+              er = convert_half<kARowBytes>(cw[s][i], sc0[s], sc1[s], h0 + i, lut,
+                                            a + s * kABytes, c);
+            if (h0 == 0) ksd[s * kTileEntries + c] = pow2i(er);
+          }
+        }
         fence_proxy_async_smem();
         mbar_arrive(&a_full[astage]);
-        const int ks = (int)(ko % kKsSlots);
-        s_ks[ks * kTileEntries + c] = pow2i(er);
-        mbar_arrive(&ks_full[ks]);
+        mbar_arrive(&ks_full[(int)(k % kKsSlots)]);
       }
       if (stop) break;
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Tile ordinal o uses accumulator o % kAccBufs.
+    // Step ordinal k uses accumulator k % kAccBufs: kS tile accumulators of
+    // kAccCols columns each.
     const int quad = warp & 3;
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    float* wq = s_wq + (warp - 2 - kMxConvWarps) * QG * kIdxHeads;   // this warp's weights
-    int64_t o = 0;                // tile ordinal (factor slot o % kKsSlots)
+    const int eg = (warp - 2 - kConvWarps) >> 2;                   // epilogue warpgroup
+    float* wq = s_wq + (warp - 2 - kConvWarps) * QG * kIdxHeads;     // this warp's weights
+    int64_t k = 0;                // step ordinal (factor slot k % kKsSlots)
     int64_t wq_g = -1;            // query group whose weights are in wq
     for (int ji = 0; ji < n_my && !*s_abort; ++ji) {
       const JobRec<QG>& J = jobs[ji];
@@ -333,41 +433,38 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
         wq_g = J.g;
       }
       bool stop = false;
-      for (int t = J.t_lo; t < J.t_hi; ++t, ++o) {
-        const int acc = (int)(o % Cfg::kAccBufs);
-        if (!mbar_wait(&t_full[acc], (uint32_t)((o / Cfg::kAccBufs) & 1), p.err)) {
+      for (int t = J.t_lo; t < J.t_hi; t += kS, ++k) {
+        const int nsub = min(kS, J.t_hi - t);
+        const int acc = (int)(k % kAccBufs);
+        if (!mbar_wait(&t_full[acc], (uint32_t)((k / kAccBufs) & 1), p.err)) {
           *s_abort = 1;
           stop = true;
           break;
         }
-        // this entry row's factor 2^(e_row), from the converters' ring
-        const int ks = (int)(o % kKsSlots);
-        if (!mbar_wait(&ks_full[ks], (uint32_t)((o / kKsSlots) & 1), p.err)) {
+        // this thread's entry rows' factors 2^(e_row), from the converters' ring
+        const int ks = (int)(k % kKsSlots);
+        if (!mbar_wait(&ks_full[ks], (uint32_t)((k / kKsSlots) & 1), p.err)) {
           *s_abort = 1;
           stop = true;
           break;
         }
-        const float kscale = s_ks[ks * kTileEntries + row_in_tile];
         tc_fence_after();
-        const int64_t j = (int64_t)t * kTileEntries + row_in_tile;
 #pragma unroll 1
-        for (int q = 0; q < J.nq; ++q) {
-          const int64_t r = (int64_t)J.b * p.T + J.t0 + q;
-          uint32_t v[64];
-          tmem_ld32_async(tmem + lane_base + acc * Cfg::kAccCols + q * kIdxHeads, v);
-          tmem_ld32_async(tmem + lane_base + acc * Cfg::kAccCols + q * kIdxHeads + 32, v + 32);
-          tmem_wait_ld();
-          const float4* w4 = reinterpret_cast<const float4*>(wq + q * kIdxHeads);
-          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float4 wv = w4[i];
-            s0 = fmaf(wv.x, fmaxf(__uint_as_float(v[4 * i + 0]), 0.f), s0);
-            s1 = fmaf(wv.y, fmaxf(__uint_as_float(v[4 * i + 1]), 0.f), s1);
-            s2 = fmaf(wv.z, fmaxf(__uint_as_float(v[4 * i + 2]), 0.f), s2);
-            s3 = fmaf(wv.w, fmaxf(__uint_as_float(v[4 * i + 3]), 0.f), s3);
+        for (int s = eg; s < nsub; s += kEpiGroups) {
+          const float kscale = s_ks[ks * Cfg::kStepEntries + s * kTileEntries + row_in_tile];
+          const int64_t j = (int64_t)(t + s) * kTileEntries + row_in_tile;
+          const uint32_t col0 = (uint32_t)((acc * kS + s) * Cfg::kAccCols);
+#pragma unroll 1
+          for (int q = 0; q < J.nq; ++q) {
+            const int64_t r = (int64_t)J.b * p.T + J.t0 + q;
+            uint32_t v[64];
+            tmem_ld32_async(tmem + lane_base + col0 + q * kIdxHeads, v);
+            tmem_ld32_async(tmem + lane_base + col0 + q * kIdxHeads + 32, v + 32);
+            tmem_wait_ld();
+            const float d =
+                relu_dot32(v, wq + q * kIdxHeads) + relu_dot32(v + 32, wq + q * kIdxHeads + 32);
+            if (j < J.n[q]) p.scores[r * p.ld + j] = d * kscale;
           }
-          if (j < J.n[q]) p.scores[r * p.ld + j] = ((s0 + s1) + (s2 + s3)) * kscale;
         }
         tc_fence_before();
         mbar_arrive(&t_empty[acc]);
@@ -403,7 +500,7 @@ static cudaError_t launch_mx_qg(const ScoreArgs& a, int num_sms, cudaStream_t st
   p.scores = a.scores;
   p.ld = a.ld;
   p.err = a.err;
-  const int grid = plan_score_jobs(p, QG, num_sms);
+  const int grid = plan_score_jobs(p, QG, num_sms, Cfg::kS);
   if (grid == 0) return cudaSuccess;
   if (grid < 0) return cudaErrorInvalidValue;
   MxPtrs x{static_cast<const uint8_t*>(a.q), static_cast<const uint8_t*>(a.q_scales),

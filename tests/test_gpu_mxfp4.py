@@ -150,3 +150,32 @@ def test_mxfp4_indexer_scores_topk_recall(B, L, k):
     o_ref, _ = oracle.attend(x["q"].reshape(w.B, w.H, w.d), list(keys), list(vals), w.sm_scale)
     o = host(step.o).reshape(o_ref.shape)
     assert float(np.abs(o - o_ref).max()) <= 2e-2
+
+
+@pytest.mark.parametrize("B,L", [(2, 1184), (1, 4128)])
+def test_mxfp4_prefill_scores(B, L):
+    """The four-queries-per-group kernel (prefill): causal limits cut groups
+    and chunks mid-tile and the last tile is ragged (N_cap = 296 = 2 tiles + 40
+    rows; 1032 = 8 tiles + 8 rows).  Scores on the oracle's MXFP4 operands,
+    every fifth query row, against the oracle's double-precision scores of the
+    dequantised values."""
+    w = synth.Workload("mxpre", "prefill", B=B, L=L, T=L, k=64, W=128, indexer="mxfp4")
+    x = synth.make_inputs(w)
+    step = make_step(w, x)
+    step.compress_csa()
+    caches = oracle.compress_all(w, x)
+    kc_ref, ks_ref = oracle.mxfp4_quantize(caches["ik_c"])
+    step.x["ik_c"].copy_(dev(kc_ref))
+    step.x["ik_c_scales"].copy_(dev(ks_ref))
+    scores = torch.full((w.B, w.T, w.ncap), float("nan"), dtype=torch.float32, device="cuda")
+    step.index_topk(scores_out=scores)
+    torch.cuda.synchronize()
+    assert step.device_errors() == 0
+    rows = np.arange(0, w.B * w.T, 5)
+    ref = oracle.reference(w, x, rows=rows, caches=dict(caches, ik_c_mx=(kc_ref, ks_ref)))
+    s_gpu = host(scores).reshape(w.B * w.T, w.ncap)[rows]
+    vis = ref["nvis"] > 0
+    assert vis.sum() > 0.9 * len(rows)
+    err = _row_rel_err(s_gpu[vis], ref["scores"][vis], ref["nvis"][vis])
+    print(f"MXFP4 prefill score rel err {err:.3e}")
+    assert err <= TOL_SCORE_MX, err
