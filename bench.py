@@ -50,6 +50,8 @@ def peaks():
 # recorded with it (a changed kernel has no valid traffic figure).
 SCORE_SOURCES = ["sparse_attention_27_b300/csrc/score_tc.cu", "sparse_attention_27_b300/csrc/common.cuh",
                  "sparse_attention_27_b300/csrc/kernels.cuh"]
+MX_SOURCES = ["sparse_attention_27_b300/csrc/score_mx.cu", "sparse_attention_27_b300/csrc/common.cuh",
+              "sparse_attention_27_b300/csrc/kernels.cuh", "sparse_attention_27_b300/csrc/score_jobs.cuh"]
 
 
 def source_hash(files) -> str:
@@ -131,7 +133,11 @@ def graph_kernels(graph, cudart) -> list:
 def algorithmic_bytes(w) -> dict:
     """Minimum bytes one decode step must move (each needed row read once)."""
     e = 2  # bf16
-    per_seq_index = w.ncap * w.dI * e + w.HI * w.dI * e + w.HI * 4
+    if w.indexer == "mxfp4":        # e2m1 codes + one e8m0 scale per 32, keys and queries
+        row = w.dI // 2 + w.dI // 32
+        per_seq_index = w.ncap * row + w.HI * row + w.HI * 4
+    else:
+        per_seq_index = w.ncap * w.dI * e + w.HI * w.dI * e + w.HI * 4
     per_seq_csa = (per_seq_index + w.k * 2 * w.d * e + w.W * 2 * w.d * e + w.H * w.d * e
                    + w.k * 4 + w.H * w.d * 4 + w.H * 4)
     per_seq_hca = (w.ncap2 * 2 * w.d * e + w.W * 2 * w.d * e + w.H * w.d * e
@@ -362,8 +368,9 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default=WORKLOAD, choices=["decode128k", "decode1m"],
-                    help="decode at 128K (B=32, the default) or at 1M (B=4)")
+    ap.add_argument("--workload", default=WORKLOAD, choices=["decode128k", "decode1m", "mxfp4"],
+                    help="decode at 128K (B=32, the default), at 1M (B=4), or at 128K with "
+                         "the MXFP4 indexer")
     args = ap.parse_args()
     globals()["WORKLOAD"] = args.workload
     if args.impl == "reference":
@@ -448,10 +455,17 @@ def main() -> None:
     D = step.D
     sc = torch.empty((w.B, w.T, w.ncap), dtype=torch.float32, device="cuda")
 
+    mx = w.indexer == "mxfp4"
+
     def score_only():
-        sa.csa_index_topk(sa.SA_BF16, D.B, D.T, D.HI, D.dI, D.m, 0, step.x["q_idx"], None,
-                          step.x["w_idx"], step.x["ik_c"], None, D.ncap, step.x["q_pos"], None,
-                          scores_out=sc)
+        if mx:   # the step has already quantised this token's indexer queries
+            sa.csa_index_topk(sa.SA_MXFP4, D.B, D.T, D.HI, D.dI, D.m, 0, step.q_codes,
+                              step.q_scales, step.x["w_idx"], step.x["ik_c"],
+                              step.x["ik_c_scales"], D.ncap, step.x["q_pos"], None, scores_out=sc)
+        else:
+            sa.csa_index_topk(sa.SA_BF16, D.B, D.T, D.HI, D.dI, D.m, 0, step.x["q_idx"], None,
+                              step.x["w_idx"], step.x["ik_c"], None, D.ncap, step.x["q_pos"],
+                              None, scores_out=sc)
     for _ in range(3):
         score_only()
     torch.cuda.synchronize()
@@ -465,7 +479,9 @@ def main() -> None:
     ab = algorithmic_bytes(w)
     peak, peak_kind = peaks()
     achieved = ab["index"] / (k_avg / 1e3) / 1e9
-    traffic, traffic_note = recorded_traffic("score_tc_kernel", SCORE_SOURCES, ab["index"])
+    score_kernel = "score_mx_kernel" if mx else "score_tc_kernel"
+    traffic, traffic_note = recorded_traffic(score_kernel, MX_SOURCES if mx else SCORE_SOURCES,
+                                             ab["index"])
     step_gbs = ab["step"] / (total_ms / args.steps / 1e3) / 1e9
 
     # ---- end to end: host (pinned) inputs of the new token in, outputs out
@@ -522,12 +538,13 @@ def main() -> None:
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "batch": w.B, "context": w.L, "heads": w.H,
                        "head_dim": w.d, "m": w.m, "top_k": w.k, "window": w.W, "m2": w.m2,
-                       "indexer_heads": w.HI, "parallelism": f"replicas x{world}",
+                       "indexer_heads": w.HI, "indexer": w.indexer,
+                       "parallelism": f"replicas x{world}",
                        "l2": "flushed before every timed step: a 512 MiB write, then a 256 MiB read",
                        "graph": "one CUDA graph per step, CSA and HCA on two streams, HCA after the CSA scores"},
             "step_algorithmic_bytes": ab["step"], "step_gbs": step_gbs,
             "step_frac_of_hbm": step_gbs / peak,
-            "roofline": {"kernel": "score_tc_kernel (csa_index_topk scores, k=0, one-node graph)",
+            "roofline": {"kernel": f"{score_kernel} (csa_index_topk scores, k=0, one-node graph)",
                          "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
                          "traffic": traffic, "traffic_source": traffic_note,
