@@ -318,3 +318,22 @@ def test_mxfp4_error_bound():
     spacing = np.where(u < 2, 0.5, np.where(u < 4, 1.0, 2.0))
     err = np.abs(x - y) / np.exp2(e)
     assert np.all(err <= np.maximum(spacing / 2, u - 6) + 1e-12)
+
+
+def test_mxfp4_row_exponent_spread_of_the_128k_draws():
+    """The MXFP4 kernel folds each block's scale into e4m3 as 2^(e_b - e_row),
+    e_row the larger of the row's two block exponents; that is exact while
+    e_row - e_b <= 8 (e4m3's smallest subnormal is 2^-9).  On the 128K decode
+    workload's own indexer draws (keys and queries; the x8 rows scale a whole
+    row and leave the spread unchanged) no row is beyond that, so the kernel's
+    only rounding there is its fp32 accumulation."""
+    w = synth.WORKLOADS["mxfp4"]
+    worst = 0
+    for name, shape in (("ik_c", (w.B, w.ncap, w.dI)), ("q_idx", (w.B, w.T, w.HI, w.dI))):
+        x = synth.normal(w.seed, name, shape, "bf16").reshape(-1, 2048, w.dI)
+        for chunk in x:
+            _, scales = oracle.mxfp4_quantize(chunk)
+            e = scales.astype(int).reshape(-1, w.dI // 32)
+            worst = max(worst, int((e.max(axis=1) - e.min(axis=1)).max()))
+    print(f"largest block-exponent spread within a row: {worst}")
+    assert worst <= 8
