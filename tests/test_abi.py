@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -52,3 +53,26 @@ def test_workspace_queries_are_host_only():
     import sparse_attention_27_b300 as m
     assert m.csa_index_topk_workspace_bytes(32, 1, 32768, 2048) == 32 * 32768 * 4
     assert m.csa_index_topk_workspace_bytes(0, 1, 10, 1) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(),
+                    reason="stand-in pointers: run only where no kernel can be launched")
+def test_mxfp4_index_host_validation():
+    """The MXFP4 scoring path's limits are checked on the host, before any
+    launch: N_cap a multiple of 8 (every bulk copy of scales a multiple of 16
+    bytes), both scale arrays given, 64 heads of width 64, 16-byte aligned
+    operands.  Stand-in pointer values (16-byte aligned integers) are never
+    dereferenced on these paths."""
+    import sparse_attention_27_b300 as m
+    P = 1 << 20                       # aligned stand-in address
+
+    def call(N_cap=4096, HI=64, dI=64, q=P, qs=P, ik=P, iks=P):
+        return m.library().csa_index_topk(m.SA_MXFP4, 2, 1, HI, dI, 4, 0, q, qs, P, ik, iks,
+                                          N_cap, P, None, P, None, None, 0, None, None)
+    assert call(N_cap=4100) == m.SA_ERR_UNSUPPORTED         # not a multiple of 8
+    assert call(qs=None) == m.SA_ERR_UNSUPPORTED            # query scales missing
+    assert call(iks=None) == m.SA_ERR_UNSUPPORTED           # key scales missing
+    assert call(HI=32) == m.SA_ERR_UNSUPPORTED
+    assert call(dI=128) == m.SA_ERR_UNSUPPORTED
+    assert call(q=P + 8) == m.SA_ERR_INVALID_ARG            # codes not 16-byte aligned
+    assert call(ik=None) == m.SA_ERR_INVALID_ARG
