@@ -130,16 +130,15 @@ __device__ __forceinline__ uint8_t e4m3_of(int c, int s) {
 
 // Eight e2m1 codes (one 32-bit word, element 2i in the low nibble of byte i)
 // -> eight e4m3 bytes, using an 8-entry magnitude table (lut_lo: codes 0-3,
-// lut_hi: codes 4-7) for the block's shift and the code's sign bit.
+// lut_hi: codes 4-7; every byte's top bit clear) for the block's shift.  The
+// code's sign bit (bit 3 of its nibble) becomes a byte-permute selector, 0 or
+// 4, into (0x00000000, 0x80808080): the e4m3 sign bit of that output byte.
 __device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lut_lo, uint32_t lut_hi) {
   const uint32_t mag_lo = __byte_perm(lut_lo, lut_hi, w & 0x7777u);
   const uint32_t mag_hi = __byte_perm(lut_lo, lut_hi, (w >> 16) & 0x7777u);
-  const uint32_t sg = w & 0x88888888u;
-  const uint32_t s_lo = ((sg & 0x8u) << 4) | ((sg & 0x80u) << 8) | ((sg & 0x800u) << 12) |
-                        ((sg & 0x8000u) << 16);
-  const uint32_t s_hi = ((sg >> 12) & 0x80u) | ((sg >> 8) & 0x8000u) | ((sg >> 4) & 0x800000u) |
-                        (sg & 0x80000000u);
-  return make_uint2(mag_lo | s_lo, mag_hi | s_hi);
+  const uint32_t sg_lo = __byte_perm(0u, 0x80808080u, (w >> 1) & 0x4444u);
+  const uint32_t sg_hi = __byte_perm(0u, 0x80808080u, (w >> 17) & 0x4444u);
+  return make_uint2(mag_lo | sg_lo, mag_hi | sg_hi);
 }
 
 // Convert block h (elements 32h..32h+31, code bytes 16h..16h+15) of one
