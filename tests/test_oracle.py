@@ -337,3 +337,25 @@ def test_mxfp4_row_exponent_spread_of_the_128k_draws():
             worst = max(worst, int((e.max(axis=1) - e.min(axis=1)).max()))
     print(f"largest block-exponent spread within a row: {worst}")
     assert worst <= 8
+
+
+def test_e2m1_grid_scaled_down_is_exact_in_e4m3_up_to_shift_8():
+    """The bound behind the MXFP4 -> FP8 fold: every e2m1 value times 2^-s is
+    an e4m3 value for s = 0..8, and not every one is at s = 9.  e4m3 as in the
+    OCP 8-bit floating point spec: bias 7, three mantissa bits, subnormals at
+    exponent field 0, no infinities, S.1111.111 the only NaNs; enumerated from
+    all 256 codes."""
+    vals = set()
+    for b in range(256):
+        sign = -1.0 if b & 0x80 else 1.0
+        e, m = (b >> 3) & 0xF, b & 7
+        if e == 15 and m == 7:
+            continue                                     # NaN
+        v = (m / 8) * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+        vals.add(sign * v)
+    assert max(vals) == 448.0 and min(v for v in vals if v > 0) == 2.0 ** -9
+    grid = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for s in range(9):
+        for c in grid:
+            assert c * 2.0 ** -s in vals and -c * 2.0 ** -s in vals, (c, s)
+    assert 0.5 * 2.0 ** -9 not in vals                   # first loss at s = 9
