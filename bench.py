@@ -145,6 +145,77 @@ def algorithmic_bytes(w) -> dict:
     return dict(index=per_seq_index * w.B, step=(per_seq_csa + per_seq_hca) * w.B)
 
 
+def prefill_pairs(w, pos) -> dict:
+    """(query, key) pairs of a prefill chunk, from its query positions: indexer
+    scores over the visible compressed entries; CSA attention over the
+    selected entries plus the window; HCA attention over every visible HCA
+    entry plus the window."""
+    import numpy as np
+    t = np.asarray(pos, dtype=np.int64).reshape(-1)
+    nc = (t + 1) // w.m
+    nh = (t + 1) // w.m2
+    win = np.minimum(w.W, t + 1)
+    return dict(index=int(nc.sum()), csa=int((np.minimum(w.k, nc) + win).sum()),
+                hca=int((nh + win).sum()))
+
+
+def run_prefill_calls(args) -> None:
+    """Per-call times of the 64K prefill chunk (every position a query) and
+    the tensor throughput of its contractions: indexer 2*HI*dI flops per
+    score, attention 4*H*d per (query, key) pair (QK and PV).  The calls read
+    GB-sized operands, far beyond L2, so no flush is needed between them."""
+    import torch
+    import synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from gpu_util import make_step
+    import sparse_attention_27_b300 as sa
+    w = synth.WORKLOADS["prefill64k"]
+    x = synth.make_inputs(w)
+    step = make_step(w, x)
+    D = step.D
+    sc = torch.empty((w.B, w.T, w.ncap), dtype=torch.float32, device="cuda")
+
+    def timeit(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(args.steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    ms = {"compress_csa": timeit(step.compress_csa)}
+    ms["score"] = timeit(lambda: sa.csa_index_topk(
+        sa.SA_BF16, D.B, D.T, D.HI, D.dI, D.m, 0, step.x["q_idx"], None, step.x["w_idx"],
+        step.x["ik_c"], None, D.ncap, step.x["q_pos"], None, scores_out=sc))
+    ms["topk"] = timeit(lambda: sa.csa_index_topk(
+        sa.SA_BF16, D.B, D.T, D.HI, D.dI, D.m, D.k, None, None, None, None, None, D.ncap,
+        step.x["q_pos"], step.idx, scores_in=sc))
+    ms["attend_csa"] = timeit(step.attend_csa)
+    ms["hca"] = timeit(step.hca)
+    pairs = prefill_pairs(w, x["q_pos"])
+    flops = {"score": pairs["index"] * 2 * w.HI * w.dI,
+             "attend_csa": pairs["csa"] * 4 * w.H * w.d, "hca": pairs["hca"] * 4 * w.H * w.d}
+    peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        pass
+    tf = {k: flops[k] / (ms[k] * 1e-3) / 1e12 for k in flops}
+    print(json.dumps({
+        "mode": "prefill-calls", "workload": "prefill64k", "steps": args.steps,
+        "warmup": args.warmup, "ms": ms, "pairs": pairs, "tflops": tf,
+        "frac_of_bf16_peak": {k: v / peak for k, v in tf.items()} if peak else None,
+        "bf16_peak_tflops": peak, "device_errors": step.device_errors(),
+    }), flush=True)
+
+
 class Clocks:
     """SM clock and clock-event reasons sampled every ~2 ms by a background
     thread while the timed region runs, read through NVML (the driver's
@@ -368,6 +439,9 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-calls", action="store_true",
+                    help="instead of the decode step: per-call times and TFLOP/s of the 64K "
+                         "prefill chunk")
     ap.add_argument("--workload", default=WORKLOAD, choices=["decode128k", "decode1m", "mxfp4"],
                     help="decode at 128K (B=32, the default), at 1M (B=4), or at 128K with "
                          "the MXFP4 indexer")
@@ -375,6 +449,9 @@ def main() -> None:
     globals()["WORKLOAD"] = args.workload
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.prefill_calls:
+        run_prefill_calls(args)
         return
     assert args.warmup >= 3
 

@@ -92,3 +92,17 @@ def test_algorithmic_bytes_of_the_workloads():
     # 1M decode: 262144 indexer rows per sequence dominate
     m1 = bench.algorithmic_bytes(synth.WORKLOADS["decode1m"])
     assert m1["index"] == 4 * (262144 * 128 + 64 * 128 + 64 * 4)
+
+
+def test_prefill_pairs_of_the_64k_chunk():
+    """The 64K prefill chunk (t = 0..65535, m = 4, m' = 128, k = 2048, W = 128):
+    536,854,528 indexer scores, 134,207,552 CSA and 25,125,440 HCA
+    (query, key) pairs -- 4.40, 4.40 and 0.82 TFLOP at 8192 and 32768 flops
+    per score and pair."""
+    import numpy as np
+    w = synth.WORKLOADS["prefill64k"]
+    p = bench.prefill_pairs(w, np.arange(65536))
+    assert p == {"index": 536854528, "csa": 134207552, "hca": 25125440}
+    assert round(p["index"] * 2 * w.HI * w.dI / 1e12, 2) == 4.40
+    assert round(p["csa"] * 4 * w.H * w.d / 1e12, 2) == 4.40
+    assert round(p["hca"] * 4 * w.H * w.d / 1e12, 2) == 0.82
