@@ -76,3 +76,36 @@ def test_mxfp4_index_host_validation():
     assert call(dI=128) == m.SA_ERR_UNSUPPORTED
     assert call(q=P + 8) == m.SA_ERR_INVALID_ARG            # codes not 16-byte aligned
     assert call(ik=None) == m.SA_ERR_INVALID_ARG
+
+
+def _sms_148():
+    return (not torch.cuda.is_available() or
+            torch.cuda.get_device_properties(0).multi_processor_count == 148)
+
+
+@pytest.mark.skipif(not _sms_148(), reason="split sizes below are worked out for 148 SMs")
+def test_attention_workspace_queries_follow_the_split_rule():
+    """Workspace sizes of the attention calls, worked out by hand from the split
+    rule: key lists of 64-key tiles; the tensor-core kernel aims at 2 (row,
+    split) items per SM and at most 32 tiles per split; split s has
+    ceil(tiles / ns) tiles; partials are rows*nsplit*H*d f32 for O plus
+    rows*nsplit*H f32 for LSE, each rounded up to 256 B.  148 SMs (the count
+    the library assumes without a device)."""
+    import sparse_attention_27_b300 as m
+
+    def ws(rows, nsplit, H=64, d=128):
+        r256 = lambda x: (x + 255) // 256 * 256
+        return r256(4 * rows * nsplit * H * d) + r256(4 * rows * nsplit * H)
+    # 128K decode CSA: 32 rows, 2048/64 + 128/64 = 34 tiles; want ceil(296/32) = 10
+    # splits -> 4 tiles each -> 9 splits
+    assert m.csa_attend_workspace_bytes(m.SA_BF16, 32, 1, 64, 128, 2048, 128) == ws(32, 9)
+    # 128K decode HCA: 1024/64 + 2 = 18 tiles; 10 wanted -> 2 tiles each -> 9 splits
+    assert m.hca_compress_attend_workspace_bytes(m.SA_BF16, 32, 1, 64, 128, 1024, 128) == ws(32, 9)
+    # 1M decode CSA: 4 rows want 74 splits, 34 tiles -> one tile each -> 34 splits
+    assert m.csa_attend_workspace_bytes(m.SA_BF16, 4, 1, 64, 128, 2048, 128) == ws(4, 34)
+    # 1M decode HCA: 8192/64 + 2 = 130 tiles; 74 wanted -> 2 tiles each -> 65 splits
+    assert m.hca_compress_attend_workspace_bytes(m.SA_BF16, 4, 1, 64, 128, 8192, 128) == ws(4, 65)
+    # 64K prefill CSA: one split wanted, but at most 32 tiles per split -> 2 splits of 17
+    assert m.csa_attend_workspace_bytes(m.SA_BF16, 1, 65536, 64, 128, 2048, 128) == ws(65536, 2)
+    # fp32 (CUDA-core kernel, one item per CTA): 256 rows fill the SMs, no split
+    assert m.csa_attend_workspace_bytes(m.SA_F32, 1, 256, 16, 128, 64, 128) == 0
