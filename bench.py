@@ -130,8 +130,9 @@ def graph_kernels(graph, cudart) -> list:
     return names
 
 
-def algorithmic_bytes(w) -> dict:
-    """Minimum bytes one decode step must move (each needed row read once)."""
+def algorithmic_bytes(w, o_bytes: int = 4) -> dict:
+    """Minimum bytes one decode step must move (each needed row read once);
+    the attention output O is written in elements of ``o_bytes``."""
     e = 2  # bf16
     if w.indexer == "mxfp4":        # e2m1 codes + one e8m0 scale per 32, keys and queries
         row = w.dI // 2 + w.dI // 32
@@ -139,9 +140,9 @@ def algorithmic_bytes(w) -> dict:
     else:
         per_seq_index = w.ncap * w.dI * e + w.HI * w.dI * e + w.HI * 4
     per_seq_csa = (per_seq_index + w.k * 2 * w.d * e + w.W * 2 * w.d * e + w.H * w.d * e
-                   + w.k * 4 + w.H * w.d * 4 + w.H * 4)
+                   + w.k * 4 + w.H * w.d * o_bytes + w.H * 4)
     per_seq_hca = (w.ncap2 * 2 * w.d * e + w.W * 2 * w.d * e + w.H * w.d * e
-                   + w.H * w.d * 4 + w.H * 4)
+                   + w.H * w.d * o_bytes + w.H * 4)
     return dict(index=per_seq_index * w.B, step=(per_seq_csa + per_seq_hca) * w.B)
 
 
@@ -159,28 +160,37 @@ def prefill_pairs(w, pos) -> dict:
                 hca=int((nh + win).sum()))
 
 
-def run_prefill_calls(args) -> None:
+def bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1800.0, "fallback"
+
+
+def prefill_calls(steps: int, warmup: int, device: int = 0) -> dict:
     """Per-call times of the 64K prefill chunk (every position a query) and
     the tensor throughput of its contractions: indexer 2*HI*dI flops per
     score, attention 4*H*d per (query, key) pair (QK and PV).  The calls read
-    GB-sized operands, far beyond L2, so no flush is needed between them."""
+    GB-sized operands, far beyond L2, so no flush is needed between them.
+    Each call is timed alone with CUDA events on the current stream, median
+    of ``steps`` after ``warmup`` untimed calls."""
     import torch
     import synth
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from gpu_util import make_step
+    from sparse_attention_27_b300.path import step_from
     import sparse_attention_27_b300 as sa
     w = synth.WORKLOADS["prefill64k"]
     x = synth.make_inputs(w)
-    step = make_step(w, x)
+    step = step_from(w, x, o_dtype="bf16")
     D = step.D
     sc = torch.empty((w.B, w.T, w.ncap), dtype=torch.float32, device="cuda")
 
     def timeit(fn):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             fn()
         torch.cuda.synchronize()
         ts = []
-        for _ in range(args.steps):
+        for _ in range(steps):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()
@@ -189,31 +199,38 @@ def run_prefill_calls(args) -> None:
             ts.append(a.elapsed_time(b))
         return statistics.median(ts)
 
-    ms = {"compress_csa": timeit(step.compress_csa)}
-    ms["score"] = timeit(lambda: sa.csa_index_topk(
-        sa.SA_BF16, D.B, D.T, D.HI, D.dI, D.m, 0, step.x["q_idx"], None, step.x["w_idx"],
-        step.x["ik_c"], None, D.ncap, step.x["q_pos"], None, scores_out=sc))
-    ms["topk"] = timeit(lambda: sa.csa_index_topk(
-        sa.SA_BF16, D.B, D.T, D.HI, D.dI, D.m, D.k, None, None, None, None, None, D.ncap,
-        step.x["q_pos"], step.idx, scores_in=sc))
-    ms["attend_csa"] = timeit(step.attend_csa)
-    ms["hca"] = timeit(step.hca)
+    with Clocks(device) as clk:
+        ms = {"compress_csa": timeit(step.compress_csa)}
+        ms["score"] = timeit(lambda: sa.csa_index_topk(
+            sa.SA_BF16, D.B, D.T, D.HI, D.dI, D.m, 0, step.x["q_idx"], None, step.x["w_idx"],
+            step.x["ik_c"], None, D.ncap, step.x["q_pos"], None, scores_out=sc))
+        ms["topk"] = timeit(lambda: sa.csa_index_topk(
+            sa.SA_BF16, D.B, D.T, D.HI, D.dI, D.m, D.k, None, None, None, None, None, D.ncap,
+            step.x["q_pos"], step.idx, scores_in=sc))
+        ms["attend_csa"] = timeit(step.attend_csa)
+        ms["hca"] = timeit(step.hca)
     pairs = prefill_pairs(w, x["q_pos"])
     flops = {"score": pairs["index"] * 2 * w.HI * w.dI,
              "attend_csa": pairs["csa"] * 4 * w.H * w.d, "hca": pairs["hca"] * 4 * w.H * w.d}
-    peak = None
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peak = float(json.load(f)["bf16_tflops"])
-    except Exception:
-        pass
+    peak, peak_kind = bf16_peak()
     tf = {k: flops[k] / (ms[k] * 1e-3) / 1e12 for k in flops}
-    print(json.dumps({
-        "mode": "prefill-calls", "workload": "prefill64k", "steps": args.steps,
-        "warmup": args.warmup, "ms": ms, "pairs": pairs, "tflops": tf,
-        "frac_of_bf16_peak": {k: v / peak for k, v in tf.items()} if peak else None,
-        "bf16_peak_tflops": peak, "device_errors": step.device_errors(),
-    }), flush=True)
+    errs = step.device_errors()
+    total = sum(ms.values())
+    out = {"workload": "prefill64k", "tokens": w.B * w.T, "steps": steps, "warmup": warmup,
+           "ms": ms, "chunk_ms": total, "tokens_per_s": w.B * w.T / (total * 1e-3),
+           "pairs": pairs, "tflop": {k: v / 1e12 for k, v in flops.items()}, "tflops": tf,
+           "frac_of_bf16_peak": {k: v / peak for k, v in tf.items()},
+           "bf16_peak_tflops": peak, "peak_source": peak_kind, "device_errors": errs,
+           "clocks": clk.summary(),
+           "note": "each call timed alone (CUDA events, median); O in bf16"}
+    del step, sc, x
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_prefill_calls(args) -> None:
+    print(json.dumps({"mode": "prefill-calls", **prefill_calls(args.steps, args.warmup)}),
+          flush=True)
 
 
 class Clocks:
@@ -432,55 +449,24 @@ def run_reference(args) -> None:
     }), flush=True)
 
 
-def main() -> None:
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--prefill-calls", action="store_true",
-                    help="instead of the decode step: per-call times and TFLOP/s of the 64K "
-                         "prefill chunk")
-    ap.add_argument("--workload", default=WORKLOAD, choices=["decode128k", "decode1m", "mxfp4"],
-                    help="decode at 128K (B=32, the default), at 1M (B=4), or at 128K with "
-                         "the MXFP4 indexer")
-    args = ap.parse_args()
-    globals()["WORKLOAD"] = args.workload
-    if args.impl == "reference":
-        run_reference(args)
-        return
-    if args.prefill_calls:
-        run_prefill_calls(args)
-        return
-    assert args.warmup >= 3
-
-    import numpy as np
+def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int,
+                   e2e: bool = True) -> dict:
+    """Time the decode step of workload ``w`` (inputs already resident in HBM):
+    the whole step (one CUDA graph, CSA and HCA on two streams), the
+    dominant kernel alone (the indexer scoring call as a one-node graph) and
+    the step end to end (inputs from pinned host memory, outputs back).  L2 is
+    flushed before every timed replay; every replay is timed with CUDA events
+    on the launching stream.  Returns the measurement as a dict."""
     import torch
-    import torch.distributed as dist
-
     import synth
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from gpu_util import dev, make_step
+    import sparse_attention_27_b300 as sa
+    from sparse_attention_27_b300.path import step_from
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-
-    w = synth.WORKLOADS[WORKLOAD]
-    if world > 1:                   # every rank decodes its own sequences (seeded by rank)
-        import dataclasses
-        w = dataclasses.replace(w, seed=rank)
     x = synth.make_inputs(w)
-    step = make_step(w, x)
+    step = step_from(w, x, o_dtype="bf16")
     io = StepIO(step, x, w)         # packs per-step inputs and outputs (before capture)
     s_csa, s_hca = torch.cuda.Stream(), torch.cuda.Stream()
-    main_s = torch.cuda.current_stream()
-    # warm-up outside the graph (sets kernel attributes, loads modules)
-    for _ in range(2):
+    for _ in range(2):              # outside the graph: sets kernel attributes, loads modules
         step.run_two_streams(s_csa, s_hca)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph(keep_graph=True)
@@ -490,7 +476,6 @@ def main() -> None:
     # the step's kernel launches: the captured graph's kernel nodes (the step
     # issues only library calls and event edges, so every kernel node is ours)
     kernels = graph_kernels(g.raw_cuda_graph(), io.cudart)
-    launches = len(kernels)
     g.instantiate()
     torch.cuda.synchronize()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
@@ -508,30 +493,28 @@ def main() -> None:
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in evs]
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         g.replay()
     torch.cuda.synchronize()
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     with Clocks(local) as clk:
-        ms = timed(g.replay, args.steps)
+        ms = timed(g.replay, steps)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    total_ms = sum(ms)
+    total_ms = max_over_ranks(sum(ms), device="cuda")
     ms_sorted = sorted(ms)
     pct = lambda q: ms_sorted[min(len(ms_sorted) - 1, int(q * len(ms_sorted)))]
-    total_ms = max_over_ranks(total_ms, device="cuda")
     errs = step.device_errors()
-    value = world * w.B * w.T * args.steps / (total_ms / 1e3)
+    value = world * w.B * w.T * steps / (total_ms / 1e3)
 
     # ---- dominant kernel: indexer scoring alone (csa_index_topk with k = 0)
-    import sparse_attention_27_b300 as sa
     D = step.D
     sc = torch.empty((w.B, w.T, w.ncap), dtype=torch.float32, device="cuda")
-
     mx = w.indexer == "mxfp4"
 
     def score_only():
@@ -551,25 +534,23 @@ def main() -> None:
         score_only()
     for _ in range(3):
         g_score.replay()
-    k_ms = timed(g_score.replay, args.steps)
+    k_ms = timed(g_score.replay, steps)
     k_avg = sum(k_ms) / len(k_ms)
-    ab = algorithmic_bytes(w)
+    ab = algorithmic_bytes(w, o_bytes=2)
     peak, peak_kind = peaks()
     achieved = ab["index"] / (k_avg / 1e3) / 1e9
     score_kernel = "score_mx_kernel" if mx else "score_tc_kernel"
     traffic, traffic_note = recorded_traffic(score_kernel, MX_SOURCES if mx else SCORE_SOURCES,
                                              ab["index"])
-    step_gbs = ab["step"] / (total_ms / args.steps / 1e3) / 1e9
+    step_gbs = ab["step"] / (total_ms / steps / 1e3) / 1e9
 
     # ---- end to end: host (pinned) inputs of the new token in, outputs out
-    e2e = None
-    if rank == 0 or world > 1:
+    e2e_out = None
+    if e2e:
         def e2e_body():
             # each layer: its inputs in, its kernels, its outputs out, on its own
             # stream; the CSA layer also waits for the positions (HCA's copy).
             # HCA starts at once here: its readback then overlaps the CSA chain
-            # (starting it after the CSA scores, as the device-only graph does,
-            # leaves both readbacks at the end of the step)
             cur = torch.cuda.current_stream()
             fork = torch.cuda.Event()
             fork.record(cur)
@@ -596,42 +577,111 @@ def main() -> None:
             e2e_body()
         for _ in range(3):
             g_e2e.replay()
-        e_ms = timed(g_e2e.replay, args.steps)
+        e_ms = timed(g_e2e.replay, steps)
         e_total = max_over_ranks(sum(e_ms), device="cuda")
-        e2e = {"value": world * w.B * w.T * args.steps / (e_total / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": io.h2d_bytes, "d2h_bytes_per_step": io.d2h_bytes,
-               "copies_per_step": io.copies,
-               "note": "one graph per step: each layer's copies on its own stream"}
+        e2e_out = {"value": world * w.B * w.T * steps / (e_total / 1e3), "unit": UNIT,
+                   "h2d_bytes_per_step": io.h2d_bytes, "d2h_bytes_per_step": io.d2h_bytes,
+                   "copies_per_step": io.copies,
+                   "note": "one graph per step: each layer's copies on its own stream; O read "
+                           "back in bf16"}
+    out = {
+        "value": value, "ms_per_step": total_ms / steps,
+        "config": {"workload": w.name, "batch": w.B, "context": w.L, "heads": w.H,
+                   "head_dim": w.d, "m": w.m, "top_k": w.k, "window": w.W, "m2": w.m2,
+                   "indexer_heads": w.HI, "indexer": w.indexer, "o_dtype": "bf16",
+                   "parallelism": f"replicas x{world}",
+                   "l2": "flushed before every timed step: a 512 MiB write, then a 256 MiB read",
+                   "graph": "one CUDA graph per step, CSA and HCA on two streams, HCA after "
+                            "the CSA scores"},
+        "step_algorithmic_bytes": ab["step"], "step_gbs": step_gbs,
+        "step_frac_of_hbm": step_gbs / peak,
+        "roofline": {"kernel": f"{score_kernel} (csa_index_topk scores, k=0, one-node graph)",
+                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "traffic": traffic, "traffic_source": traffic_note,
+                     "avg_launch_ms": k_avg, "algorithmic_bytes_per_launch": ab["index"]},
+        "e2e": e2e_out, "gpu_launches": len(kernels) * steps,
+        "step_ms": {"p10": pct(0.10), "median": statistics.median(ms), "p90": pct(0.90)},
+        "kernels_per_step": len(kernels), "kernels": sorted(set(kernels)),
+        "device_errors": errs, "clocks": clk.summary(),
+    }
+    return out, x
 
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only the headline workload (no 1M decode and 64K prefill objects)")
+    ap.add_argument("--prefill-calls", action="store_true",
+                    help="instead of the decode step: per-call times and TFLOP/s of the 64K "
+                         "prefill chunk")
+    ap.add_argument("--workload", default=WORKLOAD, choices=["decode128k", "decode1m", "mxfp4"],
+                    help="decode at 128K (B=32, the default), at 1M (B=4), or at 128K with "
+                         "the MXFP4 indexer")
+    args = ap.parse_args()
+    globals()["WORKLOAD"] = args.workload
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    if args.prefill_calls:
+        run_prefill_calls(args)
+        return
+    assert args.warmup >= 3
+
+    import dataclasses
+    import torch
+    import torch.distributed as dist
+    import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    w = synth.WORKLOADS[WORKLOAD]
+    if world > 1:                   # every rank decodes its own sequences (seeded by rank)
+        w = dataclasses.replace(w, seed=rank)
+    head, x = decode_measure(w, args.steps, args.warmup, rank, world, local)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, x, seqs=w.B)
+    del x
+    torch.cuda.empty_cache()
+
+    # the metric's second context (1M decode) and the prefill contractions, on
+    # the default run only (rank 0 of a single-GPU run)
+    extra = {}
+    if WORKLOAD == "decode128k" and world == 1 and not args.no_extra:
+        w1 = synth.WORKLOADS["decode1m"]
+        m1, x1 = decode_measure(w1, args.steps, args.warmup, rank, world, local)
+        if not args.no_cpu_baseline:
+            m1["cpu_baseline"] = cpu_baseline(w1, x1, seqs=w1.B)
+        del x1
+        torch.cuda.empty_cache()
+        extra["decode1m"] = m1
+        extra["prefill64k"] = prefill_calls(steps=3, warmup=1, device=local)
 
     if rank == 0:
-        print(json.dumps({
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        line = {
+            "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": {"workload": WORKLOAD, "batch": w.B, "context": w.L, "heads": w.H,
-                       "head_dim": w.d, "m": w.m, "top_k": w.k, "window": w.W, "m2": w.m2,
-                       "indexer_heads": w.HI, "indexer": w.indexer,
-                       "parallelism": f"replicas x{world}",
-                       "l2": "flushed before every timed step: a 512 MiB write, then a 256 MiB read",
-                       "graph": "one CUDA graph per step, CSA and HCA on two streams, HCA after the CSA scores"},
-            "step_algorithmic_bytes": ab["step"], "step_gbs": step_gbs,
-            "step_frac_of_hbm": step_gbs / peak,
-            "roofline": {"kernel": f"{score_kernel} (csa_index_topk scores, k=0, one-node graph)",
-                         "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_source": peak_kind,
-                         "traffic": traffic, "traffic_source": traffic_note,
-                         "avg_launch_ms": k_avg,
-                         "algorithmic_bytes_per_launch": ab["index"]},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * args.steps,
-            "step_ms": {"p10": pct(0.10), "median": statistics.median(ms), "p90": pct(0.90)},
-            "kernels_per_step": launches,
-            "device_errors": errs, "clocks": clk.summary(),
-        }), flush=True)
+            "data": "synthetic", "config": head["config"],
+        }
+        for k_ in ("step_algorithmic_bytes", "step_gbs", "step_frac_of_hbm", "roofline", "e2e",
+                   "gpu_launches", "step_ms", "kernels_per_step", "kernels", "device_errors",
+                   "clocks"):
+            line[k_] = head[k_]
+        line["cpu_baseline"] = cpu
+        line.update(extra)
+        print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 

@@ -125,7 +125,9 @@ int csa_compress(int dtype, int ik_dtype, int B, int d, int dI, int m, const voi
  * block exponent factored out -- exact while the row's two block exponents
  * differ by at most 8 -- contracted with tcgen05 kind::f8f6f4 into fp32, and
  * the row exponents applied in fp32 before the weighted ReLU head sum.
- * N_cap <= 393216.
+ * N_cap <= 524288 (a row's candidates split over at most 16 CTAs of one
+ * thread-block cluster; SA_ERR_UNSUPPORTED if the device cannot run the
+ * cluster size a row needs).
  * Device errors: NaN score -> SA_ERR_NAN (row written as all -1);
  * n > N_cap -> SA_ERR_BOUNDS (n clamped).
  */
@@ -148,9 +150,10 @@ size_t csa_index_topk_workspace_bytes(int B, int T, int N_cap, int k);
  * cannot afford cudaMalloc, which may synchronise the device and takes
  * unbounded time.
  *
- * Same operation, arguments, layouts and device errors as csa_index_topk,
- * without scores_out, scores_in and the workspace.  q_dtype must be SA_F32 or
- * SA_BF16.  The scores live in a fixed device array inside the library
+ * Same operation, arguments, layouts, host-side and device errors as
+ * csa_index_topk, without scores_out, scores_in and the workspace.  q_dtype
+ * must be SA_F32 or SA_BF16 (SA_MXFP4 gives SA_ERR_UNSUPPORTED; an unknown
+ * dtype SA_ERR_INVALID_ARG, as csa_index_topk).  The scores live in a fixed device array inside the library
  * (SA_NOALLOC_MAX_SCORES floats, 8 MiB), which every GPU that loads the
  * library holds until the process exits.  Limit: B * T * N_cap <=
  * SA_NOALLOC_MAX_SCORES, otherwise SA_ERR_UNSUPPORTED is returned before any
@@ -182,7 +185,8 @@ int csa_index_topk_noalloc(int q_dtype, int B, int T, int HI, int dI, int m, int
  * An empty key set gives o = 0, lse = -inf.
  *  dtype     SA_F32 or SA_BF16 for q, k_c, v_c, k_raw, v_raw
  *  q [B,T,H,d]; k_c, v_c [B,N_cap,d]; idx [B,T,k]; k_raw, v_raw [B,R,d]
- *  o [B,T,H,d] f32; lse [B,T,H] f32 (natural log)
+ *  o [B,T,H,d] in o_dtype (SA_F32, or SA_BF16 rounded to nearest-even from
+ *  the fp32 result); lse [B,T,H] f32 (natural log)
  * bf16 with H <= 64, d = 128 runs on the tensor cores; other shapes on CUDA
  * cores (d <= 256, d a multiple of 4, H * d <= 16384).  Requires R >= W.
  * Device errors: idx entry >= n or < -1 -> SA_ERR_BOUNDS (entry ignored).
@@ -190,7 +194,8 @@ int csa_index_topk_noalloc(int q_dtype, int B, int T, int HI, int dI, int m, int
 int csa_attend(int dtype, int B, int T, int H, int d, int m, int k, int W, float sm_scale,
                const void* q, const int32_t* q_pos, const void* k_c, const void* v_c,
                int N_cap, const int32_t* idx, const void* k_raw, const void* v_raw, int R,
-               float* o, float* lse, void* ws, size_t ws_bytes, int32_t* err, void* stream);
+               void* o, int o_dtype, float* lse, void* ws, size_t ws_bytes, int32_t* err,
+               void* stream);
 size_t csa_attend_workspace_bytes(int dtype, int B, int T, int H, int d, int k, int W);
 
 /* ---------------------------------------------------------------------------
@@ -202,15 +207,15 @@ size_t csa_attend_workspace_bytes(int dtype, int B, int T, int H, int d, int k, 
  *     keys = { hK_c[b,j] : j < n2 }  (+)  { K_raw[b, u mod R] : p-Wn < u <= p }
  * with the same softmax, o and lse definitions as csa_attend.
  *  q [B,T,H,d]; k_raw, v_raw [B,R,d]; z_hca [B,R] f32; hk_c, hv_c [B,N2_cap,d]
- *  o [B,T,H,d] f32; lse [B,T,H] f32
+ *  o [B,T,H,d] in o_dtype (SA_F32 or SA_BF16, as csa_attend); lse [B,T,H] f32
  * Requires R >= W and, when compressing, R >= m2; d <= 256, a multiple of 4.
  */
 int hca_compress_attend(int dtype, int B, int T, int H, int d, int m2, int W, float sm_scale,
                         const void* q, const int32_t* q_pos, const void* k_raw,
                         const void* v_raw, const float* z_hca, int R, const int32_t* blk_lo,
                         const int32_t* blk_hi, int max_blocks, void* hk_c, void* hv_c,
-                        int N2_cap, float* o, float* lse, void* ws, size_t ws_bytes,
-                        int32_t* err, void* stream);
+                        int N2_cap, void* o, int o_dtype, float* lse, void* ws,
+                        size_t ws_bytes, int32_t* err, void* stream);
 size_t hca_compress_attend_workspace_bytes(int dtype, int B, int T, int H, int d, int N2_cap,
                                            int W);
 

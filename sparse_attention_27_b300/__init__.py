@@ -55,11 +55,11 @@ _lib.csa_index_topk_noalloc.argtypes = [_i, _i, _i, _i, _i, _i, _i, _vp, _vp, _v
                                         _vp, _vp, _vp, _vp]
 _lib.sa_mxfp4_quantize.argtypes = [_vp, _i64, _vp, _vp, _vp]
 _lib.csa_attend.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _i, _vp, _vp,
-                            _vp, _i, _vp, _vp, _vp, _sz, _vp, _vp]
+                            _vp, _i, _vp, _i, _vp, _vp, _sz, _vp, _vp]
 _lib.csa_attend_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
 _lib.csa_attend_workspace_bytes.restype = _sz
 _lib.hca_compress_attend.argtypes = [_i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _i,
-                                     _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp, _vp]
+                                     _vp, _vp, _i, _vp, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp, _vp]
 _lib.hca_compress_attend_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
 _lib.hca_compress_attend_workspace_bytes.restype = _sz
 _lib.attn_merge.argtypes = [_i, _vp, _vp, _i64, _i, _vp, _i, _vp, _vp, _vp]
@@ -138,11 +138,17 @@ def csa_attend_workspace_bytes(dtype, B, T, H, d, k, W) -> int:
     return int(_lib.csa_attend_workspace_bytes(dtype, B, T, H, d, k, W))
 
 
+def _out_code(o) -> int:
+    """dtype code of an output tensor (f32 for anything that is not a tensor)."""
+    return dtype_code(o) if isinstance(o, torch.Tensor) else SA_F32
+
+
 def csa_attend(dtype, B, T, H, d, m, k, W, sm_scale, q, q_pos, k_c, v_c, N_cap, idx, k_raw, v_raw,
                R, o, lse, ws=None, ws_bytes=0, err=None, stream=None):
+    """o: f32 or bf16 tensor [B,T,H,d] (its dtype selects the output type)."""
     _check(_lib.csa_attend(dtype, B, T, H, d, m, k, W, sm_scale, _p(q), _p(q_pos), _p(k_c),
-                           _p(v_c), N_cap, _p(idx), _p(k_raw), _p(v_raw), R, _p(o), _p(lse),
-                           _p(ws), ws_bytes, _p(err), _stream(stream)), "csa_attend")
+                           _p(v_c), N_cap, _p(idx), _p(k_raw), _p(v_raw), R, _p(o), _out_code(o),
+                           _p(lse), _p(ws), ws_bytes, _p(err), _stream(stream)), "csa_attend")
 
 
 def hca_compress_attend_workspace_bytes(dtype, B, T, H, d, N2_cap, W) -> int:
@@ -154,8 +160,9 @@ def hca_compress_attend(dtype, B, T, H, d, m2, W, sm_scale, q, q_pos, k_raw, v_r
                         ws_bytes=0, err=None, stream=None):
     _check(_lib.hca_compress_attend(dtype, B, T, H, d, m2, W, sm_scale, _p(q), _p(q_pos),
                                     _p(k_raw), _p(v_raw), _p(z_hca), R, _p(blk_lo), _p(blk_hi),
-                                    max_blocks, _p(hk_c), _p(hv_c), N2_cap, _p(o), _p(lse), _p(ws),
-                                    ws_bytes, _p(err), _stream(stream)), "hca_compress_attend")
+                                    max_blocks, _p(hk_c), _p(hv_c), N2_cap, _p(o), _out_code(o),
+                                    _p(lse), _p(ws), ws_bytes, _p(err), _stream(stream)),
+           "hca_compress_attend")
 
 
 def sa_mxfp4_quantize(x, codes, scales, stream=None):

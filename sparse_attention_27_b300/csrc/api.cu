@@ -30,7 +30,7 @@ bool plain_dtype(int dt) { return dt == SA_F32 || dt == SA_BF16; }
 int status_of(cudaError_t e) {
   if (e == cudaSuccess) return SA_OK;
   cudaGetLastError();  // clear a sticky launch error for the caller's next call
-  return SA_ERR_CUDA;
+  return e == cudaErrorNotSupported ? SA_ERR_UNSUPPORTED : SA_ERR_CUDA;
 }
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -198,9 +198,10 @@ size_t csa_attend_workspace_bytes(int dtype, int B, int T, int H, int d, int k, 
 int csa_attend(int dtype, int B, int T, int H, int d, int m, int k, int W, float sm_scale,
                const void* q, const int32_t* q_pos, const void* k_c, const void* v_c,
                int N_cap, const int32_t* idx, const void* k_raw, const void* v_raw, int R,
-               float* o, float* lse, void* ws, size_t ws_bytes, int32_t* err, void* stream) {
-  if (!plain_dtype(dtype) || B < 0 || T < 0 || H <= 0 || d <= 0 || d > 256 || m < 1 || k < 0 ||
-      W < 0 || N_cap < 0 || R < W || R < 1)
+               void* o, int o_dtype, float* lse, void* ws, size_t ws_bytes, int32_t* err,
+               void* stream) {
+  if (!plain_dtype(dtype) || !plain_dtype(o_dtype) || B < 0 || T < 0 || H <= 0 || d <= 0 ||
+      d > 256 || m < 1 || k < 0 || W < 0 || N_cap < 0 || R < W || R < 1)
     return SA_ERR_INVALID_ARG;
   if (!q || !q_pos || !o || !lse || !k_raw || !v_raw || (k > 0 && (!idx || !k_c || !v_c)))
     return SA_ERR_INVALID_ARG;
@@ -212,7 +213,8 @@ int csa_attend(int dtype, int B, int T, int H, int d, int m, int k, int W, float
   AttnArgs a{};
   a.dtype = dtype; a.B = B; a.T = T; a.H = H; a.d = d; a.sm_scale = sm_scale;
   a.q = q; a.q_pos = q_pos; a.kc = k_c; a.vc = v_c; a.N_cap = N_cap; a.idx = idx;
-  a.k = k; a.m = m; a.kr = k_raw; a.vr = v_raw; a.R = R; a.W = W; a.o = o; a.lse = lse;
+  a.k = k; a.m = m; a.kr = k_raw; a.vr = v_raw; a.R = R; a.W = W; a.o = o;
+  a.o_dtype = o_dtype; a.lse = lse;
   a.err = err;
   a.gather = 1;
   return run_attention(a, ws, ws_bytes, attn_tiles(k, W), static_cast<cudaStream_t>(stream));
@@ -229,10 +231,10 @@ int hca_compress_attend(int dtype, int B, int T, int H, int d, int m2, int W, fl
                         const void* q, const int32_t* q_pos, const void* k_raw,
                         const void* v_raw, const float* z_hca, int R, const int32_t* blk_lo,
                         const int32_t* blk_hi, int max_blocks, void* hk_c, void* hv_c,
-                        int N2_cap, float* o, float* lse, void* ws, size_t ws_bytes,
-                        int32_t* err, void* stream) {
-  if (!plain_dtype(dtype) || B < 0 || T < 0 || H <= 0 || d <= 0 || d > 256 || m2 < 1 || W < 0 ||
-      N2_cap < 0 || R < W || R < 1 || max_blocks < 0)
+                        int N2_cap, void* o, int o_dtype, float* lse, void* ws,
+                        size_t ws_bytes, int32_t* err, void* stream) {
+  if (!plain_dtype(dtype) || !plain_dtype(o_dtype) || B < 0 || T < 0 || H <= 0 || d <= 0 ||
+      d > 256 || m2 < 1 || W < 0 || N2_cap < 0 || R < W || R < 1 || max_blocks < 0)
     return SA_ERR_INVALID_ARG;
   if (!q || !q_pos || !o || !lse || !k_raw || !v_raw || (N2_cap > 0 && (!hk_c || !hv_c)))
     return SA_ERR_INVALID_ARG;
@@ -255,7 +257,8 @@ int hca_compress_attend(int dtype, int B, int T, int H, int d, int m2, int W, fl
   a.dtype = dtype; a.B = B; a.T = T; a.H = H; a.d = d; a.sm_scale = sm_scale;
   a.q = q; a.q_pos = q_pos; a.kc = hk_c; a.vc = hv_c; a.N_cap = N2_cap; a.idx = nullptr;
   a.gather = 0;
-  a.k = 0; a.m = m2; a.kr = k_raw; a.vr = v_raw; a.R = R; a.W = W; a.o = o; a.lse = lse;
+  a.k = 0; a.m = m2; a.kr = k_raw; a.vr = v_raw; a.R = R; a.W = W; a.o = o;
+  a.o_dtype = o_dtype; a.lse = lse;
   a.err = err;
   return run_attention(a, ws, ws_bytes, attn_tiles(N2_cap, W), st);
 }

@@ -132,12 +132,14 @@ __global__ void __launch_bounds__(kAttnSimtThreads) attend_simt_kernel(AttnArgs 
     __syncthreads();
   }
 
-  float* out_o = a.nsplit > 1 ? a.part_o + (row * a.nsplit + split) * H * d : a.o + row * H * d;
   float* out_l = a.nsplit > 1 ? a.part_lse + (row * a.nsplit + split) * H : a.lse + row * H;
   for (int e = threadIdx.x; e < H * d; e += blockDim.x) {
     const int h = e / d;
     const float l = s_l[h];
-    out_o[e] = l > 0.f ? s_o[e] / l : 0.f;
+    const float v = l > 0.f ? s_o[e] / l : 0.f;
+    if (a.nsplit > 1) a.part_o[(row * a.nsplit + split) * H * d + e] = v;
+    else if (a.o_dtype == SA_BF16) Store<SA_BF16>::st(a.o, row * H * d + e, v);
+    else Store<SA_F32>::st(a.o, row * H * d + e, v);
   }
   for (int h = threadIdx.x; h < H; h += blockDim.x)
     out_l[h] = s_l[h] > 0.f ? s_m[h] + logf(s_l[h]) : -INFINITY;
@@ -185,7 +187,7 @@ constexpr int kMergeBatch = 16;
 
 __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(
     const float* __restrict__ part_o, const float* __restrict__ part_lse, int nsplit, int H,
-    int d, float* __restrict__ o, float* __restrict__ lse) {
+    int d, void* __restrict__ o, int o_dtype, float* __restrict__ lse) {
   extern __shared__ float s_w[];                 // [nsplit][kMergeHeads]: LSEs, then weights
   const int64_t row = blockIdx.x;
   const int h0 = blockIdx.y * kMergeHeads;
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(
   const int n4 = nh * d4;                        // float4 outputs of this CTA
   const int64_t stride4 = (int64_t)H * d4;       // float4 per split of the row
   const float4* po = reinterpret_cast<const float4*>(part_o + (row * nsplit * H + h0) * d);
-  float4* out = reinterpret_cast<float4*>(o + (row * H + h0) * d);
+  const int64_t out0 = (row * H + h0) * d;      // first output element of this CTA
   for (int e = threadIdx.x; e < n4; e += blockDim.x) {
     const int hh = e / d4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -237,7 +239,16 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(
         }
       }
     }
-    out[e] = acc;
+    if (o_dtype == SA_BF16) {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 u;
+      u.x = *reinterpret_cast<const uint32_t*>(&lo);
+      u.y = *reinterpret_cast<const uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o) + out0)[e] = u;
+    } else {
+      reinterpret_cast<float4*>(static_cast<float*>(o) + out0)[e] = acc;
+    }
   }
 }
 
@@ -281,7 +292,7 @@ cudaError_t launch_merge_splits(const AttnArgs& a, cudaStream_t st) {
   }
   const dim3 grid((unsigned)rows, (unsigned)((a.H + kMergeHeads - 1) / kMergeHeads));
   merge_splits_kernel<<<grid, kMergeThreads, smem, st>>>(a.part_o, a.part_lse, a.nsplit, a.H,
-                                                          a.d, a.o, a.lse);
+                                                          a.d, a.o, a.o_dtype, a.lse);
   return cudaGetLastError();
 }
 

@@ -319,16 +319,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     bool ok = true;
     for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x) {
       const Item I = make_item(a, it);
-      float* out_o = a.nsplit > 1 ? a.part_o + (I.row * a.nsplit + I.split) * a.H * kD
-                                  : a.o + I.row * a.H * kD;
-      float* out_l = a.nsplit > 1 ? a.part_lse + (I.row * a.nsplit + I.split) * a.H
-                                  : a.lse + I.row * a.H;
+      // a split partial (f32) or the row's output (f32 or bf16): element offset
+      // `off` of the row's [H, d] block, two consecutive columns at a time
+      const bool part = a.nsplit > 1;
+      const bool o16 = !part && a.o_dtype == SA_BF16;
+      float* out_o = part ? a.part_o + (I.row * a.nsplit + I.split) * a.H * kD
+                          : static_cast<float*>(a.o) + I.row * a.H * kD;
+      __nv_bfloat16* out_o16 = static_cast<__nv_bfloat16*>(a.o) + I.row * a.H * kD;
+      auto put2 = [&](int off, float x, float y) {
+        if (o16) *reinterpret_cast<__nv_bfloat162*>(out_o16 + off) = __floats2bfloat162_rn(x, y);
+        else *reinterpret_cast<float2*>(out_o + off) = make_float2(x, y);
+      };
+      float* out_l = part ? a.part_lse + (I.row * a.nsplit + I.split) * a.H
+                          : a.lse + I.row * a.H;
       if (I.nt == 0 || !ok) {                      // no keys (or stopped): empty result
 #pragma unroll 4
         for (int g = 0; g < kD / 8; ++g) {
           const int col = 8 * g + 2 * l4;
-          if (ok0) *reinterpret_cast<float2*>(out_o + h0 * kD + col) = make_float2(0.f, 0.f);
-          if (ok1) *reinterpret_cast<float2*>(out_o + h1 * kD + col) = make_float2(0.f, 0.f);
+          if (ok0) put2(h0 * kD + col, 0.f, 0.f);
+          if (ok1) put2(h1 * kD + col, 0.f, 0.f);
         }
         if (l4 == 0 && ok0) out_l[h0] = -INFINITY;
         if (l4 == 0 && ok1) out_l[h1] = -INFINITY;
@@ -469,13 +478,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int col = c + 8 * g + 2 * l4;
-          if (ok0)
-            *reinterpret_cast<float2*>(out_o + h0 * kD + col) =
-                have0 ? make_float2(o[4 * g] * inv0, o[4 * g + 1] * inv0) : make_float2(0.f, 0.f);
-          if (ok1)
-            *reinterpret_cast<float2*>(out_o + h1 * kD + col) =
-                have1 ? make_float2(o[4 * g + 2] * inv1, o[4 * g + 3] * inv1)
-                      : make_float2(0.f, 0.f);
+          if (ok0) put2(h0 * kD + col, o[4 * g] * inv0, o[4 * g + 1] * inv0);
+          if (ok1) put2(h1 * kD + col, o[4 * g + 2] * inv1, o[4 * g + 3] * inv1);
         }
       }
       if (l4 == 0 && ok0) out_l[h0] = have0 ? (m0 + log2f(l0)) * 0.6931471805599453f : -INFINITY;

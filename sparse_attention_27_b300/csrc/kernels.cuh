@@ -75,7 +75,8 @@ struct AttnArgs {
   const void* kr;       // [B, R, d]
   const void* vr;
   int R, W;
-  float* o;             // [B*T, H, d]
+  void* o;              // [B*T, H, d] in o_dtype
+  int o_dtype;          // SA_F32 or SA_BF16
   float* lse;           // [B*T, H]
   int nsplit;           // key-tile splits per row (1: write o/lse directly)
   int split_tiles;      // key tiles (of kAttnTile keys) per split

@@ -63,7 +63,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int status_of(cudaError_t e) {
   if (e == cudaSuccess) return SA_OK;
   cudaGetLastError();
-  return SA_ERR_CUDA;
+  return e == cudaErrorNotSupported ? SA_ERR_UNSUPPORTED : SA_ERR_CUDA;
 }
 
 }  // namespace
@@ -80,7 +80,8 @@ extern "C" int csa_index_topk_noalloc(int q_dtype, int B, int T, int HI, int dI,
     return SA_ERR_INVALID_ARG;
   if ((int64_t)B * T * N_cap > kNoAllocMaxScores) return SA_ERR_UNSUPPORTED;
   if (!topk_supported(N_cap)) return SA_ERR_UNSUPPORTED;
-  if (q_dtype != SA_F32 && q_dtype != SA_BF16) return SA_ERR_UNSUPPORTED;
+  if (q_dtype == SA_MXFP4) return SA_ERR_UNSUPPORTED;
+  if (q_dtype != SA_F32 && q_dtype != SA_BF16) return SA_ERR_INVALID_ARG;
   if (HI <= 0 || dI <= 0 || !q_idx || !w || !ik_c) return SA_ERR_INVALID_ARG;
   if (!aligned16(q_idx) || !aligned16(w) || !aligned16(ik_c)) return SA_ERR_INVALID_ARG;
   (void)q_scales;

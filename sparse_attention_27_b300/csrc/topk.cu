@@ -1,4 +1,4 @@
-// Per-query top-k of the indexer scores: exact, deterministic radix select.
+// Per-query top-k of the indexer scores: exact and deterministic.
 //
 // Source: "오픈소스 LLM의 새 이정표: DeepSeek-V4 시리즈", section
 // "압축 희소 어텐션(CSA)과 극압축 어텐션(HCA)" (each query attends only its top-k
@@ -7,231 +7,34 @@
 // index and the output is in ascending index order (readings where the pages
 // are silent).
 //
-// Rows use topk_rows_kernel (a row split over a cluster of up to 16 CTAs, one
-// histogram pass and an exact select inside one bin; see there).  Rows longer
-// than it holds: the row's candidates are split over a thread-block cluster of
-// C CTAs (C = 1 while the row fits one CTA's shared memory); CTA c keeps the order-
-// preserving 32-bit keys of candidates [c*chunk, (c+1)*chunk) in shared
-// memory.  Three radix passes (11, 11, 10 bits, most significant first) find
-// the exact k-th largest key T: each CTA histograms the keys that still match
-// the prefix chosen so far (one shared-memory atomic per key), the C
-// histograms are summed through distributed shared memory, and every CTA
-// picks the digit where the count of larger keys first reaches the remaining
-// quota.  Then every key > T is kept and, of the keys
-// == T, the lowest indices fill what is left of k.  The output position of
-// candidate i is (#keys > T before i) + min(#keys == T before i, quota), so
-// each CTA compacts its slice in index order, 1024 keys at a time with warp
-// ballots: the output comes out sorted without a sort.
+// One kernel, topk_rows_kernel: a row's candidates are split over a cluster of
+// up to 16 CTAs, one histogram pass finds the bin of the k-th largest key, an
+// exact select runs inside that bin, and the output is emitted in index order
+// with warp ballots (see there).
 #include "kernels.cuh"
 
 namespace sa {
 
-constexpr int kTopkThreads = 1024;
-constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kBins = 2048;
-constexpr int kMaxChunk = 49152;      // keys per CTA in shared memory (192 KB)
-constexpr int kMaxCluster = 8;        // portable cluster size
+constexpr int kTopkWarpsMax = 32;          // warps of the largest CTA (1024 threads)
+constexpr int kBins = 2048;                // radix pass histogram (11 bits)
 
 struct TopkSmem {
   int hist[2][kBins];
-  int scan[kTopkWarps + 1];
-  int wgt[2 * kTopkWarps], weq[kTopkWarps];   // per-warp counts / min-max scratch
+  int scan[kTopkWarpsMax + 1];
   __align__(8) int cnt[2];                // this CTA: keys > T, keys == T
   int nan_flag;
-  int wg[kTopkWarps], we[kTopkWarps];     // row kernel: per-warp keys > T, keys == T
-  int wc[kTopkWarps];                     // row kernel: per-warp keys in the selected bin
-  int gsum[64];                           // row kernel: the 13-bit histogram in 64 groups
+  int wg[kTopkWarpsMax], we[kTopkWarpsMax];   // per-warp keys > T, keys == T
+  int wc[kTopkWarpsMax];                  // per-warp keys in the selected bin
+  int gsum[64];                           // the 13-bit histogram in 64 groups
   int sel_bin, above;
-  int ncand, take;                        // row kernel: keys in the selected bin, ties kept
-  uint32_t T;                             // row kernel: the k-th largest key
+  int take;                               // keys equal to T that are kept
+  uint32_t T;                             // the k-th largest key
 };
 
 __device__ __forceinline__ unsigned lanemask_lt() {
   unsigned m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
   return m;
-}
-
-// Sum of `v` over the CTA, returned to every thread.
-__device__ __forceinline__ int block_sum(int v, int* scratch) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if (lane == 0) scratch[w] = v;
-  __syncthreads();
-  int t = lane < kTopkWarps ? scratch[lane] : 0;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-  __syncthreads();
-  return t;
-}
-
-template <bool kCluster>
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a, int C, int chunk) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  TopkSmem& S = *reinterpret_cast<TopkSmem*>(smem_raw);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + sizeof(TopkSmem));
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rank = kCluster ? (int)cluster_rank() : 0;
-  const int64_t row = blockIdx.x / C;
-  const int k = a.k;
-  int32_t* out = a.idx + row * k;
-  const int p = __ldg(a.q_pos + row);
-  int64_t n = p < 0 ? 0 : ((int64_t)p + 1) / a.m;
-  if (n > a.N_cap) {
-    if (rank == 0 && tid == 0) set_err(a.err, SA_ERR_BOUNDS);
-    n = a.N_cap;
-  }
-  if (n <= k) {                                   // everything visible is selected
-    for (int64_t i = (int64_t)rank * kTopkThreads + tid; i < k; i += (int64_t)C * kTopkThreads)
-      out[i] = i < n ? (int32_t)i : -1;
-    return;
-  }
-  auto csync = [&]() {
-    if constexpr (kCluster) cluster_sync(); else __syncthreads();
-  };
-  auto remote = [&](const void* p_, int r) -> const void* {
-    if constexpr (kCluster) return __cluster_map_shared_rank(p_, r);
-    else return p_;
-  };
-
-  const int64_t lo = (int64_t)rank * chunk;
-  const int cnt = (int)max64(0, min64(n, lo + chunk) - lo);
-  const float* src = a.scores + row * a.ld + lo;
-  int nan_local = 0;
-  for (int i = tid; i < cnt; i += kTopkThreads) {
-    const float f = src[i];
-    nan_local |= is_nan_bits(f);
-    keys[i] = score_key(f);
-  }
-  nan_local = __syncthreads_or(nan_local);
-  if (tid == 0) S.nan_flag = nan_local;
-
-  uint32_t prefix = 0, maskbits = 0;
-  int krem = k;
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const int nb = pass == 2 ? 1024 : 2048;
-    int* h = S.hist[pass & 1];
-    for (int i = tid; i < nb; i += kTopkThreads) h[i] = 0;
-    __syncthreads();
-    for (int i0 = 0; i0 < cnt; i0 += kTopkThreads) {
-      const int i = i0 + tid;
-      const bool in = i < cnt;
-      const uint32_t key = in ? keys[i] : 0u;
-      if (in && (key & maskbits) == prefix) atomicAdd(&h[(key >> shift) & (uint32_t)(nb - 1)], 1);
-    }
-    __syncthreads();
-    csync();
-    if (pass == 0) {
-      int any_nan = 0;
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r)
-        if (r < C) any_nan |= *static_cast<const int*>(remote(&S.nan_flag, r));
-      if (any_nan) {                              // reject the row: all -1
-        if (rank == 0 && tid == 0) set_err(a.err, SA_ERR_NAN);
-        for (int64_t i = (int64_t)rank * kTopkThreads + tid; i < k; i += (int64_t)C * kTopkThreads)
-          out[i] = -1;
-        csync();                                  // peers may still read our smem
-        return;
-      }
-    }
-    // Sum the C histograms.  Counting from the top digit down, thread t owns
-    // bins nb-1-per*t .. nb-per*(t+1) (per = 2 for nb = 2048, 1 for 1024):
-    // one 8- or 4-byte load from every CTA of the cluster, all issued before
-    // any is used.
-    const int per = nb / kTopkThreads;
-    int loc0 = 0, loc1 = 0;
-    if (per == 2) {
-      int2 v[kMaxCluster];
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r)
-        if (r < C) v[r] = *static_cast<const int2*>(
-                       remote(reinterpret_cast<const int2*>(h + nb - 2 * (tid + 1)), r));
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r)
-        if (r < C) { loc0 += v[r].y; loc1 += v[r].x; }
-    } else {
-      int v[kMaxCluster];
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r)
-        if (r < C) v[r] = *static_cast<const int*>(remote(h + nb - 1 - tid, r));
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r)
-        if (r < C) loc0 += v[r];
-    }
-    const int base = block_exclusive_scan<kTopkThreads>(loc0 + loc1, S.scan, nullptr);
-    {
-      const int b0 = nb - 1 - tid * per;          // loc0 is bin b0, loc1 bin b0 - 1
-      if (base < krem && base + loc0 >= krem) { S.sel_bin = b0; S.above = base; }
-      if (per == 2) {
-        const int before = base + loc0;
-        if (before < krem && before + loc1 >= krem) { S.sel_bin = b0 - 1; S.above = before; }
-      }
-    }
-    __syncthreads();
-    krem -= S.above;
-    prefix |= (uint32_t)S.sel_bin << shift;
-    maskbits |= (uint32_t)(nb - 1) << shift;
-    __syncthreads();
-  }
-  const uint32_t T = prefix;                      // the k-th largest key; take krem of the == T
-
-  // ---- counts of this CTA's slice, then of the CTAs before it
-  int n_gt = 0, n_eq = 0;
-  for (int i = tid; i < cnt; i += kTopkThreads) {
-    n_gt += keys[i] > T;
-    n_eq += keys[i] == T;
-  }
-  const int gt_total = block_sum(n_gt, S.scan);
-  const int eq_total = block_sum(n_eq, S.scan);
-  if (tid == 0) { S.cnt[0] = gt_total; S.cnt[1] = eq_total; }
-  __syncthreads();
-  csync();
-  int eq_before = 0, gt_before = 0;
-  if constexpr (kCluster) {
-    int2 v[kMaxCluster];
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r)
-      if (r < rank) v[r] = *static_cast<const int2*>(remote(reinterpret_cast<const int2*>(S.cnt), r));
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r)
-      if (r < rank) { gt_before += v[r].x; eq_before += v[r].y; }
-  }
-
-  // ---- compaction in index order, kTopkThreads keys per round.  Candidate i
-  // (key > T, or key == T with eq(<i) < krem) goes to gt(<i) + min(eq(<i), krem),
-  // with gt/eq counted over the whole row.
-  int run_gt = gt_before, run_eq = eq_before;
-  for (int i0 = 0; i0 < cnt; i0 += kTopkThreads) {
-    const int i = i0 + tid;
-    const uint32_t key = i < cnt ? keys[i] : 0u;
-    const bool gt = i < cnt && key > T;
-    const bool eq = i < cnt && key == T;
-    const unsigned bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
-    if (lane == 0) { S.wgt[warp] = __popc(bg); S.weq[warp] = __popc(be); }
-    __syncthreads();
-    const int cg = lane < kTopkWarps ? S.wgt[lane] : 0;
-    const int ce = lane < kTopkWarps ? S.weq[lane] : 0;
-    int xg = cg, xe = ce;                         // inclusive scan over the warps
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int yg = __shfl_up_sync(0xffffffffu, xg, o), ye = __shfl_up_sync(0xffffffffu, xe, o);
-      if (lane >= o) { xg += yg; xe += ye; }
-    }
-    const int pg = __shfl_sync(0xffffffffu, xg - cg, warp);   // keys of the warps before
-    const int pe = __shfl_sync(0xffffffffu, xe - ce, warp);
-    const int tg = __shfl_sync(0xffffffffu, xg, 31);          // this round's totals
-    const int te = __shfl_sync(0xffffffffu, xe, 31);
-    const int g_lt = run_gt + pg + __popc(bg & lanemask_lt());
-    const int e_lt = run_eq + pe + __popc(be & lanemask_lt());
-    if (gt) out[g_lt + min(e_lt, krem)] = (int32_t)(lo + i);
-    else if (eq && e_lt < krem) out[g_lt + e_lt] = (int32_t)(lo + i);
-    run_gt += tg;
-    run_eq += te;
-    __syncthreads();                              // per-warp counts are rewritten next round
-  }
-  if constexpr (kCluster) cluster_sync();         // keep smem alive for peers' DSMEM reads
 }
 
 // ------------------------------------------------------------------------
@@ -783,13 +586,14 @@ static cudaError_t launch_rows(const TopkArgs& a, int C, int chunk, cudaStream_t
   return cudaLaunchKernelEx(&cfg, kern, a, C, chunk);
 }
 
-bool topk_supported(int N_cap) { return N_cap <= kMaxChunk * kMaxCluster; }
+bool topk_supported(int N_cap) { return N_cap <= kRowsMaxCluster * 1024 * kKplMax; }
 
 cudaError_t launch_topk(const TopkArgs& a, int num_sms, cudaStream_t st) {
   if (a.rows <= 0) return cudaSuccess;
   // Cluster size: the largest power of two (at most 16) that keeps one wave
   // (rows * C <= SMs) and at least 4096 candidates per CTA; then the fewest
-  // threads and keys per thread that hold a CTA's share.
+  // threads and keys per thread that hold a CTA's share.  A row that no
+  // cluster size the device runs can hold is not supported.
   int C = 1;
   while (2 * C <= kRowsMaxCluster && (int64_t)a.rows * 2 * C <= num_sms &&
          a.N_cap / (2 * C) >= 4096)
@@ -813,37 +617,7 @@ cudaError_t launch_topk(const TopkArgs& a, int num_sms, cudaStream_t st) {
     }
     if (e != cudaErrorNotSupported) return e;
   }
-  // rows longer than the cluster kernels hold: radix select over a cluster of
-  // C CTAs of kMaxChunk keys each
-  int Cr = 1;
-  while ((int64_t)Cr * kMaxChunk < a.N_cap) Cr *= 2;
-  if (Cr > kMaxCluster) return cudaErrorInvalidValue;
-  int chunk = (a.N_cap + Cr - 1) / Cr;
-  chunk = (chunk + 31) & ~31;
-  const size_t smem = sizeof(TopkSmem) + sizeof(uint32_t) * (size_t)chunk;
-  if (Cr == 1) {
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    topk_kernel<false><<<(unsigned)a.rows, kTopkThreads, smem, st>>>(a, 1, chunk);
-    return cudaGetLastError();
-  }
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(Cr * a.rows));
-  cfg.blockDim = dim3(kTopkThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = Cr;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, topk_kernel<true>, a, Cr, chunk);
+  return cudaErrorNotSupported;
 }
 
 }  // namespace sa

@@ -28,6 +28,7 @@ from __future__ import annotations
 
 from dataclasses import dataclass
 
+import numpy as np
 import torch
 
 from . import (SA_BF16, SA_F32, SA_MXFP4, csa_attend, csa_attend_workspace_bytes, csa_compress,
@@ -57,6 +58,7 @@ class Dims:
     sm_scale: float
     max_blocks: int     # bound on CSA blocks compressed per sequence this pass
     max_blocks2: int    # bound on HCA blocks compressed per sequence this pass
+    o_dtype: str = "f32"  # attention output O of both layers: "f32" or "bf16"
 
 
 class HybridStep:
@@ -66,7 +68,8 @@ class HybridStep:
         rows = D.B * D.T
         dev = torch.device(device)
         self.idx = torch.empty((D.B, D.T, D.k), dtype=torch.int32, device=dev)
-        self.o = torch.empty((D.B, D.T, D.H, D.d), dtype=torch.float32, device=dev)
+        odt = torch.bfloat16 if D.o_dtype == "bf16" else torch.float32
+        self.o = torch.empty((D.B, D.T, D.H, D.d), dtype=odt, device=dev)
         self.lse = torch.empty((D.B, D.T, D.H), dtype=torch.float32, device=dev)
         self.ho = torch.empty_like(self.o)
         self.hlse = torch.empty_like(self.lse)
@@ -172,3 +175,68 @@ class HybridStep:
 
     def device_errors(self) -> int:
         return int(self.err.item())
+
+
+# ------------------------------------------------------------ host arrays
+# Helpers that upload one pass's inputs, given as numpy arrays in the
+# storage formats of the C ABI (bf16 as uint16 bit patterns, f32, int32),
+# and build the HybridStep that runs them.  ``w`` is any object with the
+# shape fields of a workload (B, T, H, d, HI, dI, m, k, W, m2, ring, ncap,
+# ncap2, dtype, indexer, sm_scale, mode).
+
+def to_device(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """numpy -> device tensor; uint16 arrays are bfloat16 bit patterns."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+def to_host(t: torch.Tensor) -> np.ndarray:
+    """device tensor -> numpy; bfloat16 comes back as uint16 bit patterns."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def dims_from(w, x: dict, o_dtype: str = "f32") -> Dims:
+    """The Dims of one pass: shapes from ``w``, compression bounds from the
+    block ranges in ``x``."""
+    return Dims(o_dtype=o_dtype, B=w.B, T=w.T, H=w.H, d=w.d, HI=w.HI, dI=w.dI, m=w.m, k=w.k, W=w.W, m2=w.m2,
+                R=w.ring, ncap=w.ncap, ncap2=w.ncap2, dtype=w.dtype, indexer=w.indexer,
+                sm_scale=w.sm_scale,
+                max_blocks=int((x["blk_hi"] - x["blk_lo"]).max()),
+                max_blocks2=int((x["hblk_hi"] - x["hblk_lo"]).max()))
+
+
+def device_inputs(w, x: dict, device="cuda") -> dict:
+    """Every array of ``x`` on the device.  An MXFP4 indexer keeps its key
+    cache as codes and scales, written by the library's quantiser from the
+    given bf16 cache (or zero for a prefill, whose compressor writes them).
+    A prefill gets zeroed caches for its compressors to fill."""
+    from . import sa_mxfp4_quantize
+    t = {k: to_device(v, device) for k, v in x.items()}
+    if w.indexer == "mxfp4":
+        ik = t.pop("ik_c", None)
+        codes = torch.zeros((w.B, w.ncap, w.dI // 2), dtype=torch.uint8, device=device)
+        scales = torch.zeros((w.B, w.ncap, w.dI // 32), dtype=torch.uint8, device=device)
+        if ik is not None:
+            sa_mxfp4_quantize(ik, codes, scales)
+        t["ik_c"], t["ik_c_scales"] = codes, scales
+    if w.mode == "prefill":
+        cdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        idt = torch.bfloat16 if w.indexer in ("bf16", "mxfp4") else torch.float32
+        t["k_c"] = torch.zeros((w.B, w.ncap, w.d), dtype=cdt, device=device)
+        t["v_c"] = torch.zeros_like(t["k_c"])
+        if w.indexer != "mxfp4":
+            t["ik_c"] = torch.zeros((w.B, w.ncap, w.dI), dtype=idt, device=device)
+        t["hk_c"] = torch.zeros((w.B, w.ncap2, w.d), dtype=cdt, device=device)
+        t["hv_c"] = torch.zeros_like(t["hk_c"])
+    return t
+
+
+def step_from(w, x: dict, device="cuda", o_dtype: str = "f32") -> HybridStep:
+    """A HybridStep over ``x`` uploaded to ``device``, with attention outputs
+    in ``o_dtype``."""
+    return HybridStep(dims_from(w, x, o_dtype), device_inputs(w, x, device), device)

@@ -109,3 +109,13 @@ def test_attention_workspace_queries_follow_the_split_rule():
     assert m.csa_attend_workspace_bytes(m.SA_BF16, 1, 65536, 64, 128, 2048, 128) == ws(65536, 2)
     # fp32 (CUDA-core kernel, one item per CTA): 256 rows fill the SMs, no split
     assert m.csa_attend_workspace_bytes(m.SA_F32, 1, 256, 16, 128, 64, 128) == 0
+
+
+def test_noalloc_limit_matches_the_header():
+    """The Python binding's copy of the no-allocation call's size limit is the
+    value include/sa.h gives the library's device array."""
+    import sparse_attention_27_b300 as m
+    src = open(os.path.join(ROOT, "include", "sa.h")).read()
+    got = re.search(r"#define\s+SA_NOALLOC_MAX_SCORES\s+(\d+)", src)
+    assert got is not None
+    assert int(got.group(1)) == m.NOALLOC_MAX_SCORES

@@ -92,6 +92,10 @@ def test_algorithmic_bytes_of_the_workloads():
     # 1M decode: 262144 indexer rows per sequence dominate
     m1 = bench.algorithmic_bytes(synth.WORKLOADS["decode1m"])
     assert m1["index"] == 4 * (262144 * 128 + 64 * 128 + 64 * 4)
+    # O written in bf16: 64 x 128 x 2 bytes fewer per layer and sequence
+    ab16 = bench.algorithmic_bytes(synth.WORKLOADS["decode128k"], o_bytes=2)
+    assert ab16["index"] == ab["index"]
+    assert ab["step"] - ab16["step"] == 32 * 2 * 64 * 128 * 2
 
 
 def test_prefill_pairs_of_the_64k_chunk():

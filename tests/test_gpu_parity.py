@@ -403,3 +403,33 @@ def test_prefill64k_full_size_sampled_rows():
                                      g.choice(w.T, 512, replace=False)]))
     r = run_staged(w, x, rows=rows)
     assert r["recall"] >= 0.99, r
+
+
+@pytest.mark.parametrize("L,B,k,m2", [(20003, 3, 256, 128), (70000, 1, 64, 16)])
+def test_bf16_output_is_the_rounded_f32_output(L, B, k, m2):
+    """csa_attend and hca_compress_attend with a bf16 O: the same kernels and
+    splits as with an f32 O, rounded to nearest-even at the store, so the
+    bf16 output is bit-identical to the f32 output rounded to bf16, and
+    within 2e-2 of the oracle (the second shape splits the HCA row over many
+    CTAs, so the rounding happens in the split merge)."""
+    w = synth.Workload("decO", "decode", B=B, L=L, T=1, R=128, k=k, m2=m2, x8=True)
+    x = synth.make_inputs(w)
+    f32 = make_step(w, x)
+    f32.run()
+    b16 = make_step(w, x, o_dtype="bf16")
+    b16.run()
+    torch.cuda.synchronize()
+    assert f32.device_errors() == 0 and b16.device_errors() == 0
+    np.testing.assert_array_equal(host(b16.idx), host(f32.idx))
+    for name in ("o", "ho"):
+        want = host(getattr(f32, name).to(torch.bfloat16))
+        np.testing.assert_array_equal(host(getattr(b16, name)), want, err_msg=name)
+    for name in ("lse", "hlse"):
+        np.testing.assert_array_equal(host(getattr(b16, name)), host(getattr(f32, name)))
+    ref = oracle.reference(w, x)
+    same = [b for b in range(w.B) if np.array_equal(host(b16.idx)[b, 0], ref["idx"][b])]
+    o = synth.bf16_bits_to_f32(host(b16.o)).reshape(ref["o"].shape).astype(np.float64)
+    ho = synth.bf16_bits_to_f32(host(b16.ho)).reshape(ref["ho"].shape).astype(np.float64)
+    if same:
+        assert np.abs(o[same] - ref["o"][same]).max() <= TOL_ATT["bf16"]
+    assert np.abs(ho - ref["ho"]).max() <= TOL_ATT["bf16"]

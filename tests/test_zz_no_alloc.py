@@ -6,8 +6,9 @@ device array inside the library instead of a caller workspace.
 
 The GPU test checks that, called through the C ABI, it selects exactly the
 indices csa_index_topk selects on the same inputs, on two calls in a row
-with different inputs (the second call reuses the array the first one
-filled).  Index sets are integer results of the same kernels, so the
+with different shapes and inputs (the second call reuses the array the first
+one filled, with a different row stride), and that a call leaves the
+device's free memory unchanged.  Index sets are integer results of the same kernels, so the
 comparison is exact.  This file is named to be collected last."""
 from __future__ import annotations
 
@@ -42,20 +43,34 @@ def _with_workspace(m, w, t):
 
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_call_twice():
+    """Two calls in a row with different shapes: the second has fewer entries
+    per sequence (a shorter row stride in the shared score array) and a
+    shorter causal range than the first, so a top-k that read a score left in
+    the array by the first call would select differently.  Each call's
+    indices must equal csa_index_topk's on a fresh workspace, and the second
+    call must not change the device's free memory."""
     import torch
     import sparse_attention_27_b300 as m
     from gpu_util import host
     lib = ctypes.CDLL(m.LIB_PATH)
     assert hasattr(lib, "csa_index_topk_noalloc")
-    # decode at 128K context for 8 sequences: 8 * 32768 scores, within the limit
-    w = synth.Workload("noalloc", "decode", B=8, L=131072, T=1, R=128, x8=True)
-    assert w.B * w.T * w.ncap <= m.NOALLOC_MAX_SCORES
-    for shift in (0, 1):                 # two calls in a row, different inputs
-        t = _inputs(w, shift)
+    # 8 sequences at 128K context (32768 entries each), then 5 at 100003
+    # tokens (25000 entries): both within the array's 2,097,152 scores
+    cases = [synth.Workload("noalloc", "decode", B=8, L=131072, T=1, R=128, x8=True),
+             synth.Workload("noalloc2", "decode", B=5, L=100003, T=1, R=128, x8=True)]
+    for i, w in enumerate(cases):
+        assert w.B * w.T * w.ncap <= m.NOALLOC_MAX_SCORES
+        t = _inputs(w, i)
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
         m.csa_index_topk_noalloc(m.SA_BF16, w.B, w.T, w.HI, w.dI, w.m, w.k, t["q_idx"], None,
                                  t["w_idx"], t["ik_c"], None, w.ncap, t["q_pos"], t["idx"],
                                  err=err)
+        torch.cuda.synchronize()
+        free_after = torch.cuda.mem_get_info()[0]
+        if i > 0:      # the first call may load the library's device code
+            assert free_after == free_before, (free_before, free_after)
         want, err_ref = _with_workspace(m, w, t)
         torch.cuda.synchronize()
         assert int(err.item()) == 0 and int(err_ref.item()) == 0
