@@ -50,6 +50,10 @@ def peaks():
 # recorded with it (a changed kernel has no valid traffic figure).
 SCORE_SOURCES = ["sparse_attention_27_b300/csrc/score_tc.cu", "sparse_attention_27_b300/csrc/common.cuh",
                  "sparse_attention_27_b300/csrc/kernels.cuh"]
+FUSED_SOURCES = ["sparse_attention_27_b300/csrc/decode_fused.cu",
+                 "sparse_attention_27_b300/csrc/common.cuh", "sparse_attention_27_b300/csrc/kernels.cuh",
+                 "sparse_attention_27_b300/csrc/topk_dev.cuh",
+                 "sparse_attention_27_b300/csrc/compress_dev.cuh"]
 MX_SOURCES = ["sparse_attention_27_b300/csrc/score_mx.cu", "sparse_attention_27_b300/csrc/common.cuh",
               "sparse_attention_27_b300/csrc/kernels.cuh", "sparse_attention_27_b300/csrc/score_jobs.cuh"]
 
@@ -143,7 +147,8 @@ def algorithmic_bytes(w, o_bytes: int = 4) -> dict:
                    + w.k * 4 + w.H * w.d * o_bytes + w.H * 4)
     per_seq_hca = (w.ncap2 * 2 * w.d * e + w.W * 2 * w.d * e + w.H * w.d * e
                    + w.H * w.d * o_bytes + w.H * 4)
-    return dict(index=per_seq_index * w.B, step=(per_seq_csa + per_seq_hca) * w.B)
+    return dict(index=per_seq_index * w.B, csa=per_seq_csa * w.B, hca=per_seq_hca * w.B,
+                step=(per_seq_csa + per_seq_hca) * w.B)
 
 
 def prefill_pairs(w, pos) -> dict:
@@ -450,13 +455,16 @@ def run_reference(args) -> None:
 
 
 def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int,
-                   e2e: bool = True) -> dict:
+                   e2e: bool = True, schedule: str = "auto") -> dict:
     """Time the decode step of workload ``w`` (inputs already resident in HBM):
     the whole step (one CUDA graph, CSA and HCA on two streams), the
     dominant kernel alone (the indexer scoring call as a one-node graph) and
     the step end to end (inputs from pinned host memory, outputs back).  L2 is
     flushed before every timed replay; every replay is timed with CUDA events
-    on the launching stream.  Returns the measurement as a dict."""
+    on the launching stream.  ``schedule``: "fused" runs the CSA layer as one
+    csa_decode launch, "split" as csa_compress, the indexer's score and top-k
+    calls and csa_attend; "auto" takes the fused one where csa_decode applies.
+    Returns the measurement as a dict."""
     import torch
     import synth
     import sparse_attention_27_b300 as sa
@@ -466,13 +474,15 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
     step = step_from(w, x, o_dtype="bf16")
     io = StepIO(step, x, w)         # packs per-step inputs and outputs (before capture)
     s_csa, s_hca = torch.cuda.Stream(), torch.cuda.Stream()
+    fused = schedule == "fused" or (schedule == "auto" and step.fused_ok())
+    run_step = step.run_fused_two_streams if fused else step.run_two_streams
     for _ in range(2):              # outside the graph: sets kernel attributes, loads modules
-        step.run_two_streams(s_csa, s_hca)
+        run_step(s_csa, s_hca)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph(keep_graph=True)
     cap = torch.cuda.Stream()
     with torch.cuda.graph(g, stream=cap):
-        step.run_two_streams(s_csa, s_hca)
+        run_step(s_csa, s_hca)
     # the step's kernel launches: the captured graph's kernel nodes (the step
     # issues only library calls and event edges, so every kernel node is ours)
     kernels = graph_kernels(g.raw_cuda_graph(), io.cudart)
@@ -512,12 +522,16 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
     errs = step.device_errors()
     value = world * w.B * w.T * steps / (total_ms / 1e3)
 
-    # ---- dominant kernel: indexer scoring alone (csa_index_topk with k = 0)
+    # ---- dominant kernel alone: the fused CSA layer (csa_decode), or the
+    # indexer's scoring call (csa_index_topk with k = 0) of the split schedule
     D = step.D
     sc = torch.empty((w.B, w.T, w.ncap), dtype=torch.float32, device="cuda")
     mx = w.indexer == "mxfp4"
 
     def score_only():
+        if fused:
+            step.csa_fused()
+            return
         if mx:   # the step has already quantised this token's indexer queries
             sa.csa_index_topk(sa.SA_MXFP4, D.B, D.T, D.HI, D.dI, D.m, 0, step.q_codes,
                               step.q_scales, step.x["w_idx"], step.x["ik_c"],
@@ -538,10 +552,14 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
     k_avg = sum(k_ms) / len(k_ms)
     ab = algorithmic_bytes(w, o_bytes=2)
     peak, peak_kind = peaks()
-    achieved = ab["index"] / (k_avg / 1e3) / 1e9
-    score_kernel = "score_mx_kernel" if mx else "score_tc_kernel"
-    traffic, traffic_note = recorded_traffic(score_kernel, MX_SOURCES if mx else SCORE_SOURCES,
-                                             ab["index"])
+    k_bytes = ab["csa"] if fused else ab["index"]
+    achieved = k_bytes / (k_avg / 1e3) / 1e9
+    score_kernel = ("csa_decode_kernel" if fused else
+                    "score_mx_kernel" if mx else "score_tc_kernel")
+    k_call = ("csa_decode, the whole CSA layer, one-node graph" if fused else
+              "csa_index_topk scores, k=0, one-node graph")
+    traffic, traffic_note = recorded_traffic(
+        score_kernel, FUSED_SOURCES if fused else MX_SOURCES if mx else SCORE_SOURCES, k_bytes)
     step_gbs = ab["step"] / (total_ms / steps / 1e3) / 1e9
 
     # ---- end to end: host (pinned) inputs of the new token in, outputs out
@@ -563,7 +581,10 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
             io.d2h("hca", s_hca)
             io.h2d("csa", s_csa)
             s_csa.wait_event(pos_in)
-            step.csa(s_csa)
+            if fused:
+                step.csa_fused(s_csa)
+            else:
+                step.csa(s_csa)
             io.d2h("csa", s_csa)
             e1, e2 = torch.cuda.Event(), torch.cuda.Event()
             e1.record(s_csa)
@@ -591,15 +612,18 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
                    "indexer_heads": w.HI, "indexer": w.indexer, "o_dtype": "bf16",
                    "parallelism": f"replicas x{world}",
                    "l2": "flushed before every timed step: a 512 MiB write, then a 256 MiB read",
-                   "graph": "one CUDA graph per step, CSA and HCA on two streams, HCA after "
-                            "the CSA scores"},
+                   "schedule": "fused" if fused else "split",
+                   "graph": ("one CUDA graph per step, the CSA layer as one csa_decode launch "
+                             "and the HCA layer on two streams, both from the start" if fused
+                             else "one CUDA graph per step, CSA and HCA on two streams, HCA "
+                                  "after the CSA scores")},
         "step_algorithmic_bytes": ab["step"], "step_gbs": step_gbs,
         "step_frac_of_hbm": step_gbs / peak,
-        "roofline": {"kernel": f"{score_kernel} (csa_index_topk scores, k=0, one-node graph)",
+        "roofline": {"kernel": f"{score_kernel} ({k_call})",
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "traffic": traffic, "traffic_source": traffic_note,
-                     "avg_launch_ms": k_avg, "algorithmic_bytes_per_launch": ab["index"]},
+                     "avg_launch_ms": k_avg, "algorithmic_bytes_per_launch": k_bytes},
         "e2e": e2e_out, "gpu_launches": len(kernels) * steps,
         "step_ms": {"p10": pct(0.10), "median": statistics.median(ms), "p90": pct(0.90)},
         "kernels_per_step": len(kernels), "kernels": sorted(set(kernels)),
@@ -615,6 +639,9 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--schedule", default="auto", choices=["auto", "fused", "split"],
+                    help="the CSA layer as one csa_decode launch (fused), as its separate calls "
+                         "(split), or fused where csa_decode applies (auto)")
     ap.add_argument("--no-extra", action="store_true",
                     help="time only the headline workload (no 1M decode and 64K prefill objects)")
     ap.add_argument("--prefill-calls", action="store_true",
@@ -648,7 +675,8 @@ def main() -> None:
     w = synth.WORKLOADS[WORKLOAD]
     if world > 1:                   # every rank decodes its own sequences (seeded by rank)
         w = dataclasses.replace(w, seed=rank)
-    head, x = decode_measure(w, args.steps, args.warmup, rank, world, local)
+    head, x = decode_measure(w, args.steps, args.warmup, rank, world, local,
+                             schedule=args.schedule)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, x, seqs=w.B)
@@ -660,7 +688,8 @@ def main() -> None:
     extra = {}
     if WORKLOAD == "decode128k" and world == 1 and not args.no_extra:
         w1 = synth.WORKLOADS["decode1m"]
-        m1, x1 = decode_measure(w1, args.steps, args.warmup, rank, world, local)
+        m1, x1 = decode_measure(w1, args.steps, args.warmup, rank, world, local,
+                                schedule=args.schedule)
         if not args.no_cpu_baseline:
             m1["cpu_baseline"] = cpu_baseline(w1, x1, seqs=w1.B)
         del x1

@@ -220,6 +220,35 @@ size_t hca_compress_attend_workspace_bytes(int dtype, int B, int T, int H, int d
                                            int W);
 
 /* ---------------------------------------------------------------------------
+ * csa_decode -- the whole CSA layer for one new token per sequence, in one
+ * launch: csa_compress of the blocks [blk_lo[b], blk_hi[b]) this step closes,
+ * csa_index_topk and csa_attend, fused ([P2]; [P3] CSA steps 1-4 and "KV
+ * Cache 관리"; [P1] IDEAS: the mega-kernel direction).  Results are those of
+ * the three calls in sequence on the same inputs: the cache rows written and
+ * idx are bit-identical to theirs (same arithmetic, same order); o and lse
+ * differ only by the fp32 rounding of a different split of the key list.
+ * One query per sequence (T = 1): query b sits at position q_pos[b].
+ *  q [B,H,128] bf16 (H <= 64); q_idx [B,64,64] bf16; w [B,64] f32
+ *  k_raw, v_raw [B,R,128] bf16; ik_raw [B,R,64] bf16; z [B,R] f32 (R >= W, R >= m)
+ *  blk_lo, blk_hi [B] int32 device; max_blocks host bound on blk_hi - blk_lo
+ *  k_c, v_c [B,N_cap,128] bf16; ik_c [B,N_cap,64] bf16 (read, and the closed
+ *            blocks written); m <= 128; N_cap <= 262144
+ *  idx [B,k] int32 output; o [B,H,128] in o_dtype (SA_F32 or SA_BF16);
+ *  lse [B,H] f32
+ * No workspace: each sequence is one thread-block cluster of up to 16 CTAs
+ * that keeps its scores, its selection and its partial results in shared
+ * memory.  Fastest when B x (CTAs per cluster) fills the GPU (e.g. B = 32 at
+ * 128K context); SA_ERR_UNSUPPORTED if the device cannot run the cluster.
+ * Device errors as csa_compress, csa_index_topk and csa_attend.
+ */
+int csa_decode(int B, int H, int d, int HI, int dI, int m, int k, int W, float sm_scale,
+               const void* q, const void* q_idx, const float* w, const int32_t* q_pos,
+               const void* k_raw, const void* v_raw, const void* ik_raw, const float* z, int R,
+               const int32_t* blk_lo, const int32_t* blk_hi, int max_blocks, void* k_c,
+               void* v_c, void* ik_c, int N_cap, int32_t* idx, void* o, int o_dtype,
+               float* lse, int32_t* err, void* stream);
+
+/* ---------------------------------------------------------------------------
  * sa_mxfp4_quantize -- MXFP4 storage of bf16 rows for the low-precision
  * indexer path ([P2q]: the indexer QK path is stored in FP4 (MXFP4)).
  * Block rule of the OCP Microscaling Formats (MX) v1.0 specification: for

@@ -27,7 +27,7 @@ EXPORTS = (
     "sa_status_string", "csa_compress", "csa_index_topk", "csa_index_topk_workspace_bytes",
     "csa_attend", "csa_attend_workspace_bytes", "hca_compress_attend",
     "hca_compress_attend_workspace_bytes", "attn_merge", "csa_index_topk_noalloc",
-    "sa_mxfp4_quantize",
+    "sa_mxfp4_quantize", "csa_decode",
 )
 
 
@@ -54,6 +54,9 @@ _lib.csa_index_topk_workspace_bytes.restype = _sz
 _lib.csa_index_topk_noalloc.argtypes = [_i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i,
                                         _vp, _vp, _vp, _vp]
 _lib.sa_mxfp4_quantize.argtypes = [_vp, _i64, _vp, _vp, _vp]
+_lib.csa_decode.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                            _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp,
+                            _vp]
 _lib.csa_attend.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _i, _vp, _vp,
                             _vp, _i, _vp, _i, _vp, _vp, _sz, _vp, _vp]
 _lib.csa_attend_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
@@ -163,6 +166,17 @@ def hca_compress_attend(dtype, B, T, H, d, m2, W, sm_scale, q, q_pos, k_raw, v_r
                                     max_blocks, _p(hk_c), _p(hv_c), N2_cap, _p(o), _out_code(o),
                                     _p(lse), _p(ws), ws_bytes, _p(err), _stream(stream)),
            "hca_compress_attend")
+
+
+def csa_decode(B, H, d, HI, dI, m, k, W, sm_scale, q, q_idx, w, q_pos, k_raw, v_raw, ik_raw, z,
+               R, blk_lo, blk_hi, max_blocks, k_c, v_c, ik_c, N_cap, idx, o, lse, err=None,
+               stream=None):
+    """The fused CSA layer of one decode step; o: f32 or bf16 tensor [B,H,d]
+    (its dtype selects the output type)."""
+    _check(_lib.csa_decode(B, H, d, HI, dI, m, k, W, sm_scale, _p(q), _p(q_idx), _p(w),
+                           _p(q_pos), _p(k_raw), _p(v_raw), _p(ik_raw), _p(z), R, _p(blk_lo),
+                           _p(blk_hi), max_blocks, _p(k_c), _p(v_c), _p(ik_c), N_cap, _p(idx),
+                           _p(o), _out_code(o), _p(lse), _p(err), _stream(stream)), "csa_decode")
 
 
 def sa_mxfp4_quantize(x, codes, scales, stream=None):

@@ -263,6 +263,34 @@ int hca_compress_attend(int dtype, int B, int T, int H, int d, int m2, int W, fl
   return run_attention(a, ws, ws_bytes, attn_tiles(N2_cap, W), st);
 }
 
+int csa_decode(int B, int H, int d, int HI, int dI, int m, int k, int W, float sm_scale,
+               const void* q, const void* q_idx, const float* w, const int32_t* q_pos,
+               const void* k_raw, const void* v_raw, const void* ik_raw, const float* z, int R,
+               const int32_t* blk_lo, const int32_t* blk_hi, int max_blocks, void* k_c,
+               void* v_c, void* ik_c, int N_cap, int32_t* idx, void* o, int o_dtype,
+               float* lse, int32_t* err, void* stream) {
+  if (B < 0 || H < 1 || m < 1 || k < 0 || W < 0 || R < 1 || R < W || R < m || N_cap < 0 ||
+      max_blocks < 0 || !plain_dtype(o_dtype))
+    return SA_ERR_INVALID_ARG;
+  if (d != 128 || HI != 64 || dI != 64 || H > 64 || m > 128) return SA_ERR_UNSUPPORTED;
+  if (!q || !q_idx || !w || !q_pos || !k_raw || !v_raw || !ik_raw || !z || !blk_lo || !blk_hi ||
+      !k_c || !v_c || !ik_c || !o || !lse || (k > 0 && !idx))
+    return SA_ERR_INVALID_ARG;
+  if (!al16(q) || !al16(q_idx) || !al16(w) || !al16(k_raw) || !al16(v_raw) || !al16(ik_raw) ||
+      !al16(k_c) || !al16(v_c) || !al16(ik_c) || !al16(o))
+    return SA_ERR_INVALID_ARG;
+  if (B == 0) return SA_OK;
+  FusedDecodeArgs a{};
+  a.B = B; a.H = H; a.m = m; a.k = k; a.W = W; a.sm_scale = sm_scale;
+  a.q = q; a.q_idx = q_idx; a.w = w; a.q_pos = q_pos;
+  a.k_raw = k_raw; a.v_raw = v_raw; a.ik_raw = ik_raw; a.z = z; a.R = R;
+  a.blk_lo = blk_lo; a.blk_hi = blk_hi; a.max_blocks = max_blocks;
+  a.k_c = k_c; a.v_c = v_c; a.ik_c = ik_c; a.N_cap = N_cap;
+  a.idx = idx; a.o = o; a.o_dtype = o_dtype; a.lse = lse; a.err = err;
+  if (!fused_decode_plan(a, device_sms())) return SA_ERR_UNSUPPORTED;
+  return status_of(launch_fused_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
 int sa_mxfp4_quantize(const void* x, int64_t nblk, void* codes, void* scales, void* stream) {
   if (nblk < 0 || (nblk > 0 && (!x || !codes || !scales))) return SA_ERR_INVALID_ARG;
   if (nblk == 0) return SA_OK;

@@ -8,13 +8,15 @@
 // rule (softmax over one logit per raw token) is the reading taken where the
 // pages give none.
 //
-// One CTA per (sequence, block).  The CTA first turns the block's m logits
-// into weights in shared memory.  Each output row is cut into 16-byte chunks
-// (8 bf16 or 4 f32 channels of K, V or the indexer key); a thread owns one
-// chunk and one group of rows (all m rows for m = 4, m/8 rows for m' = 128),
-// accumulates in fp32 with 16-byte loads, and the row groups are added in
-// shared memory.  Memory-bound: each raw byte is read once, each output byte
+// One CTA per (sequence, block).  One warp turns the block's m logits into
+// weights in shared memory.  Each output row is cut into 16-byte chunks (8
+// bf16 or 4 f32 channels of K, V or the indexer key); a thread owns one
+// chunk and one of RG = min(m, 8) row groups, accumulates in fp32 with
+// 16-byte loads, and the row groups are added in shared memory in order --
+// the evaluation order compress_dev.cuh fixes, which the fused decode kernel
+// follows too.  Memory-bound: each raw byte is read once, each output byte
 // written once.
+#include "compress_dev.cuh"
 #include "kernels.cuh"
 
 namespace sa {
@@ -59,7 +61,7 @@ template <int DT>
 __global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressArgs a) {
   using S = Store<DT>;
   constexpr int kVec = 16 / S::kBytes;               // channels per 16-byte chunk
-  extern __shared__ float s_w[];                     // [m] pooling weights
+  extern __shared__ float s_w[];                     // [m] pooling weights, then partials
   const int b = blockIdx.y;
   const int lo = __ldg(a.blk_lo + b), hi = __ldg(a.blk_hi + b);
   const int64_t j = (int64_t)lo + blockIdx.x;
@@ -70,111 +72,57 @@ __global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressArgs
   }
   const int m = a.m, R = a.R;
   const int64_t p0 = j * m;
-  // ---- work split.  Thread (chunk c, row group g) accumulates rows
-  // i = g, g+RG, ... of one 16-byte output chunk; the RG partial sums are then
-  // added in shared memory in a fixed order.
+  // ---- work split: item (chunk c, row group g) computes partial g of one
+  // 16-byte output chunk (K, V or indexer key); the RG partials of a chunk are
+  // then added in order (compress_dev.cuh fixes the arithmetic).
   const int ckv = a.d / kVec;                         // chunks per K or V row
   const bool ik_plain = a.ik_raw != nullptr && a.ik_dtype != SA_MXFP4;
   const int cik = ik_plain ? a.dI / kVec : 0;
   const int nchunks = 2 * ckv + cik;
-  int RG = 1;
-  while (RG * 2 <= m && RG * 2 * nchunks <= (int)blockDim.x) RG *= 2;
+  const int RG = pool_groups(m);
+  const int nitems = RG * nchunks;
   float* s_part = s_w + m;                            // [RG][nchunks][kVec]
-  const int c = nchunks > 0 ? threadIdx.x % nchunks : 0;
-  const int g = nchunks > 0 ? threadIdx.x / nchunks : RG;
-  const void* src = nullptr;
-  void* dst = nullptr;
-  int width = 0, off = 0;
-  if (c < ckv) { src = a.k_raw; dst = a.k_c; width = a.d; off = c * kVec; }
-  else if (c < 2 * ckv) { src = a.v_raw; dst = a.v_c; width = a.d; off = (c - ckv) * kVec; }
-  else { src = a.ik_raw; dst = a.ik_c; width = a.dI; off = (c - 2 * ckv) * kVec; }
-  const bool worker = g < RG && nchunks > 0;
-  const char* base = worker ? static_cast<const char*>(src) + (int64_t)b * R * width * S::kBytes
-                            : nullptr;
-  // the first kPre rows of this thread are loaded before the pooling weights
-  // are known, so the two trips to memory overlap
-  constexpr int kPre = 16;
-  uint4 pre[kPre];
-#pragma unroll
-  for (int q = 0; q < kPre; ++q) {
-    const int i = g + q * RG;
-    if (worker && i < m) {
-      const int64_t slot = (p0 + i) % R;
-      pre[q] = __ldg(reinterpret_cast<const uint4*>(base + (slot * width + off) * S::kBytes));
+  auto chunk_of = [&](int c, const char*& src, char*& dst, int& width, int& off) {
+    const void* sp;
+    void* dp;
+    if (c < ckv) { sp = a.k_raw; dp = a.k_c; width = a.d; off = c * kVec; }
+    else if (c < 2 * ckv) { sp = a.v_raw; dp = a.v_c; width = a.d; off = (c - ckv) * kVec; }
+    else { sp = a.ik_raw; dp = a.ik_c; width = a.dI; off = (c - 2 * ckv) * kVec; }
+    src = static_cast<const char*>(sp) + (int64_t)b * R * width * S::kBytes;
+    dst = static_cast<char*>(dp) + ((int64_t)b * a.N_cap + j) * width * S::kBytes;
+  };
+  // the rows of this thread's items start their trip to memory before the
+  // pooling weights are known, so the two round trips overlap
+  for (int it = threadIdx.x; it < nitems; it += blockDim.x) {
+    const char* src; char* dst; int width, off;
+    chunk_of(it % nchunks, src, dst, width, off);
+    for (int i = it / nchunks; i < m; i += RG) {
+      const char* pr = src + ((p0 + i) % R) * width * S::kBytes + off * S::kBytes;
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(pr));
     }
   }
-
-  // ---- pooling weights: softmax of the block's logits
-  for (int i = threadIdx.x; i < m; i += blockDim.x)
-    s_w[i] = __ldg(a.z + (int64_t)b * R + (p0 + i) % R);
+  if (threadIdx.x < 32) pool_weights_warp(a.z + (int64_t)b * R, p0, m, R, s_w);
   __syncthreads();
-  __shared__ float s_mu, s_sum;
-  if (threadIdx.x < 32) {
-    float mu = -INFINITY;
-    for (int i = threadIdx.x; i < m; i += 32) mu = fmaxf(mu, s_w[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, o));
-    float sum = 0.f;
-    for (int i = threadIdx.x; i < m; i += 32) sum += expf(s_w[i] - mu);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (threadIdx.x == 0) { s_mu = mu; s_sum = sum; }
-  }
-  __syncthreads();
-  const float mu = s_mu, inv = 1.f / s_sum;
-  for (int i = threadIdx.x; i < m; i += blockDim.x) s_w[i] = expf(s_w[i] - mu) * inv;
-  __syncthreads();
-
-  // ---- weighted sums
-  if (worker) {
+  for (int it = threadIdx.x; it < nitems; it += blockDim.x) {
+    const int c = it % nchunks, g = it / nchunks;
+    const char* src; char* dst; int width, off;
+    chunk_of(c, src, dst, width, off);
     float acc[kVec];
-#pragma unroll
-    for (int e = 0; e < kVec; ++e) acc[e] = 0.f;
-    auto add_row = [&](const uint4& u, float wi) {
-      float f[kVec];
-      if constexpr (DT == SA_BF16) {
-        bf16x8_to_f32(u, f);
-      } else {
-        f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
-        f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
-      }
-#pragma unroll
-      for (int e = 0; e < kVec; ++e) acc[e] = fmaf(wi, f[e], acc[e]);
-    };
-#pragma unroll
-    for (int q = 0; q < kPre; ++q) {
-      const int i = g + q * RG;
-      if (i < m) add_row(pre[q], s_w[i]);
-    }
-#pragma unroll 4
-    for (int i = g + kPre * RG; i < m; i += RG) {
-      const int64_t slot = (p0 + i) % R;
-      add_row(__ldg(reinterpret_cast<const uint4*>(base + (slot * width + off) * S::kBytes)),
-              s_w[i]);
-    }
+    pool_partial<DT>(src, (int64_t)width * S::kBytes, off * S::kBytes, p0, m, R, s_w, g, RG, acc);
 #pragma unroll
     for (int e = 0; e < kVec; ++e) s_part[(g * nchunks + c) * kVec + e] = acc[e];
   }
   __syncthreads();
-  if (g == 0 && nchunks > 0) {
+  for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {
+    const char* src; char* dst; int width, off;
+    chunk_of(c, src, dst, width, off);
     float acc[kVec];
 #pragma unroll
     for (int e = 0; e < kVec; ++e) acc[e] = s_part[c * kVec + e];
-    for (int q = 1; q < RG; ++q)
+    for (int g = 1; g < RG; ++g)
 #pragma unroll
-      for (int e = 0; e < kVec; ++e) acc[e] += s_part[(q * nchunks + c) * kVec + e];
-    char* out = static_cast<char*>(dst) + (((int64_t)b * a.N_cap + j) * width + off) * S::kBytes;
-    if constexpr (DT == SA_BF16) {
-      uint32_t w4[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
-        w4[e] = *reinterpret_cast<uint32_t*>(&h);
-      }
-      *reinterpret_cast<uint4*>(out) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-    } else {
-      *reinterpret_cast<float4*>(out) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    }
+      for (int e = 0; e < kVec; ++e) acc[e] += s_part[(g * nchunks + c) * kVec + e];
+    store_chunk<DT>(dst + off * S::kBytes, acc);
   }
 
   // ---- indexer key stored as MXFP4: one warp per 32-element block
@@ -208,12 +156,27 @@ __global__ void mxfp4_quantize_kernel(const __nv_bfloat16* x, int64_t nblk, uint
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t st) {
   if (a.max_blocks <= 0) return cudaSuccess;
   dim3 grid(a.max_blocks, a.B);
-  // weights [m] + partial sums [RG <= 256/nchunks][nchunks][4 or 8 floats]
-  size_t smem = sizeof(float) * (a.m + 2 * kCompressThreads * 8);
-  if (a.dtype == SA_BF16)
+  // weights [m] + partial sums [RG][nchunks][16 bytes of floats]
+  const int vec = a.dtype == SA_BF16 ? 8 : 4;
+  const bool ik_plain = a.ik_raw != nullptr && a.ik_dtype != SA_MXFP4;
+  const int nchunks = 2 * a.d / vec + (ik_plain ? a.dI / vec : 0);
+  const size_t smem = sizeof(float) * ((size_t)a.m + (size_t)pool_groups(a.m) * nchunks * vec);
+  cudaError_t e;
+  if (a.dtype == SA_BF16) {
+    if (smem > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(compress_kernel<SA_BF16>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+            cudaSuccess)
+      return e;
     compress_kernel<SA_BF16><<<grid, kCompressThreads, smem, st>>>(a);
-  else
+  } else {
+    if (smem > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(compress_kernel<SA_F32>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+            cudaSuccess)
+      return e;
     compress_kernel<SA_F32><<<grid, kCompressThreads, smem, st>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -93,6 +93,42 @@ int attend_tc_items_per_sm();   // (row, split) items per SM the split choice ai
 // Merge nsplit partials per (row, head) into o/lse.
 cudaError_t launch_merge_splits(const AttnArgs& a, cudaStream_t st);
 
+// Fused CSA decode (csa_decode): one cluster of C CTAs per sequence, one
+// query token each.  All tensors bf16 unless stated.
+struct FusedDecodeArgs {
+  int B, H, m, k, W;
+  float sm_scale;
+  const void* q;        // [B, H, 128]
+  const void* q_idx;    // [B, 64, 64]
+  const float* w;       // [B, 64] f32
+  const int32_t* q_pos; // [B]
+  const void* k_raw;    // [B, R, 128]
+  const void* v_raw;
+  const void* ik_raw;   // [B, R, 64]
+  const float* z;       // [B, R] f32
+  int R;
+  const int32_t* blk_lo;
+  const int32_t* blk_hi;
+  int max_blocks;
+  void* k_c;            // [B, N_cap, 128] (blocks [blk_lo, blk_hi) written)
+  void* v_c;
+  void* ik_c;           // [B, N_cap, 64]
+  int N_cap;
+  int32_t* idx;         // [B, k] int32
+  void* o;              // [B, H, 128] in o_dtype
+  int o_dtype;
+  float* lse;           // [B, H] f32
+  int32_t* err;
+  // launch plan (fused_decode_plan)
+  int C;                // CTAs per cluster (one cluster per sequence)
+  int cap;              // key slots per CTA (8192 or 16384)
+  int selcap;           // selected-list slots per CTA
+  int stages_a;         // indexer-key stages (16 KB)
+  int stages_kv;        // K/V stages (32 KB)
+};
+bool fused_decode_plan(FusedDecodeArgs& a, int num_sms);
+cudaError_t launch_fused_decode(const FusedDecodeArgs& a, cudaStream_t st);
+
 struct MergeArgs {
   int n;
   const float* o_parts[8];

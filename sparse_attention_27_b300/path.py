@@ -5,6 +5,8 @@ prefill chunk) and issues, in order, the library calls of the two layer
 kinds:
 
   CSA layer:  csa_compress -> csa_index_topk -> csa_attend
+              (or csa_decode, the same layer in one launch, for one query
+              per sequence)
   HCA layer:  hca_compress_attend
 
 (CSA and HCA are different layers, interleaved in the model -- "오픈소스 LLM의
@@ -32,7 +34,7 @@ import numpy as np
 import torch
 
 from . import (SA_BF16, SA_F32, SA_MXFP4, csa_attend, csa_attend_workspace_bytes, csa_compress,
-               csa_index_topk, csa_index_topk_workspace_bytes, hca_compress_attend,
+               csa_decode, csa_index_topk, csa_index_topk_workspace_bytes, hca_compress_attend,
                hca_compress_attend_workspace_bytes, sa_mxfp4_quantize)
 
 _CODES = {"f32": SA_F32, "bf16": SA_BF16, "mxfp4": SA_MXFP4}
@@ -146,6 +148,22 @@ class HybridStep:
         self.index_topk(stream)
         self.attend_csa(stream)
 
+    def fused_ok(self) -> bool:
+        """Whether csa_decode takes this pass: one bf16 query per sequence
+        with the bf16 indexer, 64 x 64 indexer heads, head dim 128."""
+        D = self.D
+        return (D.T == 1 and D.dtype == "bf16" and D.indexer == "bf16" and D.HI == 64 and
+                D.dI == 64 and D.d == 128 and D.H <= 64)
+
+    def csa_fused(self, stream=None):
+        """The CSA layer in one launch (csa_decode): compress the blocks this
+        pass closes, index, top-k and attend."""
+        D, x = self.D, self.x
+        csa_decode(D.B, D.H, D.d, D.HI, D.dI, D.m, D.k, D.W, D.sm_scale, x["q"], x["q_idx"],
+                   x["w_idx"], x["q_pos"], x["k_raw"], x["v_raw"], x["ik_raw"], x["z"], D.R,
+                   x["blk_lo"], x["blk_hi"], D.max_blocks, x["k_c"], x["v_c"], x["ik_c"], D.ncap,
+                   self.idx, self.o, self.lse, err=self.err, stream=stream)
+
     def run(self, stream=None):
         """The whole pass on one stream."""
         self.csa(stream)
@@ -166,6 +184,22 @@ class HybridStep:
         self.index_topk_split(s_csa, scored)
         self.attend_csa(s_csa)
         s_hca.wait_event(scored)
+        self.hca(s_hca)
+        e1, e2 = torch.cuda.Event(), torch.cuda.Event()
+        e1.record(s_csa)
+        e2.record(s_hca)
+        cur.wait_event(e1)
+        cur.wait_event(e2)
+
+    def run_fused_two_streams(self, s_csa: torch.cuda.Stream, s_hca: torch.cuda.Stream):
+        """The CSA layer in one launch (csa_decode) on one stream and the HCA
+        layer on another, both starting at once (they share no buffer)."""
+        cur = torch.cuda.current_stream()
+        ev = torch.cuda.Event()
+        ev.record(cur)
+        s_csa.wait_event(ev)
+        s_hca.wait_event(ev)
+        self.csa_fused(s_csa)
         self.hca(s_hca)
         e1, e2 = torch.cuda.Event(), torch.cuda.Event()
         e1.record(s_csa)

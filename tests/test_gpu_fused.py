@@ -1,0 +1,144 @@
+"""GPU parity of csa_decode, the CSA layer of one decode step in one launch,
+through the C ABI.
+
+csa_decode must give the results of the three calls it fuses (csa_compress,
+csa_index_topk, csa_attend) on the same inputs:
+  * the cache rows it pools are bit-identical to csa_compress's (the same
+    fp32 evaluation order), and every other cache row is untouched;
+  * idx is bit-identical to csa_index_topk's (the same scores, the same
+    exact top-k), which the staged tests check against the oracle;
+  * O and LSE are within 2e-2 (bf16 inputs, fp32 accumulation) of the
+    float64 oracle's attention over the same selected rows and window.
+Shapes cover several tiles per CTA with a ragged last tile, rows whose
+visible entries are all selected (n <= k), rows where no block closes, very
+early positions (no compressed entry, a short window), k = 0 (window only),
+fewer heads than the MMA's 64, a NaN row, and the full 128K and 1M decode
+workloads.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import dev, host, make_step
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+
+
+def sa():
+    import sparse_attention_27_b300 as m
+    return m
+
+
+def oracle_attention_given_idx(w, x, idx, caches):
+    """The oracle's CSA attention of every row over the given selection."""
+    k_c, v_c = caches["k_c"], caches["v_c"]
+    pos = x["q_pos"].reshape(-1).astype(np.int64)
+    keys, vals = zip(*[oracle.csa_keys(b, int(pos[b]), idx[b], k_c, v_c, x["k_raw"],
+                                       x["v_raw"], w.W) for b in range(w.B)])
+    q = x["q"].reshape(w.B, w.H, w.d)
+    return oracle.attend(q, list(keys), list(vals), w.sm_scale)
+
+
+def run_both(w, x, o_dtype="f32"):
+    """(unfused step, fused step) after one pass each on the same inputs."""
+    ref = make_step(w, x, o_dtype=o_dtype)
+    ref.csa()
+    fus = make_step(w, x, o_dtype=o_dtype)
+    assert fus.fused_ok()
+    fus.csa_fused()
+    torch.cuda.synchronize()
+    return ref, fus
+
+
+def check_fused(w, x, expect_err=0, o_dtype="f32"):
+    ref, fus = run_both(w, x, o_dtype)
+    assert ref.device_errors() == expect_err and fus.device_errors() == expect_err, (
+        ref.device_errors(), fus.device_errors())
+    for name in ("k_c", "v_c", "ik_c"):
+        np.testing.assert_array_equal(host(fus.x[name]), host(ref.x[name]), err_msg=name)
+    idx = host(fus.idx).reshape(w.B, w.k)
+    np.testing.assert_array_equal(idx, host(ref.idx).reshape(w.B, w.k))
+    caches = oracle.compress_all(w, x)
+    o_ref, lse_ref = oracle_attention_given_idx(w, x, idx, caches)
+    o = host(fus.o)
+    if o.dtype == np.uint16:
+        o = synth.bf16_bits_to_f32(o)
+    o = o.reshape(w.B, w.H, w.d).astype(np.float64)
+    lse = host(fus.lse).reshape(w.B, w.H)
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(lse), fin)
+    err_o = float(np.abs(o - o_ref).max())
+    err_l = float(np.abs(lse[fin] - lse_ref[fin]).max()) if fin.any() else 0.0
+    assert err_o <= TOL and err_l <= TOL, (err_o, err_l)
+    return dict(o_err=err_o, lse_err=err_l, idx=idx)
+
+
+@pytest.mark.parametrize("L,B,k", [(20003, 3, 256), (8192, 8, 2048), (4100, 2, 64),
+                                   (70000, 1, 64), (60003, 5, 1000)])
+def test_fused_decode_matches_the_three_calls(L, B, k):
+    w = synth.Workload("fdec", "decode", B=B, L=L, T=1, R=128, k=k, x8=True)
+    check_fused(w, synth.make_inputs(w))
+
+
+def test_fused_decode_mixed_positions_and_closing_blocks():
+    """Each sequence at its own position: some close a block this step, some
+    do not (empty block range), some are so early that no compressed entry is
+    visible and the window is short."""
+    w = synth.Workload("fmix", "decode", B=8, L=12000, T=1, R=128, k=256, x8=True)
+    x = synth.make_inputs(w)
+    pos = np.array([11999, 11998, 3, 0, 1024 * 4 - 1, 1024 * 4, 2, 6003], dtype=np.int32)
+    x["q_pos"] = pos.reshape(w.B, 1)
+    closes = (pos + 1) % w.m == 0
+    x["blk_hi"] = ((pos + 1) // w.m).astype(np.int32)
+    x["blk_lo"] = (x["blk_hi"] - closes).astype(np.int32)
+    x["hblk_hi"] = ((pos + 1) // w.m2).astype(np.int32)
+    x["hblk_lo"] = x["hblk_hi"].copy()
+    check_fused(w, x)
+
+
+def test_fused_decode_window_only_and_fewer_heads():
+    w = synth.Workload("fwin", "decode", B=3, L=3000, T=1, R=128, H=40, k=0, W=100)
+    check_fused(w, synth.make_inputs(w))
+    w2 = synth.Workload("fh", "decode", B=4, L=9001, T=1, R=256, H=16, k=300, W=200)
+    check_fused(w2, synth.make_inputs(w2), o_dtype="bf16")
+
+
+def test_fused_decode_nan_row_rejected_like_the_three_calls():
+    """A NaN in one sequence's indexer queries makes its scores NaN: both
+    paths reject that row (idx all -1, SA_ERR_NAN) and attend its window only;
+    the other rows are unaffected."""
+    w = synth.Workload("fnan", "decode", B=3, L=20003, T=1, R=128, k=256, x8=True)
+    x = synth.make_inputs(w)
+    x["q_idx"] = x["q_idx"].copy()
+    x["q_idx"][1, 0, 5, 7] = 0x7FC0                     # bf16 NaN
+    r = check_fused(w, x, expect_err=1 << sa().SA_ERR_NAN)
+    assert np.all(r["idx"][1] == -1) and np.all(r["idx"][[0, 2]] >= 0)
+
+
+@pytest.mark.parametrize("name", ["decode128k", "decode1m"])
+def test_fused_decode_full_size(name):
+    w = synth.WORKLOADS[name]
+    check_fused(w, synth.make_inputs(w), o_dtype="bf16")
+
+
+def test_fused_decode_host_validation():
+    m = sa()
+    x = torch.empty(4096, dtype=torch.bfloat16, device="cuda")
+    i = torch.zeros(8, dtype=torch.int32, device="cuda")
+    f = torch.zeros(64, dtype=torch.float32, device="cuda")
+    args = dict(q=x, q_idx=x, w=f, q_pos=i, k_raw=x, v_raw=x, ik_raw=x, z=f, R=128, blk_lo=i,
+                blk_hi=i, max_blocks=1, k_c=x, v_c=x, ik_c=x, N_cap=16, idx=i, o=x, lse=f)
+    with pytest.raises(m.SaError) as e:        # head dim 64: not this kernel's shape
+        m.csa_decode(1, 64, 64, 64, 64, 4, 8, 16, 0.1, **args)
+    assert e.value.status == m.SA_ERR_UNSUPPORTED
+    with pytest.raises(m.SaError) as e:        # misaligned queries
+        m.csa_decode(1, 64, 128, 64, 64, 4, 8, 16, 0.1, **dict(args, q=x[1:]))
+    assert e.value.status == m.SA_ERR_INVALID_ARG
+    with pytest.raises(m.SaError) as e:        # window longer than the ring
+        m.csa_decode(1, 64, 128, 64, 64, 4, 8, 200, 0.1, **args)
+    assert e.value.status == m.SA_ERR_INVALID_ARG
