@@ -151,6 +151,20 @@ def uniform(seed: int, name: str, shape) -> np.ndarray:
     return _draw(seed, name, int(np.prod(shape)), "uniform").reshape(shape)
 
 
+def integers(seed: int, name: str, shape, lo: int, hi: int, store: str) -> np.ndarray:
+    """Uniform integers in [lo, hi] of ``shape``, stored as float32 or
+    bfloat16 bits (exact for |value| <= 256)."""
+    g = _gen(seed, name, 0)
+    x = g.integers(lo, hi + 1, size=shape).astype(np.float32)
+    return f32_to_bf16_bits(x) if store == "bf16" else x
+
+
+def dyadic(seed: int, name: str, shape, num_hi: int, den: int) -> np.ndarray:
+    """Uniform values j / den, j in [0, num_hi], of ``shape`` as float32."""
+    g = _gen(seed, name, 0)
+    return (g.integers(0, num_hi + 1, size=shape).astype(np.float32) / np.float32(den))
+
+
 def choose_rows(seed: int, name: str, n: int, count: int) -> np.ndarray:
     """``count`` distinct indices in [0, n), sorted."""
     g = _gen(seed, name, 0)
