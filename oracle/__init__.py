@@ -68,6 +68,10 @@ def lib():
             L.orc_merge.argtypes = [C.c_int, C.c_int64, C.c_int, _dp, _dp, _dp, _dp]
             L.orc_mxfp4_quantize.argtypes = [C.c_int64, _dp, _u8p, _u8p]
             L.orc_mxfp4_dequantize.argtypes = [C.c_int64, _u8p, _u8p, _dp]
+            L.orc_attend_backward.argtypes = [C.c_int64, C.c_int, C.c_int, C.c_double, _dp, _ip,
+                                              _dp, _dp, _dp, _dp, _dp, _dp]
+            L.orc_compress_backward.argtypes = [C.c_int64, C.c_int, C.c_int, _dp, _dp, _dp, _dp,
+                                                _dp]
             _lib = L
     return _lib
 
@@ -292,4 +296,113 @@ def compress_all(w, x: dict) -> dict:
             hk_c[b, lo:hi] = compress(x["hk_raw"][b], x["hz"][b], w.m2, lo, hi, store)
             hv_c[b, lo:hi] = compress(x["hv_raw"][b], x["hz"][b], w.m2, lo, hi, store)
     out.update(k_c=k_c, v_c=v_c, ik_c=ik_c, hk_c=hk_c, hv_c=hv_c)
+    return out
+
+
+# --------------------------------------------------------------- backward
+# The gradient of one pass for a loss whose gradient with respect to the
+# attention outputs is given (dO for the CSA layer, dhO for the HCA layer).
+# The top-k selection is a constant mask ("EP 95. DeepSeek-V4 논문 읽기 — 노정석",
+# IDEAS: top-k selection is not differentiable), so the indexer (its queries,
+# weights and keys) gets no gradient; the gradient flows to the queries, to
+# the attended cache rows and window rows, and through the pooling of the
+# blocks compressed in this pass to the raw rows and their pooling logits.
+# The storage rounding of the caches is taken as the identity.
+
+def attend_backward(q: np.ndarray, keys: list, values: list, dO: np.ndarray, scale: float):
+    """Gradient of ``attend`` for dL/dO = dO: (dq [rows,H,d], dK [n_total,d],
+    dV [n_total,d]) with dK, dV per entry of the concatenated key multisets."""
+    rows, H, d = q.shape
+    off = np.zeros(rows + 1, dtype=np.int64)
+    off[1:] = np.cumsum([len(k) for k in keys])
+    n = int(off[-1])
+    K = _c(np.concatenate([to_f64(k).reshape(-1, d) for k in keys]) if n else np.zeros((1, d)))
+    V = _c(np.concatenate([to_f64(v).reshape(-1, d) for v in values]) if n else np.zeros((1, d)))
+    dq = np.empty((rows, H, d))
+    dK = np.empty((max(n, 1), d))
+    dV = np.empty((max(n, 1), d))
+    lib().orc_attend_backward(rows, H, d, scale, _c(to_f64(q)), off, K, V, _c(dO), dq, dK, dV)
+    return dq, dK[:n], dV[:n], off
+
+
+def compress_backward(x_ring: np.ndarray, z_ring: np.ndarray, m: int, blk_lo: int,
+                      blk_hi: int, dXc: np.ndarray):
+    """Gradient of ``compress`` (unrounded) for blocks [blk_lo, blk_hi):
+    (dX [nb*m, d] of raw positions blk_lo*m .., dz [nb*m])."""
+    R, d = x_ring.shape
+    nb = blk_hi - blk_lo
+    pos = np.arange(blk_lo * m, blk_hi * m) % R
+    X = _c(to_f64(x_ring)[pos])
+    Z = _c(np.asarray(z_ring, dtype=np.float64)[pos])
+    dX = np.empty((nb * m, d))
+    dz = np.zeros(nb * m)
+    if nb > 0:
+        lib().orc_compress_backward(nb, m, d, X, Z, _c(dXc), dX, dz)
+    return dX, dz
+
+
+def reference_backward(w, x: dict, dO: np.ndarray, dhO: np.ndarray, fwd: dict | None = None):
+    """Gradients of one pass (all query rows) for dL/dO = dO [B,T,H,d] (CSA
+    layer) and dL/dhO = dhO (HCA layer), given the forward ``fwd`` (from
+    ``reference``; computed if None).  Returns dq, dq_hca [B,T,H,d]; dk_c,
+    dv_c [B,ncap,d] and dhk_c, dhv_c [B,ncap2,d] (cache rows as attended);
+    dk_raw, dv_raw, dhk_raw, dhv_raw [B,R,d] (window rows plus the pooling of
+    this pass's blocks); dz, dhz [B,R]."""
+    B, T, H, d = w.B, w.T, w.H, w.d
+    R = w.ring
+    if fwd is None:
+        fwd = reference(w, x)
+    out = {}
+    pos = x["q_pos"].reshape(-1).astype(np.int64)
+    rows = np.arange(B * T)
+    for layer in ("csa", "hca"):
+        hca = layer == "hca"
+        qn, kc_n, vc_n, kr_n, vr_n = (("q_hca", "hk_c", "hv_c", "hk_raw", "hv_raw") if hca else
+                                      ("q", "k_c", "v_c", "k_raw", "v_raw"))
+        kc, vc = fwd[kc_n], fwd[vc_n]
+        keys, vals, src = [], [], []
+        for r in rows:
+            b, t = int(r // T), int(pos[r])
+            win = window_positions(t, w.W) % R
+            if hca:
+                sel = np.arange((t + 1) // w.m2)
+                K, V = hca_keys(b, t, w.m2, kc, vc, x[kr_n], x[vr_n], w.W)
+            else:
+                sel = fwd["idx"][r][fwd["idx"][r] >= 0]
+                K, V = csa_keys(b, t, fwd["idx"][r], kc, vc, x[kr_n], x[vr_n], w.W)
+            keys.append(K)
+            vals.append(V)
+            src.append((b, sel, win))
+        g = (dhO if hca else dO).reshape(B * T, H, d).astype(np.float64)
+        dq, dK, dV, off = attend_backward(x[qn].reshape(B * T, H, d), keys, vals, g, w.sm_scale)
+        dkc = np.zeros(kc.shape)
+        dvc = np.zeros(vc.shape)
+        dkr = np.zeros((B, R, d))
+        dvr = np.zeros((B, R, d))
+        for r, (b, sel, win) in enumerate(src):
+            o = off[r]
+            ns = len(sel)
+            np.add.at(dkc[b], sel, dK[o:o + ns])
+            np.add.at(dvc[b], sel, dV[o:o + ns])
+            np.add.at(dkr[b], win, dK[o + ns:off[r + 1]])
+            np.add.at(dvr[b], win, dV[o + ns:off[r + 1]])
+        # the pooling of this pass's blocks: cache-row gradients to raw rows
+        m = w.m2 if hca else w.m
+        zn = "hz" if hca else "z"
+        lo_n, hi_n = ("hblk_lo", "hblk_hi") if hca else ("blk_lo", "blk_hi")
+        dz = np.zeros((B, R))
+        for b in range(B):
+            lo, hi = int(x[lo_n][b]), int(x[hi_n][b])
+            if hi <= lo:
+                continue
+            rr = np.arange(lo * m, hi * m) % R
+            for src_n, dc, dr in ((kr_n, dkc, dkr), (vr_n, dvc, dvr)):
+                dX, dzp = compress_backward(x[src_n][b], x[zn][b], m, lo, hi, dc[b, lo:hi])
+                np.add.at(dr[b], rr, dX)
+                np.add.at(dz[b], rr, dzp)
+        pre = "h" if hca else ""
+        out["dq_hca" if hca else "dq"] = dq.reshape(B, T, H, d)
+        out[f"d{pre}k_c"], out[f"d{pre}v_c"] = dkc, dvc
+        out[f"d{pre}k_raw"], out[f"d{pre}v_raw"] = dkr, dvr
+        out["dhz" if hca else "dz"] = dz
     return out

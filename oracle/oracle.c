@@ -317,3 +317,103 @@ void orc_mxfp4_dequantize(int64_t nblk, const uint8_t *codes, const uint8_t *sca
         }
     }
 }
+
+/* ------------------------------------------------------------- backward */
+
+/* Gradient of orc_attend for one loss L with dL/dO = dO, the key multiset of
+ * every row held fixed (the top-k selection is not differentiable -- "EP 95.
+ * DeepSeek-V4 논문 읽기 — 노정석", IDEAS -- so it is a constant mask here).
+ * With l_o = scale * q_h . K_o, P_o = exp(l_o - LSE_h) (LSE as in orc_attend):
+ *     dV_o += sum_h P_o * dO_h
+ *     dP_o  = dO_h . V_o,      D_h = sum_o P_o * dP_o
+ *     dl_o  = P_o * (dP_o - D_h)
+ *     dq_h  = scale * sum_o dl_o * K_o
+ *     dK_o += scale * sum_h dl_o * q_h
+ * dK, dV [off[rows], d] are per entry of the multisets (the caller adds the
+ * entries that name the same cache or ring row); dq [rows, H, d].  A row with
+ * no keys gets dq = 0. */
+void orc_attend_backward(int64_t rows, int H, int d, double scale, const double *q,
+                         const int64_t *off, const double *K, const double *V,
+                         const double *dO, double *dq, double *dK, double *dV)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t o0 = off[r], o1 = off[r + 1], n = o1 - o0;
+        for (int64_t o = o0; o < o1; ++o)
+            for (int c = 0; c < d; ++c) { dK[o * d + c] = 0.0; dV[o * d + c] = 0.0; }
+        double *p = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+        double *dp = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+        for (int h = 0; h < H; ++h) {
+            const double *qh = q + (r * H + h) * (int64_t)d;
+            const double *gh = dO + (r * H + h) * (int64_t)d;
+            double *dqh = dq + (r * H + h) * (int64_t)d;
+            for (int c = 0; c < d; ++c) dqh[c] = 0.0;
+            if (n <= 0) continue;
+            double mu = -INFINITY;
+            for (int64_t o = o0; o < o1; ++o) {
+                double dot = 0.0;
+                for (int c = 0; c < d; ++c) dot += qh[c] * K[o * d + c];
+                p[o - o0] = scale * dot;
+                if (p[o - o0] > mu) mu = p[o - o0];
+            }
+            double sum = 0.0;
+            for (int64_t i = 0; i < n; ++i) sum += exp(p[i] - mu);
+            double L = mu + log(sum);
+            double D = 0.0;
+            for (int64_t o = o0; o < o1; ++o) {
+                double pr = exp(p[o - o0] - L);
+                p[o - o0] = pr;
+                double g = 0.0;
+                for (int c = 0; c < d; ++c) g += gh[c] * V[o * d + c];
+                dp[o - o0] = g;
+                D += pr * g;
+            }
+            for (int64_t o = o0; o < o1; ++o) {
+                double pr = p[o - o0];
+                double dl = pr * (dp[o - o0] - D);
+                for (int c = 0; c < d; ++c) {
+                    dV[o * d + c] += pr * gh[c];
+                    dqh[c] += scale * dl * K[o * d + c];
+                    dK[o * d + c] += scale * dl * qh[c];
+                }
+            }
+        }
+        free(p);
+        free(dp);
+    }
+}
+
+/* Gradient of orc_compress for dL/dXc = dXc, the storage rounding taken as
+ * the identity.  With a = softmax(z_block) and the unrounded pooled row
+ * Xc = sum_i a_i X_i:
+ *     dX_i  = a_i * dXc                        (written)
+ *     dz_i += a_i * (X_i - Xc) . dXc           (added: arrays pooled with the
+ *                                               same logits add their parts)
+ * Layouts as orc_compress: X, dX [nblk*m, d], z, dz [nblk*m], dXc [nblk, d]. */
+void orc_compress_backward(int64_t nblk, int m, int d, const double *X, const double *z,
+                           const double *dXc, double *dX, double *dz)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < nblk; ++b) {
+        const double *zb = z + b * m;
+        double mu = zb[0];
+        for (int i = 1; i < m; ++i) if (zb[i] > mu) mu = zb[i];
+        double den = 0.0;
+        for (int i = 0; i < m; ++i) den += exp(zb[i] - mu);
+        const double *g = dXc + b * (int64_t)d;
+        for (int i = 0; i < m; ++i) {
+            double a = exp(zb[i] - mu) / den;
+            const double *xi = X + (b * m + i) * (int64_t)d;
+            double *dxi = dX + (b * m + i) * (int64_t)d;
+            double t = 0.0;
+            for (int c = 0; c < d; ++c) {
+                double xc = 0.0;
+                for (int l = 0; l < m; ++l)
+                    xc += (exp(zb[l] - mu) / den) * X[(b * m + l) * (int64_t)d + c];
+                dxi[c] = a * g[c];
+                t += (xi[c] - xc) * g[c];
+            }
+            dz[b * m + i] += a * t;
+        }
+    }
+}
