@@ -347,6 +347,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       float m0 = -INFINITY, m1 = -INFINITY;        // running max (log2 units), per head
       float l0 = 0.f, l1 = 0.f;                    // this lane's share of the running sums
       for (int t = 0; t < I.nt && ok; ++t, ++n) {
+        // (before the wait for S: the index loads overlap it) key i of the tile
+        // is real iff it is a selected row naming a visible entry (a -1 or
+        // out-of-range index is ignored: its zero-filled tile row must not
+        // enter the softmax) or a window row.  Lane l tests keys 2l and 2l+1;
+        // two ballots give the tile's even and odd keys, and this lane keeps
+        // the bits of its keys 8g + 2(l%4) + j as bit 2g + j of keep16.
+        const int64_t s0 = (I.t_begin + t) * kKeys;
+        auto is_real = [&](int64_t sk) -> bool {
+          if (sk < I.n_comp) {
+            if (!a.gather) return true;
+            const int64_t jj = __ldg(a.idx + I.row * a.k + sk);
+            return jj >= 0 && jj < I.nvis;
+          }
+          return sk >= I.n_comp_pad && sk < I.n_comp_pad + I.n_win;
+        };
+        const uint32_t re = __ballot_sync(0xffffffffu, is_real(s0 + 2 * lane));
+        const uint32_t ro = __ballot_sync(0xffffffffu, is_real(s0 + 2 * lane + 1));
+        uint32_t keep16 = 0;
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          keep16 |= (((re >> (4 * g + l4)) & 1u) << (2 * g)) |
+                    (((ro >> (4 * g + l4)) & 1u) << (2 * g + 1));
         const int sb = (int)(n & 1), pb = (int)(n & 1);
         ok = __all_sync(0xffffffffu, mbar_wait(&C.s_full[sb], (uint32_t)((n >> 1) & 1), a.err));
         if (!ok) break;
@@ -361,21 +383,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         tc_fence_before();
         mbar_arrive(&C.s_empty[sb]);
-        // key i of the tile is real iff it is in the compressed part or the
-        // window: bits [0, c_hi) and [w_lo, w_hi) of a 64-bit mask
-        const int64_t s0 = (I.t_begin + t) * kKeys;
-        const int c_hi = (int)max64(0, min64(64, I.n_comp - s0));
-        const int w_lo = (int)max64(0, min64(64, I.n_comp_pad - s0));
-        const int w_hi = (int)max64(0, min64(64, I.n_comp_pad + I.n_win - s0));
-        auto ones = [](int k) -> uint64_t { return k >= 64 ? ~0ull : ((1ull << k) - 1ull); };
-        const uint64_t real = ones(c_hi) | (ones(w_hi) & ~ones(w_lo));
-        if (real != ~0ull || !ok0 || !ok1) {
-          const uint64_t rl = real >> (2 * l4);
+        if (keep16 != 0xFFFFu || !ok0 || !ok1) {
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-              const bool keep = (rl >> (8 * g + j)) & 1ull;
+              const bool keep = (keep16 >> (2 * g + j)) & 1u;
               if (!keep || !ok0) v[4 * g + j] = -INFINITY;
               if (!keep || !ok1) v[4 * g + 2 + j] = -INFINITY;
             }

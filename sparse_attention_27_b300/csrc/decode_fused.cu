@@ -16,7 +16,8 @@
 // CTA per SM, 512 threads.  CTA r of the cluster owns a contiguous slice of
 // the sequence's visible compressed entries (whole 128-entry tiles).  Phases:
 //  1. scores: warp 0 streams the slice's indexer-key tiles by TMA through a
-//     ring of 16 KB stages; warp 1 issues tcgen05 MMAs D[j, h] =
+//     ring of 32 KB stages (two 128-entry tiles per copy: the copy engine's
+//     cost is per request, so larger requests stream faster per SM); warp 1 issues tcgen05 MMAs D[j, h] =
 //     Ik_c[j] . q_I[h] (M = 128 entries, N = 64 heads, K = 64) into four TMEM
 //     accumulators; warps 4-11 (two warpgroups, alternate tiles) fold ReLU
 //     and the head weights in fp32 and write each score as an
@@ -58,7 +59,9 @@ constexpr int kHI = 64, kDI = 64;              // indexer heads, indexer key wid
 constexpr int kD = 128;                        // head dim
 constexpr int kHeads = 64;                     // attention MMA M
 constexpr int kKeys = 64;                      // keys per attention tile
-constexpr int kABytes = kTile * kDI * 2;       // 16 KB: one score stage
+constexpr int kStageTiles = 2;                 // score tiles per stage (one TMA box of 256 rows)
+constexpr int kTileBytes = kTile * kDI * 2;    // 16 KB: one score tile
+constexpr int kABytes = kStageTiles * kTileBytes;   // 32 KB: one score stage
 constexpr int kBBytes = kHI * kDI * 2;         // 8 KB: the row's indexer queries
 constexpr int kQBytes = kHeads * kD * 2;       // 16 KB: the row's query heads
 constexpr int kHalf = kKeys * 128;             // 8 KB: 64 dims of a K or V tile
@@ -66,7 +69,7 @@ constexpr int kKVBytes = 4 * kHalf;            // 32 KB: one K/V stage
 constexpr int kPBytes = kHeads * kKeys * 2;    // 8 KB
 constexpr int kAcc = 4;                        // score accumulators (64 TMEM columns each)
 constexpr int kTmemCols = 256;                 // score: 4 x 64; attention: S 2 x 64 + O 128
-constexpr int kMaxStagesA = 12, kMaxStagesKV = 6;
+constexpr int kMaxStagesA = 6, kMaxStagesKV = 6;
 constexpr int kMaxPool = 128;                  // largest block size m this kernel pools
 constexpr float kRescaleThreshold = 32.f;      // log2 units
 
@@ -92,7 +95,7 @@ struct Ctl {
 };
 
 struct TMaps {
-  CUtensorMap ik;                              // [B*N_cap, 64] bf16, box 64 x 128
+  CUtensorMap ik;                              // [B*N_cap, 64] bf16, box 64 x 256
   CUtensorMap qi;                              // [B*64, 64] bf16, box 64 x 64
   CUtensorMap q;                               // [B*H, 128] bf16, box 64 x 64
 };
@@ -261,8 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int issued = 0;
       bool waited_fresh = false;
-      for (int t = t_lo; t < t_hi && !*abort_flag; ++t, ++issued) {
-        if (t >= t_fresh && !waited_fresh) {     // the pooled rows must be in memory first
+      for (int t = t_lo; t < t_hi && !*abort_flag; t += kStageTiles, ++issued) {
+        if (t + kStageTiles - 1 >= t_fresh && !waited_fresh) {   // pooled rows in memory first
           if (!mbar_wait(&C.fresh, 0, a.err)) { *abort_flag = 1; break; }
           waited_fresh = true;
         }
@@ -284,20 +287,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(&C.b_full, 0, a.err);
       const uint32_t b_base = smem_u32(sB);
       for (int o = 0; o < nt_score && ok && !*abort_flag; ++o) {
-        const int st = o % a.stages_a, acc = o % kAcc;
-        if (!mbar_wait(&C.a_full[st], (uint32_t)((o / a.stages_a) & 1), a.err) ||
+        const int u = o / kStageTiles, half = o % kStageTiles;   // stage, tile within it
+        const int st = u % a.stages_a, acc = o % kAcc;
+        if ((half == 0 && !mbar_wait(&C.a_full[st], (uint32_t)((u / a.stages_a) & 1), a.err)) ||
             !mbar_wait(&C.t_empty[acc], (uint32_t)(((o / kAcc) & 1) ^ 1), a.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t a_base = smem_u32(sA + st * kABytes);
+        const uint32_t a_base = smem_u32(sA + st * kABytes + half * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kDI / 16; ++kk)
           tc_mma_f16(tmem + acc * kHI, sdesc_kmajor_sw128(a_base + kk * 32),
                      sdesc_kmajor_sw128(b_base + kk * 32), idesc, kk > 0 ? 1u : 0u);
-        tc_commit(&C.a_empty[st]);
         tc_commit(&C.t_full[acc]);
+        if (half == kStageTiles - 1 || o == nt_score - 1) tc_commit(&C.a_empty[st]);
       }
       if (!ok) *abort_flag = 1;
     }
@@ -533,6 +537,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     bool ok = true;
     for (int n = 0; n < nt_att && ok; ++n) {
+      // (before the wait for S) key i of the tile is real iff it is a selected
+      // row naming a visible entry (a -1 from a rejected row is ignored) or a
+      // window row.  Lane l tests keys 2l and 2l+1; two ballots give the
+      // tile's even and odd keys, and this lane keeps the bits of its keys
+      // 8g + 2(l%4) + j as bit 2g + j of keep16.
+      const int s0 = (at_lo + n) * kKeys;
+      const bool ok0 = h0 < a.H, ok1 = h1 < a.H;
+      auto is_real = [&](int sk) -> bool {
+        if (sk < P.n_comp) {
+          const int jj = sel[sk - sel_lo];
+          return jj >= 0 && jj < P.n;
+        }
+        return sk >= P.n_comp_pad && sk < P.n_comp_pad + P.n_win;
+      };
+      const uint32_t re = __ballot_sync(0xffffffffu, is_real(s0 + 2 * lane));
+      const uint32_t ro = __ballot_sync(0xffffffffu, is_real(s0 + 2 * lane + 1));
+      uint32_t keep16 = 0;
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        keep16 |= (((re >> (4 * g + l4)) & 1u) << (2 * g)) |
+                  (((ro >> (4 * g + l4)) & 1u) << (2 * g + 1));
       const int sb = n & 1, pb = n & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(&C.s_full[sb], (uint32_t)((n >> 1) & 1), a.err));
       if (!ok) break;
@@ -547,21 +572,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&C.s_empty[sb]);
-      // key i of the tile is real iff it is a selected row or a window row
-      const int s0 = (at_lo + n) * kKeys;
-      const int c_hi = max(0, min(64, P.n_comp - s0));
-      const int w_lo = max(0, min(64, P.n_comp_pad - s0));
-      const int w_hi = max(0, min(64, P.n_comp_pad + P.n_win - s0));
-      auto ones = [](int q) -> uint64_t { return q >= 64 ? ~0ull : ((1ull << q) - 1ull); };
-      const uint64_t real = ones(c_hi) | (ones(w_hi) & ~ones(w_lo));
-      const bool ok0 = h0 < a.H, ok1 = h1 < a.H;
-      if (real != ~0ull || !ok0 || !ok1) {
-        const uint64_t rl = real >> (2 * l4);
+      if (keep16 != 0xFFFFu || !ok0 || !ok1) {
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            const bool keep = (rl >> (8 * g + j)) & 1ull;
+            const bool keep = (keep16 >> (2 * g + j)) & 1u;
             if (!keep || !ok0) v[4 * g + j] = -INFINITY;
             if (!keep || !ok1) v[4 * g + 2 + j] = -INFINITY;
           }
@@ -827,7 +843,8 @@ cudaError_t launch_fused_decode(const FusedDecodeArgs& a, cudaStream_t st) {
   // used: it then describes the query rows instead, so that it still encodes
   const bool no_keys = (uint64_t)a.B * a.N_cap == 0;
   if (!tmap_bf16(&tm.ik, no_keys ? a.q_idx : a.ik_c,
-                 no_keys ? (uint64_t)a.B * kHI : (uint64_t)a.B * a.N_cap, kDI, kTile) ||
+                 no_keys ? (uint64_t)a.B * kHI : (uint64_t)a.B * a.N_cap, kDI,
+                 kStageTiles * kTile) ||
       !tmap_bf16(&tm.qi, a.q_idx, (uint64_t)a.B * kHI, kDI, kHI) ||
       !tmap_bf16(&tm.q, a.q, (uint64_t)a.B * a.H, kD, kHeads))
     return cudaErrorInvalidValue;

@@ -433,3 +433,34 @@ def test_bf16_output_is_the_rounded_f32_output(L, B, k, m2):
     if same:
         assert np.abs(o[same] - ref["o"][same]).max() <= TOL_ATT["bf16"]
     assert np.abs(ho - ref["ho"]).max() <= TOL_ATT["bf16"]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_attend_ignores_minus_one_inside_the_selection(dtype):
+    """A -1 inside the first min(k, n) slots of idx (a rejected row is all
+    -1) names no key: csa_attend must leave it out of the softmax, as the
+    oracle's key multiset does, on the tensor-core (bf16) and CUDA-core
+    (f32) kernels alike.  Holes in every other row, a whole row of -1 in
+    one."""
+    w = synth.Workload("holes", "decode", B=4, L=20003, T=1, R=128, k=256, x8=True, dtype=dtype,
+                       indexer=dtype)
+    x = synth.make_inputs(w)
+    ref = oracle.reference(w, x)
+    idx = ref["idx"].copy()
+    idx[0, ::3] = -1
+    idx[2, 100:180] = -1
+    idx[3, :] = -1
+    step = make_step(w, x)
+    step.compress_csa()
+    step.attend_csa(idx=dev(idx.reshape(w.B, 1, w.k)))
+    torch.cuda.synchronize()
+    assert step.device_errors() == 0
+    caches = oracle.compress_all(w, x)
+    keys, vals = zip(*[oracle.csa_keys(b, w.L - 1, idx[b], caches["k_c"], caches["v_c"],
+                                       x["k_raw"], x["v_raw"], w.W) for b in range(w.B)])
+    o_ref, lse_ref = oracle.attend(x["q"].reshape(w.B, w.H, w.d), list(keys), list(vals),
+                                   w.sm_scale)
+    o = host(step.o).reshape(w.B, w.H, w.d)
+    lse = host(step.lse).reshape(w.B, w.H)
+    tol = TOL_ATT[dtype]
+    assert np.abs(o - o_ref).max() <= tol and np.abs(lse - lse_ref).max() <= tol
