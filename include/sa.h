@@ -249,6 +249,57 @@ int csa_decode(int B, int H, int d, int HI, int dI, int m, int k, int W, float s
                float* lse, int32_t* err, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Backward pass.  The top-k selection is not differentiable ([P1] IDEAS), so
+ * it is a constant mask: the gradient of a loss with dL/dO given reaches the
+ * queries, the attended cache rows and window rows, and -- through the
+ * pooling of the blocks a pass compressed -- the raw rows and their pooling
+ * logits.  The indexer (q_idx, w, the indexer keys) gets no gradient.  The
+ * caches' storage rounding is taken as the identity.  Every gradient output
+ * is fp32 and is ADDED to (the caller zeroes it first, or accumulates over
+ * layers and steps); several queries that attend the same row add their
+ * parts with atomics, so the summation order is not fixed.
+ *
+ * csa_attend_backward -- gradient of csa_attend for the given idx:
+ *   with P = exp(sm_scale q.k - lse) over the row's key list,
+ *   dV += sum_h P dO_h; dS = P (dO_h.V - dO_h.O_h); dq += sm_scale sum dS K;
+ *   dK += sm_scale sum_h dS q_h  (selected rows -> dk_c/dv_c, window rows ->
+ *   dk_raw/dv_raw at ring row u mod R).
+ *  arguments as csa_attend, plus o [B,T,H,d] f32 and lse [B,T,H] f32 (the
+ *  forward's outputs, o_dtype SA_F32) and dout [B,T,H,d] f32;
+ *  dq [B,T,H,d], dk_c, dv_c [B,N_cap,d], dk_raw, dv_raw [B,R,d]: f32, added to.
+ *  CUDA cores, fp32 (H*d*12 + 33*(d+1)*8 bytes of shared memory <= 227 KB).
+ */
+int csa_attend_backward(int dtype, int B, int T, int H, int d, int m, int k, int W,
+                        float sm_scale, const void* q, const int32_t* q_pos, const void* k_c,
+                        const void* v_c, int N_cap, const int32_t* idx, const void* k_raw,
+                        const void* v_raw, int R, const float* o, const float* lse,
+                        const float* dout, float* dq, float* dk_c, float* dv_c, float* dk_raw,
+                        float* dv_raw, int32_t* err, void* stream);
+
+/* hca_attend_backward -- gradient of the attention of hca_compress_attend
+ * (every visible HCA row plus the window): as csa_attend_backward with the
+ * dense key list; dhk_c, dhv_c [B,N2_cap,d]. */
+int hca_attend_backward(int dtype, int B, int T, int H, int d, int m2, int W, float sm_scale,
+                        const void* q, const int32_t* q_pos, const void* hk_c, const void* hv_c,
+                        int N2_cap, const void* k_raw, const void* v_raw, int R, const float* o,
+                        const float* lse, const float* dout, float* dq, float* dhk_c,
+                        float* dhv_c, float* dk_raw, float* dv_raw, int32_t* err, void* stream);
+
+/* sa_compress_backward -- gradient of the K/V pooling of csa_compress (or of
+ * hca_compress_attend's, with m = m') for the blocks [blk_lo[b], blk_hi[b]):
+ * with a = softmax(z over the block) and the unrounded pooled row
+ * Xc = sum_i a_i X_i, for X in {K, V}:
+ *     dX_raw[p_i mod R] += a_i dXc;   dz[p_i mod R] += a_i (X_i - Xc) . dXc
+ *  k_raw, v_raw [B,R,d] in dtype; z [B,R] f32; dk_c, dv_c [B,N_cap,d] f32
+ *  (the cache-row gradients, e.g. from csa_attend_backward); dk_raw, dv_raw
+ *  [B,R,d] and dz [B,R] f32, added to.  m <= 6144.
+ */
+int sa_compress_backward(int dtype, int B, int d, int m, const void* k_raw, const void* v_raw,
+                         const float* z, int R, const int32_t* blk_lo, const int32_t* blk_hi,
+                         int max_blocks, const float* dk_c, const float* dv_c, int N_cap,
+                         float* dk_raw, float* dv_raw, float* dz, int32_t* err, void* stream);
+
+/* ---------------------------------------------------------------------------
  * sa_mxfp4_quantize -- MXFP4 storage of bf16 rows for the low-precision
  * indexer path ([P2q]: the indexer QK path is stored in FP4 (MXFP4)).
  * Block rule of the OCP Microscaling Formats (MX) v1.0 specification: for

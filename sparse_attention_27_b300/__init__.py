@@ -27,7 +27,8 @@ EXPORTS = (
     "sa_status_string", "csa_compress", "csa_index_topk", "csa_index_topk_workspace_bytes",
     "csa_attend", "csa_attend_workspace_bytes", "hca_compress_attend",
     "hca_compress_attend_workspace_bytes", "attn_merge", "csa_index_topk_noalloc",
-    "sa_mxfp4_quantize", "csa_decode",
+    "sa_mxfp4_quantize", "csa_decode", "csa_attend_backward", "hca_attend_backward",
+    "sa_compress_backward",
 )
 
 
@@ -54,6 +55,13 @@ _lib.csa_index_topk_workspace_bytes.restype = _sz
 _lib.csa_index_topk_noalloc.argtypes = [_i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i,
                                         _vp, _vp, _vp, _vp]
 _lib.sa_mxfp4_quantize.argtypes = [_vp, _i64, _vp, _vp, _vp]
+_lib.csa_attend_backward.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _i,
+                                     _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                     _vp, _vp]
+_lib.hca_attend_backward.argtypes = [_i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _i, _vp,
+                                     _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+_lib.sa_compress_backward.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp,
+                                      _i, _vp, _vp, _vp, _vp, _vp]
 _lib.csa_decode.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                             _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp,
                             _vp]
@@ -177,6 +185,38 @@ def csa_decode(B, H, d, HI, dI, m, k, W, sm_scale, q, q_idx, w, q_pos, k_raw, v_
                            _p(q_pos), _p(k_raw), _p(v_raw), _p(ik_raw), _p(z), R, _p(blk_lo),
                            _p(blk_hi), max_blocks, _p(k_c), _p(v_c), _p(ik_c), N_cap, _p(idx),
                            _p(o), _out_code(o), _p(lse), _p(err), _stream(stream)), "csa_decode")
+
+
+def csa_attend_backward(dtype, B, T, H, d, m, k, W, sm_scale, q, q_pos, k_c, v_c, N_cap, idx,
+                        k_raw, v_raw, R, o, lse, dout, dq, dk_c, dv_c, dk_raw, dv_raw, err=None,
+                        stream=None):
+    """Gradient of csa_attend for the given selection; adds into the f32
+    gradient tensors dq, dk_c, dv_c, dk_raw, dv_raw."""
+    _check(_lib.csa_attend_backward(dtype, B, T, H, d, m, k, W, sm_scale, _p(q), _p(q_pos),
+                                    _p(k_c), _p(v_c), N_cap, _p(idx), _p(k_raw), _p(v_raw), R,
+                                    _p(o), _p(lse), _p(dout), _p(dq), _p(dk_c), _p(dv_c),
+                                    _p(dk_raw), _p(dv_raw), _p(err), _stream(stream)),
+           "csa_attend_backward")
+
+
+def hca_attend_backward(dtype, B, T, H, d, m2, W, sm_scale, q, q_pos, hk_c, hv_c, N2_cap, k_raw,
+                        v_raw, R, o, lse, dout, dq, dhk_c, dhv_c, dk_raw, dv_raw, err=None,
+                        stream=None):
+    """Gradient of the HCA attention (all visible HCA rows and the window)."""
+    _check(_lib.hca_attend_backward(dtype, B, T, H, d, m2, W, sm_scale, _p(q), _p(q_pos),
+                                    _p(hk_c), _p(hv_c), N2_cap, _p(k_raw), _p(v_raw), R, _p(o),
+                                    _p(lse), _p(dout), _p(dq), _p(dhk_c), _p(dhv_c), _p(dk_raw),
+                                    _p(dv_raw), _p(err), _stream(stream)), "hca_attend_backward")
+
+
+def sa_compress_backward(dtype, B, d, m, k_raw, v_raw, z, R, blk_lo, blk_hi, max_blocks, dk_c,
+                         dv_c, N_cap, dk_raw, dv_raw, dz, err=None, stream=None):
+    """Gradient of the K/V pooling of blocks [blk_lo, blk_hi); adds into
+    dk_raw, dv_raw and dz."""
+    _check(_lib.sa_compress_backward(dtype, B, d, m, _p(k_raw), _p(v_raw), _p(z), R, _p(blk_lo),
+                                     _p(blk_hi), max_blocks, _p(dk_c), _p(dv_c), N_cap,
+                                     _p(dk_raw), _p(dv_raw), _p(dz), _p(err), _stream(stream)),
+           "sa_compress_backward")
 
 
 def sa_mxfp4_quantize(x, codes, scales, stream=None):

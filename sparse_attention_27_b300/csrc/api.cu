@@ -1,6 +1,7 @@
 // extern "C" entry points of libsa27 (declared and documented in include/sa.h):
 // host-side argument validation, kernel choice by dtype and shape, workspace
 // carving and launches.  Nothing here allocates, frees or synchronises.
+#include <algorithm>
 #include <mutex>
 
 #include "kernels.cuh"
@@ -289,6 +290,75 @@ int csa_decode(int B, int H, int d, int HI, int dI, int m, int k, int W, float s
   a.idx = idx; a.o = o; a.o_dtype = o_dtype; a.lse = lse; a.err = err;
   if (!fused_decode_plan(a, device_sms())) return SA_ERR_UNSUPPORTED;
   return status_of(launch_fused_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+// Shared checks and launch of the two attention backward calls.
+int attention_backward(AttnBwdArgs& a, int64_t n_keys_max, cudaStream_t st) {
+  if (!plain_dtype(a.dtype) || a.B < 0 || a.T < 0 || a.H <= 0 || a.d <= 0 || a.d > 256 ||
+      a.d % 4 || a.m < 1 || a.k < 0 || a.W < 0 || a.N_cap < 0 || a.R < 1 || a.R < a.W)
+    return SA_ERR_INVALID_ARG;
+  if (!a.q || !a.q_pos || !a.kr || !a.vr || !a.o || !a.lse || !a.dout || !a.dq || !a.dkr ||
+      !a.dvr || ((a.gather ? a.k > 0 : a.N_cap > 0) && (!a.kc || !a.vc || !a.dkc || !a.dvc)) ||
+      (a.gather && a.k > 0 && !a.idx))
+    return SA_ERR_INVALID_ARG;
+  if (attend_backward_smem(a.H, a.d) > 227 * 1024) return SA_ERR_UNSUPPORTED;
+  const int64_t rows = (int64_t)a.B * a.T;
+  if (rows == 0) return SA_OK;
+  const int tile = attend_backward_key_tile();
+  const int tiles = (int)std::max<int64_t>(1, (n_keys_max + tile - 1) / tile);
+  const int64_t want = std::max<int64_t>(1, (2 * (int64_t)device_sms() + rows - 1) / rows);
+  const int ns = (int)std::min<int64_t>(want, tiles);
+  a.split_tiles = (tiles + ns - 1) / ns;
+  a.nsplit = (tiles + a.split_tiles - 1) / a.split_tiles;
+  return status_of(launch_attend_backward(a, st));
+}
+}  // namespace
+
+int csa_attend_backward(int dtype, int B, int T, int H, int d, int m, int k, int W,
+                        float sm_scale, const void* q, const int32_t* q_pos, const void* k_c,
+                        const void* v_c, int N_cap, const int32_t* idx, const void* k_raw,
+                        const void* v_raw, int R, const float* o, const float* lse,
+                        const float* dout, float* dq, float* dk_c, float* dv_c, float* dk_raw,
+                        float* dv_raw, int32_t* err, void* stream) {
+  AttnBwdArgs a{};
+  a.dtype = dtype; a.B = B; a.T = T; a.H = H; a.d = d; a.sm_scale = sm_scale;
+  a.q = q; a.q_pos = q_pos; a.kc = k_c; a.vc = v_c; a.N_cap = N_cap; a.idx = idx;
+  a.gather = 1; a.k = k; a.m = m; a.kr = k_raw; a.vr = v_raw; a.R = R; a.W = W;
+  a.o = o; a.lse = lse; a.dout = dout; a.dq = dq; a.dkc = dk_c; a.dvc = dv_c;
+  a.dkr = dk_raw; a.dvr = dv_raw; a.err = err;
+  return attention_backward(a, (int64_t)std::min(k, N_cap) + W, static_cast<cudaStream_t>(stream));
+}
+
+int hca_attend_backward(int dtype, int B, int T, int H, int d, int m2, int W, float sm_scale,
+                        const void* q, const int32_t* q_pos, const void* hk_c, const void* hv_c,
+                        int N2_cap, const void* k_raw, const void* v_raw, int R, const float* o,
+                        const float* lse, const float* dout, float* dq, float* dhk_c,
+                        float* dhv_c, float* dk_raw, float* dv_raw, int32_t* err,
+                        void* stream) {
+  AttnBwdArgs a{};
+  a.dtype = dtype; a.B = B; a.T = T; a.H = H; a.d = d; a.sm_scale = sm_scale;
+  a.q = q; a.q_pos = q_pos; a.kc = hk_c; a.vc = hv_c; a.N_cap = N2_cap; a.idx = nullptr;
+  a.gather = 0; a.k = 0; a.m = m2; a.kr = k_raw; a.vr = v_raw; a.R = R; a.W = W;
+  a.o = o; a.lse = lse; a.dout = dout; a.dq = dq; a.dkc = dhk_c; a.dvc = dhv_c;
+  a.dkr = dk_raw; a.dvr = dv_raw; a.err = err;
+  return attention_backward(a, (int64_t)N2_cap + W, static_cast<cudaStream_t>(stream));
+}
+
+int sa_compress_backward(int dtype, int B, int d, int m, const void* k_raw, const void* v_raw,
+                         const float* z, int R, const int32_t* blk_lo, const int32_t* blk_hi,
+                         int max_blocks, const float* dk_c, const float* dv_c, int N_cap,
+                         float* dk_raw, float* dv_raw, float* dz, int32_t* err, void* stream) {
+  if (!plain_dtype(dtype) || B < 0 || d <= 0 || m < 1 || R < m || max_blocks < 0 || N_cap < 0)
+    return SA_ERR_INVALID_ARG;
+  if (B == 0 || max_blocks == 0) return SA_OK;
+  if (!k_raw || !v_raw || !z || !blk_lo || !blk_hi || !dk_c || !dv_c || !dk_raw || !dv_raw ||
+      !dz)
+    return SA_ERR_INVALID_ARG;
+  if (2 * (size_t)m * sizeof(float) > 48 * 1024) return SA_ERR_UNSUPPORTED;
+  CompressBwdArgs a{dtype, B, d, m, k_raw, v_raw, z, R, blk_lo, blk_hi, max_blocks, dk_c, dv_c,
+                    N_cap, dk_raw, dv_raw, dz, err};
+  return status_of(launch_compress_backward(a, static_cast<cudaStream_t>(stream)));
 }
 
 int sa_mxfp4_quantize(const void* x, int64_t nblk, void* codes, void* scales, void* stream) {

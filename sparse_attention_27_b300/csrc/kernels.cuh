@@ -129,6 +129,56 @@ struct FusedDecodeArgs {
 bool fused_decode_plan(FusedDecodeArgs& a, int num_sms);
 cudaError_t launch_fused_decode(const FusedDecodeArgs& a, cudaStream_t st);
 
+// Backward of the attention branches (the key list as in AttnArgs, fixed)
+// and of the block pooling; every gradient is added (fp32 atomics) into the
+// caller's buffers.
+struct AttnBwdArgs {
+  int dtype, B, T, H, d;
+  float sm_scale;
+  const void* q;        // [B*T, H, d]
+  const int32_t* q_pos;
+  const void* kc;       // [B, N_cap, d]
+  const void* vc;
+  int N_cap;
+  const int32_t* idx;   // [B*T, k] when gather
+  int gather, k, m;
+  const void* kr;       // [B, R, d]
+  const void* vr;
+  int R, W;
+  const float* o;       // [B*T, H, d] forward output
+  const float* lse;     // [B*T, H] forward LSE
+  const float* dout;    // [B*T, H, d]
+  float* dq;            // [B*T, H, d]
+  float* dkc;           // [B, N_cap, d]
+  float* dvc;
+  float* dkr;           // [B, R, d]
+  float* dvr;
+  int nsplit, split_tiles;   // key tiles of attend_backward_key_tile() keys
+  int32_t* err;
+};
+cudaError_t launch_attend_backward(const AttnBwdArgs& a, cudaStream_t st);
+size_t attend_backward_smem(int H, int d);
+int attend_backward_key_tile();
+
+struct CompressBwdArgs {
+  int dtype, B, d, m;
+  const void* k_raw;    // [B, R, d]
+  const void* v_raw;
+  const float* z;       // [B, R]
+  int R;
+  const int32_t* blk_lo;
+  const int32_t* blk_hi;
+  int max_blocks;
+  const float* dkc;     // [B, N_cap, d]
+  const float* dvc;
+  int N_cap;
+  float* dkr;           // [B, R, d]
+  float* dvr;
+  float* dz;            // [B, R]
+  int32_t* err;
+};
+cudaError_t launch_compress_backward(const CompressBwdArgs& a, cudaStream_t st);
+
 struct MergeArgs {
   int n;
   const float* o_parts[8];

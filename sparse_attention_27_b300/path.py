@@ -33,9 +33,10 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from . import (SA_BF16, SA_F32, SA_MXFP4, csa_attend, csa_attend_workspace_bytes, csa_compress,
-               csa_decode, csa_index_topk, csa_index_topk_workspace_bytes, hca_compress_attend,
-               hca_compress_attend_workspace_bytes, sa_mxfp4_quantize)
+from . import (SA_BF16, SA_F32, SA_MXFP4, csa_attend, csa_attend_backward,
+               csa_attend_workspace_bytes, csa_compress, csa_decode, csa_index_topk,
+               csa_index_topk_workspace_bytes, hca_attend_backward, hca_compress_attend,
+               hca_compress_attend_workspace_bytes, sa_compress_backward, sa_mxfp4_quantize)
 
 _CODES = {"f32": SA_F32, "bf16": SA_BF16, "mxfp4": SA_MXFP4}
 
@@ -206,6 +207,45 @@ class HybridStep:
         e2.record(s_hca)
         cur.wait_event(e1)
         cur.wait_event(e2)
+
+    def backward(self, dout, dhout, idx=None, o=None, lse=None, ho=None, hlse=None,
+                 stream=None) -> dict:
+        """Gradients of this pass for dL/dO = dout and dL/dhO = dhout (f32
+        [B,T,H,d]), the selection (idx, default this pass's) held fixed.  The
+        forward's O and LSE default to this pass's outputs (o_dtype "f32").
+        Returns fresh f32 tensors: dq, dq_hca; dk_c, dv_c, dhk_c, dhv_c (cache
+        rows as attended); dk_raw, dv_raw, dhk_raw, dhv_raw (window rows and
+        the pooling of this pass's blocks); dz, dhz."""
+        D, x = self.D, self.x
+        dt = _CODES[D.dtype]
+        dev = self.o.device
+        f = lambda shape: torch.zeros(shape, dtype=torch.float32, device=dev)
+        g = {"dq": f((D.B, D.T, D.H, D.d)), "dq_hca": f((D.B, D.T, D.H, D.d)),
+             "dk_c": f((D.B, D.ncap, D.d)), "dv_c": f((D.B, D.ncap, D.d)),
+             "dhk_c": f((D.B, D.ncap2, D.d)), "dhv_c": f((D.B, D.ncap2, D.d)),
+             "dk_raw": f((D.B, D.R, D.d)), "dv_raw": f((D.B, D.R, D.d)),
+             "dhk_raw": f((D.B, D.R, D.d)), "dhv_raw": f((D.B, D.R, D.d)),
+             "dz": f((D.B, D.R)), "dhz": f((D.B, D.R))}
+        o = self.o if o is None else o
+        lse = self.lse if lse is None else lse
+        ho = self.ho if ho is None else ho
+        hlse = self.hlse if hlse is None else hlse
+        csa_attend_backward(dt, D.B, D.T, D.H, D.d, D.m, D.k, D.W, D.sm_scale, x["q"], x["q_pos"],
+                            x["k_c"], x["v_c"], D.ncap, self.idx if idx is None else idx,
+                            x["k_raw"], x["v_raw"], D.R, o, lse, dout, g["dq"], g["dk_c"],
+                            g["dv_c"], g["dk_raw"], g["dv_raw"], err=self.err, stream=stream)
+        hca_attend_backward(dt, D.B, D.T, D.H, D.d, D.m2, D.W, D.sm_scale, x["q_hca"],
+                            x["q_pos"], x["hk_c"], x["hv_c"], D.ncap2, x["hk_raw"], x["hv_raw"],
+                            D.R, ho, hlse, dhout, g["dq_hca"], g["dhk_c"], g["dhv_c"],
+                            g["dhk_raw"], g["dhv_raw"], err=self.err, stream=stream)
+        sa_compress_backward(dt, D.B, D.d, D.m, x["k_raw"], x["v_raw"], x["z"], D.R, x["blk_lo"],
+                             x["blk_hi"], D.max_blocks, g["dk_c"], g["dv_c"], D.ncap,
+                             g["dk_raw"], g["dv_raw"], g["dz"], err=self.err, stream=stream)
+        sa_compress_backward(dt, D.B, D.d, D.m2, x["hk_raw"], x["hv_raw"], x["hz"], D.R,
+                             x["hblk_lo"], x["hblk_hi"], D.max_blocks2, g["dhk_c"], g["dhv_c"],
+                             D.ncap2, g["dhk_raw"], g["dhv_raw"], g["dhz"], err=self.err,
+                             stream=stream)
+        return g
 
     def device_errors(self) -> int:
         return int(self.err.item())
