@@ -15,9 +15,10 @@
 //
 // Warp roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer and
 // TMEM owner, warps 2..9 = two epilogue warpgroups taking alternate tiles
-// (warp w reads TMEM lanes 32*(w%4)..+31).  Decode keeps 12 tiles (192 KB) in
-// flight per SM: under load a tile takes microseconds to arrive, and the
-// bytes in flight set the bandwidth.
+// (warp w reads TMEM lanes 32*(w%4)..+31).  A stage is two consecutive tiles
+// of one job, loaded by one 256-row TMA box (32 KB); decode keeps 6 stages
+// (192 KB) in flight per SM: under load a copy takes microseconds to arrive,
+// and the bytes in flight set the bandwidth.
 // A ring of shared-memory stages holds the streamed Ik_c tiles; several TMEM
 // accumulators let the epilogue of tile i overlap the MMAs of later tiles.
 // Persistent grid of at most one CTA per SM; a job is (query group, chunk of
@@ -39,11 +40,16 @@ constexpr int kHI = kIdxHeads;
 
 template <int QG>
 struct ScoreTcCfg {
-  static constexpr int kStages = QG == 1 ? 12 : 8;
+  // a stage holds two consecutive tiles of one job, loaded by one TMA box of
+  // 256 rows: the copy engine's cost is per request, so 32 KB requests stream
+  // faster per SM than 16 KB ones
+  static constexpr int kStageTiles = 2;
+  static constexpr int kStages = QG == 1 ? 6 : 4;
   static constexpr int kAccCols = QG * kHI;
   static constexpr int kAccBufs = QG == 1 ? 4 : 2;
   static constexpr int kTmemCols = kAccBufs * kAccCols;       // 256 or 512
-  static constexpr int kABytes = kTileEntries * kDI * 2;      // 16 KB
+  static constexpr int kTileBytes = kTileEntries * kDI * 2;   // 16 KB
+  static constexpr int kABytes = kStageTiles * kTileBytes;    // 32 KB
   static constexpr int kBBytes = QG * kHI * kDI * 2;          // 8 KB per query
   static constexpr size_t kSmem = 1024 /*align slack*/ + kStages * kABytes + 2 * kBBytes + 512 +
                                   kMaxJobsPerCta * sizeof(JobRec<QG>);
@@ -115,7 +121,7 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
           prev_g = J.g;
           ++nsw;
         }
-        for (int t = J.t_lo; t < J.t_hi; ++t) {
+        for (int t = J.t_lo; t < J.t_hi; t += Cfg::kStageTiles) {
           if (!mbar_wait(&empty[stage], ph ^ 1, p.err)) { *s_abort = 1; break; }
           mbar_arrive_expect_tx(&full[stage], Cfg::kABytes);
           tma_load_2d(&tm_ik, &full[stage], sA + stage * Cfg::kABytes, 0,
@@ -148,17 +154,20 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
         }
         const uint32_t b_base = smem_u32(sB + slot * Cfg::kBBytes);
         for (int t = J.t_lo; t < J.t_hi; ++t) {
-          if (!mbar_wait(&full[stage], ph, p.err)) { *s_abort = 1; break; }
+          const int half = (t - J.t_lo) % Cfg::kStageTiles;     // tile within its stage
+          if (half == 0 && !mbar_wait(&full[stage], ph, p.err)) { *s_abort = 1; break; }
           if (!mbar_wait(&tempty[acc], acc_ph ^ 1, p.err)) { *s_abort = 1; break; }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + stage * Cfg::kABytes);
+          const uint32_t a_base = smem_u32(sA + stage * Cfg::kABytes + half * Cfg::kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < kDI / 16; ++kk)
             tc_mma_f16(tmem + acc * Cfg::kAccCols, sdesc_kmajor_sw128(a_base + kk * 32),
                        sdesc_kmajor_sw128(b_base + kk * 32), idesc, kk > 0 ? 1u : 0u);
-          tc_commit(&empty[stage]);
           tc_commit(&tfull[acc]);
-          if (++stage == Cfg::kStages) { stage = 0; ph ^= 1; }
+          if (half == Cfg::kStageTiles - 1 || t == J.t_hi - 1) {
+            tc_commit(&empty[stage]);
+            if (++stage == Cfg::kStages) { stage = 0; ph ^= 1; }
+          }
           if (++acc == Cfg::kAccBufs) { acc = 0; acc_ph ^= 1; }
         }
       }
@@ -257,7 +266,8 @@ template <int QG>
 static cudaError_t launch_qg(const ScoreArgs& a, int num_sms, cudaStream_t st) {
   using Cfg = ScoreTcCfg<QG>;
   CUtensorMap tm_ik, tm_q;
-  if (!make_tmap_bf16_rows64(&tm_ik, a.ik, (uint64_t)a.B * a.N_cap, kTileEntries) ||
+  if (!make_tmap_bf16_rows64(&tm_ik, a.ik, (uint64_t)a.B * a.N_cap,
+                             Cfg::kStageTiles * kTileEntries) ||
       !make_tmap_bf16_rows64(&tm_q, a.q, (uint64_t)a.B * a.T * kHI, QG * kHI))
     return cudaErrorInvalidValue;
   ScoreJobs p{};
@@ -270,7 +280,7 @@ static cudaError_t launch_qg(const ScoreArgs& a, int num_sms, cudaStream_t st) {
   p.scores = a.scores;
   p.ld = a.ld;
   p.err = a.err;
-  const int grid = plan_score_jobs(p, QG, num_sms);
+  const int grid = plan_score_jobs(p, QG, num_sms, Cfg::kStageTiles);
   if (grid == 0) return cudaSuccess;
   if (grid < 0) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<QG>,

@@ -442,8 +442,10 @@ def test_attend_ignores_minus_one_inside_the_selection(dtype):
     oracle's key multiset does, on the tensor-core (bf16) and CUDA-core
     (f32) kernels alike.  Holes in every other row, a whole row of -1 in
     one."""
-    w = synth.Workload("holes", "decode", B=4, L=20003, T=1, R=128, k=256, x8=True, dtype=dtype,
-                       indexer=dtype)
+    # (fp32: no x8 rows, whose large logits are outside the 1e-5 regime of the
+    # fp32 configuration)
+    w = synth.Workload("holes", "decode", B=4, L=20003, T=1, R=128, k=256, x8=dtype == "bf16",
+                       dtype=dtype, indexer=dtype)
     x = synth.make_inputs(w)
     ref = oracle.reference(w, x)
     idx = ref["idx"].copy()
