@@ -32,6 +32,8 @@
  *    work is enqueued on `stream` (a cudaStream_t; NULL = legacy default).
  *  - Scratch memory is the caller's `ws` of `ws_bytes` bytes, at least the
  *    size the matching *_workspace_bytes() query returns (256-byte aligned).
+ *    The attention calls also keep a work counter there, zeroed by the call
+ *    on its stream: calls that share a workspace must not overlap.
  *  - Return value: SA_OK, or an sa_status for a host-side rejection (bad
  *    argument, unsupported shape) or a CUDA launch error.  Problems found on
  *    the device (an index out of range, a NaN score, a wait that timed out) are

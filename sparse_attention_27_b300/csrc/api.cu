@@ -57,6 +57,7 @@ size_t split_bytes(int64_t rows, int H, int d, const Split& s) {
   return round256(sizeof(float) * (size_t)rows * s.nsplit * H * d) +
          round256(sizeof(float) * (size_t)rows * s.nsplit * H);
 }
+constexpr size_t kCounterBytes = 256;   // the attention's item counter, after the partials
 int attn_tiles(int64_t n_comp_max, int W) {
   return (int)((n_comp_max + kAttnTile - 1) / kAttnTile + (W + kAttnTile - 1) / kAttnTile);
 }
@@ -86,15 +87,23 @@ int run_attention(AttnArgs& a, void* ws, size_t ws_bytes, int max_tiles, cudaStr
   a.split_tiles = s.split_tiles;
   a.part_o = nullptr;
   a.part_lse = nullptr;
+  a.item_counter = nullptr;
+  const size_t need = split_bytes(rows, a.H, a.d, s);
   if (s.nsplit > 1) {
-    const size_t need = split_bytes(rows, a.H, a.d, s);
     if (ws == nullptr || ws_bytes < need || !al16(ws)) return SA_ERR_INVALID_ARG;
     a.part_o = static_cast<float*>(ws);
     a.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) +
                                           round256(sizeof(float) * (size_t)rows * s.nsplit * a.H * a.d));
   }
-  cudaError_t e = attend_tc_supported(a) ? launch_attend_tc(a, device_sms(), st)
-                                         : launch_attend_simt(a, st);
+  const bool tc = attend_tc_supported(a);
+  if (tc && ws != nullptr && ws_bytes >= need + kCounterBytes && al16(ws)) {
+    // a workspace with room for the item counter: the tensor-core kernel takes
+    // its items dynamically
+    a.item_counter = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + need);
+    const cudaError_t z = cudaMemsetAsync(a.item_counter, 0, sizeof(unsigned), st);
+    if (z != cudaSuccess) return status_of(z);
+  }
+  cudaError_t e = tc ? launch_attend_tc(a, device_sms(), st) : launch_attend_simt(a, st);
   if (e != cudaSuccess) return status_of(e);
   return status_of(launch_merge_splits(a, st));
 }
@@ -193,7 +202,8 @@ int csa_index_topk(int q_dtype, int B, int T, int HI, int dI, int m, int k, cons
 size_t csa_attend_workspace_bytes(int dtype, int B, int T, int H, int d, int k, int W) {
   const int64_t rows = (int64_t)B * T;
   if (rows <= 0 || H <= 0 || d <= 0) return 0;
-  return split_bytes(rows, H, d, attention_split(dtype, rows, H, d, attn_tiles(k, W)));
+  return split_bytes(rows, H, d, attention_split(dtype, rows, H, d, attn_tiles(k, W))) +
+         kCounterBytes;
 }
 
 int csa_attend(int dtype, int B, int T, int H, int d, int m, int k, int W, float sm_scale,
@@ -225,7 +235,8 @@ size_t hca_compress_attend_workspace_bytes(int dtype, int B, int T, int H, int d
                                            int W) {
   const int64_t rows = (int64_t)B * T;
   if (rows <= 0 || H <= 0 || d <= 0) return 0;
-  return split_bytes(rows, H, d, attention_split(dtype, rows, H, d, attn_tiles(N2_cap, W)));
+  return split_bytes(rows, H, d, attention_split(dtype, rows, H, d, attn_tiles(N2_cap, W))) +
+         kCounterBytes;
 }
 
 int hca_compress_attend(int dtype, int B, int T, int H, int d, int m2, int W, float sm_scale,

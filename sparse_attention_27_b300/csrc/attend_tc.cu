@@ -9,7 +9,7 @@
 // "EP 95. DeepSeek-V4 논문 읽기 — 노정석", section IDEAS (one shared KV head).
 //
 // Work: an item is (query row, split of the row's key list); a persistent grid
-// of at most two CTAs per SM takes items c, c+G, ...  Two resident CTAs give
+// of at most two CTAs per SM takes items as they come free.  Two resident CTAs give
 // each SM two independent pipelines (each CTA: two K/V stages, one Q tile,
 // 256 TMEM columns).  A row's key list is the
 // compressed part (rows idx[r, i] for CSA, rows 0.. for HCA), padded to a
@@ -17,8 +17,14 @@
 // processed in tiles of 64 keys.
 //
 // Warp roles (288 threads):
-//  * warps 0-3, producers: warp w < kProducers issues the tiles with ordinal
-//    n = w (mod kProducers) (warps past kProducers only wait).
+//  * warp 3, fetcher: takes the CTA's items one by one from a counter shared
+//    by the grid (zeroed by the call before the launch) and passes them to
+//    the other roles through a two-slot ring in shared memory.  CTAs that
+//    start late -- behind another kernel that holds most SMs -- find the
+//    work already taken, so the grid never waits for them.  Without a
+//    counter it hands out items c, c+G, ...
+//  * warps 0-1, producers: warp w issues the tiles with ordinal n = w (mod
+//    kProducers).
 //    Lane l gathers keys 2l and 2l+1 -- sixteen 16-byte chunks of the K row
 //    and of the V row each, by cp.async, straight into the 128B-swizzled
 //    layout the tensor core reads (keys past the list are zero-filled) --
@@ -60,6 +66,10 @@ constexpr int kStages = 2;                     // K/V tiles in flight per CTA
 // kProducers waited for the release of tile n - kProducers - kStages, which
 // covers tile n - 2 * kStages as long as kProducers <= kStages.
 constexpr int kProducers = kStages;
+constexpr int kFetchWarp = 3;                  // fills the item ring (a warp no producer uses)
+// warps that read every item: the producers, the MMA warp, the 4 softmax warps
+constexpr int kItemReaders = kProducers + 1 + 4;
+static_assert(kProducers < kFetchWarp, "the fetcher is not a producer");
 constexpr int kQBufs = 1;                      // query tiles per CTA
 constexpr int kOBufs = 1;                      // TMEM O accumulators per CTA
 constexpr int kD = 128;                        // head dim
@@ -77,6 +87,8 @@ struct Ctl {
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], p_empty[2];
   uint64_t o_empty[kOBufs];
+  uint64_t it_full[2], it_empty[2];   // ring of the CTA's next items (fetched by warp 3)
+  int64_t it_slot[2];
   uint32_t tmem;
   int abort;
 };
@@ -161,6 +173,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       mbar_init(&C.p_empty[s], 1);
     }
     for (int s = 0; s < kOBufs; ++s) mbar_init(&C.o_empty[s], 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&C.it_full[s], 1);
+      mbar_init(&C.it_empty[s], kItemReaders);
+    }
     C.abort = 0;
     mbar_fence_init();
   }
@@ -171,7 +187,43 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   tc_fence_after();
   const uint32_t tmem = C.tmem;
 
-  if (warp < 4) {
+  // The e-th item of this CTA (-1: none left), from the ring warp 3 fills;
+  // lane 0 of each reading warp releases the slot once the warp has read it.
+  auto next_item = [&](int64_t e, bool whole_warp) -> int64_t {
+    const int slot = (int)(e & 1);
+    if (!mbar_wait(&C.it_full[slot], (uint32_t)((e >> 1) & 1), a.err)) {
+      *abort_flag = 1;
+      return -1;
+    }
+    const int64_t it = *reinterpret_cast<volatile int64_t*>(&C.it_slot[slot]);
+    if (whole_warp) __syncwarp();
+    if (!whole_warp || lane == 0) mbar_arrive(&C.it_empty[slot]);
+    return it;
+  };
+
+  if (warp == kFetchWarp) {
+    // ======================================================= item fetcher
+    // Items come from a counter shared by the grid (dynamic: CTAs that start
+    // late, behind other kernels, find the work already taken), or c, c+G,
+    // ... without one.
+    if (lane == 0) {
+      for (int64_t e = 0;; ++e) {
+        const int slot = (int)(e & 1);
+        int64_t it = -1;
+        if (mbar_wait(&C.it_empty[slot], (uint32_t)(((e >> 1) & 1) ^ 1), a.err)) {
+          it = a.item_counter ? (int64_t)atomicAdd(a.item_counter, 1u)
+                              : (int64_t)blockIdx.x + e * gridDim.x;
+          if (it >= n_items || *abort_flag) it = -1;
+        } else {
+          *abort_flag = 1;
+        }
+        *reinterpret_cast<volatile int64_t*>(&C.it_slot[slot]) = it;
+        mbar_arrive(&C.it_full[slot]);
+        if (it < 0) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp < kProducers) {
     // ============================================================ producer
     // warp w issues the tiles with ordinal n = w (mod kProducers): lane l gathers keys
     // 2l and 2l+1 (16 chunks of K and 16 of V each), waits for its copies,
@@ -182,7 +234,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const __nv_bfloat16* vr = static_cast<const __nv_bfloat16*>(a.vr);
     int64_t n = 0, e = 0;
     bool ok = true;
-    for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    for (int64_t ei = 0; ok; ++ei) {
+      const int64_t it = next_item(ei, true);
+      if (it < 0) break;
       const Item I = make_item(a, it);
       if (I.nt == 0) continue;
       if (warp == 0) {            // the item's query heads, once the MMA warp has let go of the buffer
@@ -242,6 +296,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     if (!ok) *abort_flag = 1;
+  } else if (warp < 4) {
+    // warps between the producers and the fetcher have no role
   } else if (warp == 4) {
     // ================================================================= MMA
     if (lane == 0) {
@@ -269,7 +325,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         tc_commit(&C.p_empty[pb]);
         return true;
       };
-      for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      for (int64_t ei = 0; ok; ++ei) {
+        const int64_t it = next_item(ei, false);
+        if (it < 0) break;
         const Item I = make_item(a, it);
         if (I.nt == 0) continue;
         const int qb = (int)(e % kQBufs), ob = (int)(e % kOBufs);
@@ -317,7 +375,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const float c2 = a.sm_scale * 1.4426950408889634f;   // natural logits -> log2 units
     int64_t n = 0, e = 0;
     bool ok = true;
-    for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x) {
+    for (int64_t ei = 0;; ++ei) {
+      const int64_t it = next_item(ei, true);
+      if (it < 0) break;
       const Item I = make_item(a, it);
       // a split partial (f32) or the row's output (f32 or bf16): element offset
       // `off` of the row's [H, d] block, two consecutive columns at a time

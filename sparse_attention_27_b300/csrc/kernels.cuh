@@ -82,6 +82,7 @@ struct AttnArgs {
   int split_tiles;      // key tiles (of kAttnTile keys) per split
   float* part_o;        // [B*T, nsplit, H, d] when nsplit > 1
   float* part_lse;      // [B*T, nsplit, H]
+  unsigned* item_counter;   // zeroed before the launch: items taken dynamically (or NULL)
   int32_t* err;
 };
 constexpr int kAttnTile = 64;     // keys per attention tile (split granularity)

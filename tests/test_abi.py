@@ -89,13 +89,15 @@ def test_attention_workspace_queries_follow_the_split_rule():
     rule: key lists of 64-key tiles; the tensor-core kernel aims at 2 (row,
     split) items per SM and at most 32 tiles per split; split s has
     ceil(tiles / ns) tiles; partials are rows*nsplit*H*d f32 for O plus
-    rows*nsplit*H f32 for LSE, each rounded up to 256 B.  148 SMs (the count
-    the library assumes without a device)."""
+    rows*nsplit*H f32 for LSE, each rounded up to 256 B, then 256 B for the
+    tensor-core kernel's item counter.  148 SMs (the count the library
+    assumes without a device)."""
     import sparse_attention_27_b300 as m
 
     def ws(rows, nsplit, H=64, d=128):
         r256 = lambda x: (x + 255) // 256 * 256
-        return r256(4 * rows * nsplit * H * d) + r256(4 * rows * nsplit * H)
+        parts = r256(4 * rows * nsplit * H * d) + r256(4 * rows * nsplit * H) if nsplit > 1 else 0
+        return parts + 256
     # 128K decode CSA: 32 rows, 2048/64 + 128/64 = 34 tiles; want ceil(296/32) = 10
     # splits -> 4 tiles each -> 9 splits
     assert m.csa_attend_workspace_bytes(m.SA_BF16, 32, 1, 64, 128, 2048, 128) == ws(32, 9)
@@ -108,7 +110,7 @@ def test_attention_workspace_queries_follow_the_split_rule():
     # 64K prefill CSA: one split wanted, but at most 32 tiles per split -> 2 splits of 17
     assert m.csa_attend_workspace_bytes(m.SA_BF16, 1, 65536, 64, 128, 2048, 128) == ws(65536, 2)
     # fp32 (CUDA-core kernel, one item per CTA): 256 rows fill the SMs, no split
-    assert m.csa_attend_workspace_bytes(m.SA_F32, 1, 256, 16, 128, 64, 128) == 0
+    assert m.csa_attend_workspace_bytes(m.SA_F32, 1, 256, 16, 128, 64, 128) == ws(256, 1)
 
 
 def test_noalloc_limit_matches_the_header():
