@@ -238,6 +238,69 @@ def run_prefill_calls(args) -> None:
           flush=True)
 
 
+def fp32_alu_peak(device: int = 0) -> float:
+    """fp32 CUDA-core peak in TFLOP/s: SMs x 128 fp32 lanes x 2 (FMA) x the
+    SM clock's maximum (NVML), the bound of the backward's CUDA-core kernels."""
+    import torch
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    mhz = Clocks(device).max_mhz or 2032.0
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def backward_pairs(w, pos) -> dict:
+    """(query, key) pairs of the backward's attention: CSA selected + window,
+    HCA visible + window (as prefill_pairs)."""
+    return prefill_pairs(w, pos)
+
+
+def backward_calls(steps: int, warmup: int, device: int = 0) -> dict:
+    """Time the backward of one pass -- csa_attend_backward,
+    hca_attend_backward and the two sa_compress_backward calls -- at the 128K
+    decode shape (32 rows) and on a 4096-token prefill chunk.  Flops: 10*H*d
+    per (query, key) pair (S, dP, dq, dK and dV products)."""
+    import torch
+    import synth
+    from sparse_attention_27_b300.path import step_from
+    out = {}
+    peak = fp32_alu_peak(device)
+    for name, w in (("decode128k", synth.WORKLOADS["decode128k"]),
+                    ("prefill4k", synth.Workload("prefill4k", "prefill", B=1, L=4096, T=4096,
+                                                  x8=True))):
+        x = synth.make_inputs(w)
+        step = step_from(w, x, o_dtype="f32")
+        step.run()
+        g = torch.Generator(device="cuda")
+        g.manual_seed(5)
+        dO = torch.randn(step.o.shape, device="cuda", generator=g)
+        dhO = torch.randn(step.o.shape, device="cuda", generator=g)
+        for _ in range(warmup):
+            step.backward(dO, dhO)
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            step.backward(dO, dhO)
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        pairs = backward_pairs(w, x["q_pos"])
+        flop = (pairs["csa"] + pairs["hca"]) * 10 * w.H * w.d
+        tf = flop / (ms * 1e-3) / 1e12
+        out[name] = {"ms": ms, "tflop": flop / 1e12, "tflops": tf,
+                     "roofline": {"bound": "alu", "achieved": tf, "peak": peak,
+                                  "unit": "TFLOP/s", "frac": tf / peak,
+                                  "peak_source": "SMs x 128 fp32 lanes x 2 x max SM clock"},
+                     "device_errors": step.device_errors()}
+        del step, x
+        torch.cuda.empty_cache()
+    out["note"] = ("backward of one pass (selection fixed): attention of both layers and the "
+                   "pooling; fp32 CUDA-core kernels; gradient buffers allocated and zeroed "
+                   "inside the timed call")
+    return out
+
+
 class Clocks:
     """SM clock and clock-event reasons sampled every ~2 ms by a background
     thread while the timed region runs, read through NVML (the driver's
@@ -696,6 +759,7 @@ def main() -> None:
         torch.cuda.empty_cache()
         extra["decode1m"] = m1
         extra["prefill64k"] = prefill_calls(steps=3, warmup=1, device=local)
+        extra["backward"] = backward_calls(steps=5, warmup=2, device=local)
 
     if rank == 0:
         line = {

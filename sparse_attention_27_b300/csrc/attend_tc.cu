@@ -25,9 +25,10 @@
 //    counter it hands out items c, c+G, ...
 //  * warps 0-1, producers: warp w issues the tiles with ordinal n = w (mod
 //    kProducers).
-//    Lane l gathers keys 2l and 2l+1 -- sixteen 16-byte chunks of the K row
-//    and of the V row each, by cp.async, straight into the 128B-swizzled
-//    layout the tensor core reads (keys past the list are zero-filled) --
+//    Lane l finds the source rows of keys 2l and 2l+1; then each cp.async
+//    instruction of the warp copies two whole 256-byte rows (half-warp per
+//    key, one 16-byte chunk per lane) straight into the 128B-swizzled layout
+//    the tensor core reads (keys past the list are zero-filled); the warp
 //    waits for its copies, fences them to the async proxy and arrives on the
 //    stage's mbarrier, so two tiles are in flight per CTA (four per SM).
 //    Warp 0 also brings the item's 64 query heads by one TMA tiled load per
@@ -181,6 +182,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     mbar_fence_init();
   }
   if (warp == 0 && lane == 0) tma_prefetch_desc(&tm.q);
+  // the fetcher claims its first item now, so the round trip to the counter
+  // overlaps the set-up
+  int64_t first_item = -1;
+  if (warp == kFetchWarp && lane == 0)
+    first_item = a.item_counter ? (int64_t)atomicAdd(a.item_counter, 1u) : (int64_t)blockIdx.x;
   if (warp == 4) tmem_alloc(&C.tmem, kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -211,8 +217,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int slot = (int)(e & 1);
         int64_t it = -1;
         if (mbar_wait(&C.it_empty[slot], (uint32_t)(((e >> 1) & 1) ^ 1), a.err)) {
-          it = a.item_counter ? (int64_t)atomicAdd(a.item_counter, 1u)
-                              : (int64_t)blockIdx.x + e * gridDim.x;
+          it = e == 0 ? first_item
+                      : a.item_counter ? (int64_t)atomicAdd(a.item_counter, 1u)
+                                       : (int64_t)blockIdx.x + e * gridDim.x;
           if (it >= n_items || *abort_flag) it = -1;
         } else {
           *abort_flag = 1;
@@ -258,35 +265,43 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           break;
         }
         unsigned char* stage = sKV + st * kStageBytes;
+        // lane l resolves the source rows of keys 2l and 2l+1 as (row << 1 | raw),
+        // -1 for a key with no row (masked: zero-filled)
+        int64_t src2[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          const int key = 2 * lane + q;
-          const int64_t s = (I.t_begin + t) * kKeys + key;
-          const __nv_bfloat16* ks = kr;
-          const __nv_bfloat16* vs = vr;
-          int64_t row = -1;
+          const int64_t s = (I.t_begin + t) * kKeys + 2 * lane + q;
+          int64_t code = -1;
           if (s < I.n_comp) {
             const int64_t j = a.gather ? (int64_t)__ldg(a.idx + I.row * a.k + s) : s;
-            if (j >= 0 && j < I.nvis) {
-              row = (int64_t)I.b * a.N_cap + j;
-              ks = kc;
-              vs = vc;
-            } else if (j != -1) {
-              set_err(a.err, SA_ERR_BOUNDS);
-            }
+            if (j >= 0 && j < I.nvis) code = ((int64_t)I.b * a.N_cap + j) << 1;
+            else if (j != -1) set_err(a.err, SA_ERR_BOUNDS);
           } else if (s >= I.n_comp_pad && s < I.n_comp_pad + I.n_win) {
             const int64_t u = (int64_t)I.p - I.n_win + 1 + (s - I.n_comp_pad);
-            row = (int64_t)I.b * a.R + u % a.R;
+            code = (((int64_t)I.b * a.R + u % a.R) << 1) | 1;
           }
-          const uint32_t bytes = row >= 0 ? 16u : 0u;
-          const int64_t off = (row >= 0 ? row : 0) * kD;
-          const uint32_t kd = smem_u32(stage), vd = smem_u32(stage) + 2 * kHalf;
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const uint32_t o = (c >> 3) * kHalf + swz(key, c & 7);
-            cp_async16(kd + o, ks + off + c * 8, bytes);
-            cp_async16(vd + o, vs + off + c * 8, bytes);
-          }
+          src2[q] = code;
+        }
+        // then the warp copies two keys per instruction: half-warp h takes key
+        // 2p + h of pair p, lane l its 16-byte chunk l % 16 -- each instruction
+        // reads two whole 256-byte rows, so the memory system sees four full
+        // lines instead of 32 scattered sectors
+        const uint32_t kd = smem_u32(stage), vd = smem_u32(stage) + 2 * kHalf;
+        const int hw = lane >> 4, ch = lane & 15;
+#pragma unroll 4
+        for (int pr = 0; pr < kKeys / 2; ++pr) {
+          const int64_t c0 = __shfl_sync(0xffffffffu, src2[0], pr);
+          const int64_t c1 = __shfl_sync(0xffffffffu, src2[1], pr);
+          const int64_t code = hw ? c1 : c0;
+          const int key = 2 * pr + hw;
+          const bool raw = code >= 0 && (code & 1);
+          const __nv_bfloat16* ks = raw ? kr : kc;
+          const __nv_bfloat16* vs = raw ? vr : vc;
+          const uint32_t bytes = code >= 0 ? 16u : 0u;
+          const int64_t off = (code >= 0 ? (code >> 1) : 0) * kD + ch * 8;
+          const uint32_t o = (ch >> 3) * kHalf + swz(key, ch & 7);
+          cp_async16(kd + o, (code >= 0 ? ks : kr) + off, bytes);
+          cp_async16(vd + o, (code >= 0 ? vs : vr) + off, bytes);
         }
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
         fence_proxy_async_smem();

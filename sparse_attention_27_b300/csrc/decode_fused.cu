@@ -446,34 +446,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         unsigned char* stage = sKV + st * kKVBytes;
         const uint32_t kd = smem_u32(stage), vd = kd + 2 * kHalf;
+        // lane l resolves the source rows of keys 2l and 2l+1 as (row << 1 | raw),
+        // -1 for a key with no row (masked: zero-filled); then each cp.async
+        // instruction copies two whole 256-byte rows (half-warp per key, one
+        // 16-byte chunk per lane), four full lines per instruction
+        int64_t src2[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          const int key = 2 * lane + q;
-          const int s = (at_lo + n) * kKeys + key;            // list position
-          const __nv_bfloat16* ks = kr;
-          const __nv_bfloat16* vs = vr;
-          int64_t row = -1;
+          const int s = (at_lo + n) * kKeys + 2 * lane + q;   // list position
+          int64_t code = -1;
           if (s < P.n_comp) {
             const int j = sel[s - sel_lo];
-            if (j >= 0 && j < P.n) {
-              row = (int64_t)b * a.N_cap + j;
-              ks = kc;
-              vs = vc;
-            } else if (j != -1) {
-              set_err(a.err, SA_ERR_BOUNDS);
-            }
+            if (j >= 0 && j < P.n) code = ((int64_t)b * a.N_cap + j) << 1;
+            else if (j != -1) set_err(a.err, SA_ERR_BOUNDS);
           } else if (s >= P.n_comp_pad && s < P.n_comp_pad + P.n_win) {
             const int64_t u = (int64_t)P.p - P.n_win + 1 + (s - P.n_comp_pad);
-            row = (int64_t)b * a.R + u % a.R;
+            code = (((int64_t)b * a.R + u % a.R) << 1) | 1;
           }
-          const uint32_t bytes = row >= 0 ? 16u : 0u;
-          const int64_t off = (row >= 0 ? row : 0) * kD;
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const uint32_t o = (c >> 3) * kHalf + swz(key, c & 7);
-            cp_async16(kd + o, ks + off + c * 8, bytes);
-            cp_async16(vd + o, vs + off + c * 8, bytes);
-          }
+          src2[q] = code;
+        }
+        const int hw = lane >> 4, ch = lane & 15;
+#pragma unroll 4
+        for (int pr = 0; pr < kKeys / 2; ++pr) {
+          const int64_t c0 = __shfl_sync(0xffffffffu, src2[0], pr);
+          const int64_t c1 = __shfl_sync(0xffffffffu, src2[1], pr);
+          const int64_t code = hw ? c1 : c0;
+          const int key = 2 * pr + hw;
+          const bool raw = code >= 0 && (code & 1);
+          const __nv_bfloat16* ks = raw ? kr : kc;
+          const __nv_bfloat16* vs = raw ? vr : vc;
+          const uint32_t bytes = code >= 0 ? 16u : 0u;
+          const int64_t off = (code >= 0 ? (code >> 1) : 0) * kD + ch * 8;
+          const uint32_t o = (ch >> 3) * kHalf + swz(key, ch & 7);
+          cp_async16(kd + o, (code >= 0 ? ks : kr) + off, bytes);
+          cp_async16(vd + o, (code >= 0 ? vs : vr) + off, bytes);
         }
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
         fence_proxy_async_smem();
