@@ -18,17 +18,17 @@
 //  1. scores: warp 0 streams the slice's indexer-key tiles by TMA through a
 //     ring of 32 KB stages (two 128-entry tiles per copy: the copy engine's
 //     cost is per request, so larger requests stream faster per SM); warp 1 issues tcgen05 MMAs D[j, h] =
-//     Ik_c[j] . q_I[h] (M = 128 entries, N = 64 heads, K = 64) into four TMEM
-//     accumulators; warps 4-11 (two warpgroups, alternate tiles) fold ReLU
-//     and the head weights in fp32 and write each score as an
-//     order-preserving 32-bit key into shared memory -- the scores never go to
-//     global memory.  Meanwhile warps 12-15 pool the blocks this step
+//     Ik_c[j] . q_I[h] (M = 128 entries, N = 64 heads, K = 64) into six TMEM
+//     accumulators; three warpgroups (warps 4-7, 8-11, 12-15; tiles
+//     round-robin) fold ReLU and the head weights in fp32 and write each score
+//     as an order-preserving 32-bit key into shared memory -- the scores never
+//     go to global memory.  Warps 12-15 first pool the blocks this step
 //     compresses (the block the new token closes) and write them to the
 //     caches; the producer loads a tile holding such a block only after them.
 //  2. top-k: the row's exact top-k over the cluster (topk_dev.cuh: a 13-bit
 //     histogram summed over distributed shared memory, an exact select in
-//     the k-th key's bin, emission in index order).  Each selected index goes
-//     to the idx output and into the shared memory of the CTA that attends it.
+//     the k-th key's bin, emission in index order) into the idx output; each
+//     CTA then reads its share of the key list back through L2.
 //  3. attention: the key list (selected rows ascending, padded to a multiple
 //     of 4, then the window) is cut into tiles of 64 keys, and CTA r attends
 //     its contiguous share of the tiles: warps 12-15 gather K/V rows by 16-byte
@@ -67,8 +67,9 @@ constexpr int kQBytes = kHeads * kD * 2;       // 16 KB: the row's query heads
 constexpr int kHalf = kKeys * 128;             // 8 KB: 64 dims of a K or V tile
 constexpr int kKVBytes = 4 * kHalf;            // 32 KB: one K/V stage
 constexpr int kPBytes = kHeads * kKeys * 2;    // 8 KB
-constexpr int kAcc = 4;                        // score accumulators (64 TMEM columns each)
-constexpr int kTmemCols = 256;                 // score: 4 x 64; attention: S 2 x 64 + O 128
+constexpr int kEpiGroups = 3;                  // score epilogue warpgroups (tiles round-robin)
+constexpr int kAcc = 6;                        // score accumulators (64 TMEM columns each)
+constexpr int kTmemCols = 512;                 // score: 6 x 64; attention: S 2 x 64 + O 128
 constexpr int kMaxStagesA = 6, kMaxStagesKV = 6;
 constexpr int kMaxPool = 128;                  // largest block size m this kernel pools
 constexpr float kRescaleThreshold = 32.f;      // log2 units
@@ -116,14 +117,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // block with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
-}
-
-// Store a 32-bit word into the shared memory of CTA `rank` of this cluster.
-__device__ __forceinline__ void dsmem_st_u32(void* local_ptr, uint32_t rank, uint32_t v) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_ptr)),
-               "r"(rank));
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
 }
 
 // The row's geometry, the same in every CTA of the cluster.
@@ -306,13 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) *abort_flag = 1;
     }
     __syncwarp();
-  } else if (warp >= kWarpEpi && warp < kWarpEpi + 8) {
-    // two warpgroups take alternate tiles; warp w reads TMEM lanes 32*(w%4)..
-    const int grp = (warp - kWarpEpi) >> 2;
+  }
+  // The score epilogue of warpgroup grp (tiles o = grp (mod kEpiGroups));
+  // warp w reads TMEM lanes 32*(w%4)..
+  auto score_epilogue = [&](int grp) {
     const int quad = warp & 3;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const float4* w4 = reinterpret_cast<const float4*>(C.w);
-    for (int o = grp; o < nt_score; o += 2) {
+    for (int o = grp; o < nt_score; o += kEpiGroups) {
       const int acc = o % kAcc;
       if (*abort_flag || !mbar_wait(&C.t_full[acc], (uint32_t)((o / kAcc) & 1), a.err)) {
         *abort_flag = 1;
@@ -320,28 +314,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t v[32];
-        tmem_ld32_async(tmem + lane_base + acc * kHI + half * 32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 wv = w4[half * 8 + i];
-          s0 = fmaf(wv.x, fmaxf(__uint_as_float(v[4 * i + 0]), 0.f), s0);
-          s1 = fmaf(wv.y, fmaxf(__uint_as_float(v[4 * i + 1]), 0.f), s1);
-          s2 = fmaf(wv.z, fmaxf(__uint_as_float(v[4 * i + 2]), 0.f), s2);
-          s3 = fmaf(wv.w, fmaxf(__uint_as_float(v[4 * i + 3]), 0.f), s3);
-        }
-      }
+      uint32_t v[64];
+      tmem_ld32_async(tmem + lane_base + acc * kHI, v);
+      tmem_ld32_async(tmem + lane_base + acc * kHI + 32, v + 32);
+      tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&C.t_empty[acc]);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float4 wv = w4[i];
+        s0 = fmaf(wv.x, fmaxf(__uint_as_float(v[4 * i + 0]), 0.f), s0);
+        s1 = fmaf(wv.y, fmaxf(__uint_as_float(v[4 * i + 1]), 0.f), s1);
+        s2 = fmaf(wv.z, fmaxf(__uint_as_float(v[4 * i + 2]), 0.f), s2);
+        s3 = fmaf(wv.w, fmaxf(__uint_as_float(v[4 * i + 3]), 0.f), s3);
+      }
       const float s = (s0 + s1) + (s2 + s3);
       const int jl = o * kTile + quad * 32 + lane;          // slot in this CTA's keys
       const bool real = lo + jl < P.n;
       nan_local |= real && is_nan_bits(s);
       keys[jl] = real ? score_key(s) : 0u;
     }
+  };
+  if (warp >= kWarpEpi && warp < kWarpEpi + 8) {
+    score_epilogue((warp - kWarpEpi) >> 2);
   } else if (warp >= kWarpAux) {
     // pool this CTA's share of the step's blocks (K, V and the indexer key),
     // then release the producer's wait on them
@@ -383,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     mbar_arrive(&C.fresh);
+    score_epilogue(2);                           // then the third epilogue warpgroup
   }
   tc_fence_before();
   nan_local = __syncthreads_or(nan_local);
@@ -397,24 +393,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     for (int i = tid; i < cnt; i += kThreads) atomicAdd(&hist[keys[i] >> kFineShift], 1);
     __syncthreads();
-    auto emit = [&](int pos, int j) {
-      out_idx[pos] = j;
-      const int owner = (pos / kKeys) / P.qt;    // the CTA whose attention tiles hold pos
-      const int slot = pos - owner * P.qt * kKeys;
-      if (Cn > 1) dsmem_st_u32(sel + slot, (uint32_t)owner, (uint32_t)j);
-      else sel[slot] = j;
-    };
+    auto emit = [&](int pos, int j) { out_idx[pos] = j; };
     if (a.cap == 8192)
       topk_select<kThreads, 16>(TS, keys, cnt, lo, hist, ck, ci, nan_local, k, Cn, rank, a.err,
                                 emit);
     else
       topk_select<kThreads, 32>(TS, keys, cnt, lo, hist, ck, ci, nan_local, k, Cn, rank, a.err,
                                 emit);
-    // padding slots [n_comp, n_comp_pad) of this CTA's share of the list
+    // the selection is complete in global memory (topk_select ends with a
+    // cluster barrier after the emission): this CTA's share of the key list,
+    // read through L2 (other CTAs wrote it), padding slots -1
     for (int s = tid; s < P.qt * kKeys; s += kThreads) {
       const int pos = sel_lo + s;
-      if (pos >= P.n_comp && pos < P.n_comp_pad) sel[s] = -1;
+      sel[s] = pos < P.n_comp ? __ldcg(out_idx + pos) : -1;
     }
+    __syncthreads();
   } else {
     // every visible entry is selected, in order
     for (int i = rank * kThreads + tid; i < k; i += Cn * kThreads) out_idx[i] = i < P.n ? i : -1;
@@ -422,10 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pos = sel_lo + s;
       sel[s] = pos < P.n_comp ? pos : -1;
     }
+    // the pooled rows (global memory, written by the pooling CTA) are visible
+    // to every CTA of the cluster
+    if (Cn > 1) cluster_sync(); else __syncthreads();
   }
-  // the selected lists (written across the cluster) and the pooled rows
-  // (global memory) are complete and visible to every CTA of the cluster
-  if (Cn > 1) cluster_sync(); else __syncthreads();
   tc_fence_after();
 
   // ====================================================== 3. attention
