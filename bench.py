@@ -537,7 +537,11 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
     step = step_from(w, x, o_dtype="bf16")
     io = StepIO(step, x, w)         # packs per-step inputs and outputs (before capture)
     s_csa, s_hca = torch.cuda.Stream(), torch.cuda.Stream()
-    fused = schedule == "fused" or (schedule == "auto" and step.fused_ok())
+    # auto: the fused CSA layer (one cluster of CTAs per sequence) where the
+    # batch fills most of the GPU with clusters (measured: 100 vs 108 us a
+    # step at 128K, B = 32); with few sequences (1M, B = 4) the clusters leave
+    # most SMs idle and the separate calls are faster (86 vs 125 us)
+    fused = schedule == "fused" or (schedule == "auto" and step.fused_ok() and w.B >= 16)
     run_step = step.run_fused_two_streams if fused else step.run_two_streams
     for _ in range(2):              # outside the graph: sets kernel attributes, loads modules
         run_step(s_csa, s_hca)
