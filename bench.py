@@ -370,92 +370,152 @@ class Clocks:
         return out
 
 
-class StepIO:
-    """Host <-> device traffic of one decode step for the end-to-end figure.
+def load_cudart():
+    """The CUDA runtime library, for the graph API calls of graph_kernels."""
+    for name in ("libcudart.so.13", "libcudart.so"):
+        try:
+            return ctypes.CDLL(name)
+        except OSError:
+            continue
+    raise RuntimeError("libcudart not found")
 
-    Each layer's share of the new token's inputs (CSA: q, q_I, w; HCA: q_hca
-    and the positions both layers read) lives in one device buffer filled by
-    one copy from one pinned host buffer; the new raw rows (ring slot t mod R
-    of the layer's per-token arrays) are written by one strided 2-D copy per
-    array; each layer's outputs (O and LSE) live in one device buffer read
-    back by one copy.  Every copy is issued on its layer's stream."""
 
-    IN = {"csa": ["q", "q_idx", "w_idx"], "hca": ["q_hca", "q_pos"]}
+class PipelinedIO:
+    """End-to-end decode steps from pinned host memory, double-buffered.
+
+    Two HybridSteps (slots 0 and 1) share the caches and rings; each has its
+    own per-step inputs -- q, q_hca, q_idx, w_idx, q_pos and the new token's
+    ring rows (staged) -- in one device buffer filled by one copy from one
+    pinned host buffer, and its own outputs (o, lse, ho, hlse) in one device
+    buffer read back by one copy.  ``record`` captures two consecutive steps:
+    while step 0 computes, step 1's inputs come in on a copy stream; step 0's
+    outputs go out while step 1 computes; step 0's slot is refilled for the
+    next pair once step 0 is done with it.  Each step writes its ring rows
+    (ring slot t mod R of every layer's per-token arrays) from its staged copy
+    on its layer's stream just before its layer runs, so no step writes a ring
+    row another step may still read.  Every step's copies are inside the
+    timed region."""
+
+    IN = ["q", "q_hca", "q_idx", "w_idx", "q_pos"]
     RING = {"csa": ["k_raw", "v_raw", "ik_raw", "z"], "hca": ["hk_raw", "hv_raw", "hz"]}
-    OUT = {"csa": ["o", "lse"], "hca": ["ho", "hlse"]}
+    OUT = ["o", "lse", "ho", "hlse"]
 
-    def __init__(self, step, x, w):
+    def __init__(self, w, x, fused: bool):
         import numpy as np
         import torch
-        dev = step.o.device
-
-        def carve(tensors):
-            offs, off = [], 0
-            for t in tensors:
-                offs.append(off)
-                off += (t.numel() * t.element_size() + 255) // 256 * 256
-            buf = torch.empty(off, dtype=torch.uint8, device=dev)
-            views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-                     for o, t in zip(offs, tensors)]
-            return buf, views
-
-        self.d_in, self.h_in, self.d_out, self.h_out, self.rings = {}, {}, {}, {}, {}
+        from sparse_attention_27_b300.path import HybridStep, step_from
+        self.fused = fused
+        base = step_from(w, x, o_dtype="bf16")
+        dev = base.o.device
         slot = (w.L - 1) % w.ring
-        for g in ("csa", "hca"):
-            ins = [step.x[n] for n in self.IN[g]]
-            self.d_in[g], views = carve(ins)
-            for n, t, v in zip(self.IN[g], ins, views):
-                v.copy_(t)
-                step.x[n] = v
-            self.h_in[g] = torch.empty(self.d_in[g].numel(), dtype=torch.uint8, pin_memory=True)
-            self.h_in[g].copy_(self.d_in[g].cpu())
-            outs = [getattr(step, n) for n in self.OUT[g]]
-            self.d_out[g], views = carve(outs)
-            for n, v in zip(self.OUT[g], views):
-                setattr(step, n, v)
-            self.h_out[g] = torch.empty(self.d_out[g].numel(), dtype=torch.uint8,
-                                        pin_memory=True)
-            self.rings[g] = []
-            for n in self.RING[g]:
-                d = step.x[n]
-                row = d[0, 0].numel() * d.element_size()
-                h = torch.from_numpy(np.ascontiguousarray(x[n][:, slot]).view(np.uint8)
-                                     .reshape(-1)).pin_memory()
-                self.rings[g].append((d.data_ptr() + slot * row, d.stride(0) * d.element_size(),
-                                      h, row, d.shape[0]))
-        self.h2d_bytes = sum(self.d_in[g].numel() + sum(r[3] * r[4] for r in self.rings[g])
-                             for g in ("csa", "hca"))
-        self.d2h_bytes = sum(self.d_out[g].numel() for g in ("csa", "hca"))
-        self.copies = sum(2 + len(self.rings[g]) for g in ("csa", "hca"))
-        self.cudart = None
-        for name in ("libcudart.so.13", "libcudart.so"):
-            try:
-                self.cudart = ctypes.CDLL(name)
-                break
-            except OSError:
-                continue
-        if self.cudart is None:
-            raise RuntimeError("libcudart not found for the strided host-to-device copies")
+        ring_names = self.RING["csa"] + self.RING["hca"]
+        self.steps, self.d_in, self.h_in, self.d_out, self.h_out, self.staged = [], [], [], [], [], []
+        for p in range(2):
+            xs = dict(base.x)
+            tens = [base.x[n] for n in self.IN] + [base.x[n][:, slot] for n in ring_names]
+            buf, views = self._carve(tens, dev)
+            for n, v in zip(self.IN, views[:len(self.IN)]):
+                v.copy_(base.x[n])
+                xs[n] = v
+            staged = dict(zip(ring_names, views[len(self.IN):]))
+            for n, v in staged.items():
+                v.copy_(base.x[n][:, slot])
+            st = base if p == 0 else HybridStep(base.D, xs, dev)
+            if p == 0:
+                for n in self.IN:
+                    st.x[n] = xs[n]
+            outs = [getattr(st, n) for n in self.OUT]
+            obuf, oviews = self._carve(outs, dev)
+            for n, v in zip(self.OUT, oviews):
+                setattr(st, n, v)
+            hbuf = torch.empty(buf.numel(), dtype=torch.uint8, pin_memory=True)
+            hbuf.copy_(buf.cpu())
+            self.steps.append(st)
+            self.d_in.append(buf)
+            self.h_in.append(hbuf)
+            self.staged.append(staged)
+            self.d_out.append(obuf)
+            self.h_out.append(torch.empty(obuf.numel(), dtype=torch.uint8, pin_memory=True))
+        self.slot = slot
+        self.h2d_bytes = self.d_in[0].numel()
+        self.d2h_bytes = self.d_out[0].numel()
+        self.copies = 2
 
-    def h2d(self, g, stream):
-        """Layer g's inputs, host to device, on ``stream``."""
+    @staticmethod
+    def _carve(tensors, dev):
         import torch
-        with torch.cuda.stream(stream):
-            self.d_in[g].copy_(self.h_in[g], non_blocking=True)
-        ct = ctypes
-        for dst, pitch, h, row, nrows in self.rings[g]:
-            rc = self.cudart.cudaMemcpy2DAsync(ct.c_void_p(dst), ct.c_size_t(pitch),
-                                               ct.c_void_p(h.data_ptr()), ct.c_size_t(row),
-                                               ct.c_size_t(row), ct.c_size_t(nrows), 1,
-                                               ct.c_void_p(stream.cuda_stream))
-            if rc != 0:
-                raise RuntimeError(f"cudaMemcpy2DAsync failed: {rc}")
+        offs, off = [], 0
+        for t in tensors:
+            offs.append(off)
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        buf = torch.empty(off, dtype=torch.uint8, device=dev)
+        views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                 for o, t in zip(offs, tensors)]
+        return buf, views
 
-    def d2h(self, g, stream):
-        """Layer g's outputs, device to host, on ``stream``."""
+    def _compute(self, p, s_csa, s_hca):
+        """Step p on the two layer streams, scheduled as in the device-timed
+        step: fused, both layers at once; split, HCA after the CSA scores."""
         import torch
-        with torch.cuda.stream(stream):
-            self.h_out[g].copy_(self.d_out[g], non_blocking=True)
+        st = self.steps[p]
+        with torch.cuda.stream(s_hca):
+            for n in self.RING["hca"]:
+                st.x[n][:, self.slot].copy_(self.staged[p][n])
+        with torch.cuda.stream(s_csa):
+            for n in self.RING["csa"]:
+                st.x[n][:, self.slot].copy_(self.staged[p][n])
+        if self.fused:
+            st.csa_fused(s_csa)
+            st.hca(s_hca)
+        else:
+            st.compress_csa(s_csa)
+            scored = torch.cuda.Event()
+            st.index_topk_split(s_csa, scored)
+            st.attend_csa(s_csa)
+            s_hca.wait_event(scored)
+            st.hca(s_hca)
+
+    def record(self, s_csa, s_hca, s_cp, s_out):
+        """Two consecutive steps (see the class description)."""
+        import torch
+        cur = torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(cur)
+        for s_ in (s_csa, s_hca, s_cp, s_out):
+            s_.wait_event(start)
+        with torch.cuda.stream(s_cp):          # step 1's inputs while step 0 runs
+            self.d_in[1].copy_(self.h_in[1], non_blocking=True)
+        in1 = torch.cuda.Event()
+        in1.record(s_cp)
+        self._compute(0, s_csa, s_hca)
+        done0 = torch.cuda.Event()
+        d_csa, d_hca = torch.cuda.Event(), torch.cuda.Event()
+        d_csa.record(s_csa)
+        d_hca.record(s_hca)
+        s_out.wait_event(d_csa)
+        s_out.wait_event(d_hca)
+        done0.record(s_out)
+        with torch.cuda.stream(s_out):         # step 0's outputs while step 1 runs
+            self.h_out[0].copy_(self.d_out[0], non_blocking=True)
+        s_cp.wait_event(done0)
+        with torch.cuda.stream(s_cp):          # step 0's slot refilled for the next pair
+            self.d_in[0].copy_(self.h_in[0], non_blocking=True)
+        for s_ in (s_csa, s_hca):
+            s_.wait_event(in1)
+            s_.wait_event(done0)
+        self._compute(1, s_csa, s_hca)
+        e1, e2 = torch.cuda.Event(), torch.cuda.Event()
+        e1.record(s_csa)
+        e2.record(s_hca)
+        s_out.wait_event(e1)
+        s_out.wait_event(e2)
+        with torch.cuda.stream(s_out):
+            self.h_out[1].copy_(self.d_out[1], non_blocking=True)
+        j1, j2 = torch.cuda.Event(), torch.cuda.Event()
+        j1.record(s_out)
+        j2.record(s_cp)
+        cur.wait_event(j1)
+        cur.wait_event(j2)
 
 
 def cpu_baseline(w, x, seqs: int) -> dict:
@@ -535,7 +595,7 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
 
     x = synth.make_inputs(w)
     step = step_from(w, x, o_dtype="bf16")
-    io = StepIO(step, x, w)         # packs per-step inputs and outputs (before capture)
+    cudart = load_cudart()
     s_csa, s_hca = torch.cuda.Stream(), torch.cuda.Stream()
     # auto: the fused CSA layer (one cluster of CTAs per sequence) where the
     # batch fills most of the GPU with clusters (measured: 100 vs 108 us a
@@ -552,7 +612,7 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
         run_step(s_csa, s_hca)
     # the step's kernel launches: the captured graph's kernel nodes (the step
     # issues only library calls and event edges, so every kernel node is ours)
-    kernels = graph_kernels(g.raw_cuda_graph(), io.cudart)
+    kernels = graph_kernels(g.raw_cuda_graph(), cudart)
     g.instantiate()
     torch.cuda.synchronize()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
@@ -629,49 +689,31 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
         score_kernel, FUSED_SOURCES if fused else MX_SOURCES if mx else SCORE_SOURCES, k_bytes)
     step_gbs = ab["step"] / (total_ms / steps / 1e3) / 1e9
 
-    # ---- end to end: host (pinned) inputs of the new token in, outputs out
+    # ---- end to end: each step's inputs from pinned host memory, its
+    # outputs back to pinned host memory, two steps per graph, double-buffered
     e2e_out = None
     if e2e:
-        def e2e_body():
-            # each layer: its inputs in, its kernels, its outputs out, on its own
-            # stream; the CSA layer also waits for the positions (HCA's copy).
-            # HCA starts at once here: its readback then overlaps the CSA chain
-            cur = torch.cuda.current_stream()
-            fork = torch.cuda.Event()
-            fork.record(cur)
-            s_csa.wait_event(fork)
-            s_hca.wait_event(fork)
-            io.h2d("hca", s_hca)
-            pos_in = torch.cuda.Event()
-            pos_in.record(s_hca)
-            step.hca(s_hca)
-            io.d2h("hca", s_hca)
-            io.h2d("csa", s_csa)
-            s_csa.wait_event(pos_in)
-            if fused:
-                step.csa_fused(s_csa)
-            else:
-                step.csa(s_csa)
-            io.d2h("csa", s_csa)
-            e1, e2 = torch.cuda.Event(), torch.cuda.Event()
-            e1.record(s_csa)
-            e2.record(s_hca)
-            cur.wait_event(e1)
-            cur.wait_event(e2)
-        e2e_body()
+        pio = PipelinedIO(w, x, fused)
+        s_cp, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        for _ in range(2):
+            pio.record(s_csa, s_hca, s_cp, s_out)
         torch.cuda.synchronize()
         g_e2e = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_e2e, stream=cap):
-            e2e_body()
+            pio.record(s_csa, s_hca, s_cp, s_out)
         for _ in range(3):
             g_e2e.replay()
-        e_ms = timed(g_e2e.replay, steps)
+        e_ms = timed(g_e2e.replay, max(1, steps // 2))
         e_total = max_over_ranks(sum(e_ms), device="cuda")
-        e2e_out = {"value": world * w.B * w.T * steps / (e_total / 1e3), "unit": UNIT,
-                   "h2d_bytes_per_step": io.h2d_bytes, "d2h_bytes_per_step": io.d2h_bytes,
-                   "copies_per_step": io.copies,
-                   "note": "one graph per step: each layer's copies on its own stream; O read "
-                           "back in bf16"}
+        n_steps = 2 * max(1, steps // 2)
+        e2e_out = {"value": world * w.B * w.T * n_steps / (e_total / 1e3), "unit": UNIT,
+                   "h2d_bytes_per_step": pio.h2d_bytes, "d2h_bytes_per_step": pio.d2h_bytes,
+                   "copies_per_step": pio.copies, "steps": n_steps,
+                   "note": "pinned host buffers; each step one copy of its inputs in (q, q_hca, "
+                           "q_idx, w, positions, the new ring rows) and one of its outputs (O in "
+                           "bf16, LSE) out; double-buffered: a step's inputs arrive while the "
+                           "step before it runs, its outputs leave while the next one runs"}
+        del pio
     out = {
         "value": value, "ms_per_step": total_ms / steps,
         "config": {"workload": w.name, "batch": w.B, "context": w.L, "heads": w.H,
