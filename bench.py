@@ -54,6 +54,10 @@ FUSED_SOURCES = ["sparse_attention_27_b300/csrc/decode_fused.cu",
                  "sparse_attention_27_b300/csrc/common.cuh", "sparse_attention_27_b300/csrc/kernels.cuh",
                  "sparse_attention_27_b300/csrc/topk_dev.cuh",
                  "sparse_attention_27_b300/csrc/compress_dev.cuh"]
+STEP_SOURCES = ["sparse_attention_27_b300/csrc/decode_step.cu",
+                "sparse_attention_27_b300/csrc/common.cuh", "sparse_attention_27_b300/csrc/kernels.cuh",
+                "sparse_attention_27_b300/csrc/topk_dev.cuh",
+                "sparse_attention_27_b300/csrc/compress_dev.cuh"]
 MX_SOURCES = ["sparse_attention_27_b300/csrc/score_mx.cu", "sparse_attention_27_b300/csrc/common.cuh",
               "sparse_attention_27_b300/csrc/kernels.cuh", "sparse_attention_27_b300/csrc/score_jobs.cuh"]
 
@@ -400,11 +404,11 @@ class PipelinedIO:
     RING = {"csa": ["k_raw", "v_raw", "ik_raw", "z"], "hca": ["hk_raw", "hv_raw", "hz"]}
     OUT = ["o", "lse", "ho", "hlse"]
 
-    def __init__(self, w, x, fused: bool):
+    def __init__(self, w, x, mode: str):
         import numpy as np
         import torch
         from sparse_attention_27_b300.path import HybridStep, step_from
-        self.fused = fused
+        self.mode = mode
         base = step_from(w, x, o_dtype="bf16")
         dev = base.o.device
         slot = (w.L - 1) % w.ring
@@ -454,17 +458,24 @@ class PipelinedIO:
         return buf, views
 
     def _compute(self, p, s_csa, s_hca):
-        """Step p on the two layer streams, scheduled as in the device-timed
-        step: fused, both layers at once; split, HCA after the CSA scores."""
+        """Step p on the layer streams, scheduled as in the device-timed step:
+        step, one sa_decode_step launch; fused, both layers at once; split,
+        HCA after the CSA scores."""
         import torch
         st = self.steps[p]
+        if self.mode == "step":
+            with torch.cuda.stream(s_csa):
+                for n in self.RING["csa"] + self.RING["hca"]:
+                    st.x[n][:, self.slot].copy_(self.staged[p][n])
+            st.decode_step(s_csa)
+            return
         with torch.cuda.stream(s_hca):
             for n in self.RING["hca"]:
                 st.x[n][:, self.slot].copy_(self.staged[p][n])
         with torch.cuda.stream(s_csa):
             for n in self.RING["csa"]:
                 st.x[n][:, self.slot].copy_(self.staged[p][n])
-        if self.fused:
+        if self.mode == "fused":
             st.csa_fused(s_csa)
             st.hca(s_hca)
         else:
@@ -584,9 +595,12 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
     dominant kernel alone (the indexer scoring call as a one-node graph) and
     the step end to end (inputs from pinned host memory, outputs back).  L2 is
     flushed before every timed replay; every replay is timed with CUDA events
-    on the launching stream.  ``schedule``: "fused" runs the CSA layer as one
-    csa_decode launch, "split" as csa_compress, the indexer's score and top-k
-    calls and csa_attend; "auto" takes the fused one where csa_decode applies.
+    on the launching stream.  ``schedule``: "step" runs both layers as one
+    sa_decode_step launch; "fused" runs the CSA layer as one csa_decode launch
+    and the HCA layer on a second stream; "split" runs csa_compress, the
+    indexer's score and top-k calls and csa_attend, HCA on a second stream;
+    "auto" takes the fused one where csa_decode fills the GPU, else the split
+    one (the measured faster schedules).
     Returns the measurement as a dict."""
     import torch
     import synth
@@ -598,11 +612,20 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
     cudart = load_cudart()
     s_csa, s_hca = torch.cuda.Stream(), torch.cuda.Stream()
     # auto: the fused CSA layer (one cluster of CTAs per sequence) where the
-    # batch fills most of the GPU with clusters (measured: 100 vs 108 us a
-    # step at 128K, B = 32); with few sequences (1M, B = 4) the clusters leave
-    # most SMs idle and the separate calls are faster (86 vs 125 us)
-    fused = schedule == "fused" or (schedule == "auto" and step.fused_ok() and w.B >= 16)
-    run_step = step.run_fused_two_streams if fused else step.run_two_streams
+    # batch fills most of the GPU with clusters (measured at 128K, B = 32:
+    # 99.8 us a step, against 112.2 us for the separate calls and 121.7 us
+    # for the whole step in one sa_decode_step launch); with few sequences
+    # (1M, B = 4) the clusters leave most SMs idle and the separate calls are
+    # faster (86 vs 125 us)
+    if schedule == "auto":
+        mode = "fused" if step.fused_ok() and w.B >= 16 else "split"
+    else:
+        mode = schedule
+    fused = mode == "fused"
+    if mode == "step":
+        run_step = lambda s_csa, s_hca: step.decode_step()      # on the current stream
+    else:
+        run_step = step.run_fused_two_streams if fused else step.run_two_streams
     for _ in range(2):              # outside the graph: sets kernel attributes, loads modules
         run_step(s_csa, s_hca)
     torch.cuda.synchronize()
@@ -656,6 +679,9 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
     mx = w.indexer == "mxfp4"
 
     def score_only():
+        if mode == "step":
+            step.decode_step()
+            return
         if fused:
             step.csa_fused()
             return
@@ -679,21 +705,24 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
     k_avg = sum(k_ms) / len(k_ms)
     ab = algorithmic_bytes(w, o_bytes=2)
     peak, peak_kind = peaks()
-    k_bytes = ab["csa"] if fused else ab["index"]
+    k_bytes = ab["step"] if mode == "step" else ab["csa"] if fused else ab["index"]
     achieved = k_bytes / (k_avg / 1e3) / 1e9
-    score_kernel = ("csa_decode_kernel" if fused else
+    score_kernel = ("decode_step_kernel" if mode == "step" else
+                    "csa_decode_kernel" if fused else
                     "score_mx_kernel" if mx else "score_tc_kernel")
-    k_call = ("csa_decode, the whole CSA layer, one-node graph" if fused else
+    k_call = ("sa_decode_step, both layers, counter memset + kernel" if mode == "step" else
+              "csa_decode, the whole CSA layer, one-node graph" if fused else
               "csa_index_topk scores, k=0, one-node graph")
     traffic, traffic_note = recorded_traffic(
-        score_kernel, FUSED_SOURCES if fused else MX_SOURCES if mx else SCORE_SOURCES, k_bytes)
+        score_kernel, STEP_SOURCES if mode == "step" else FUSED_SOURCES if fused else
+        MX_SOURCES if mx else SCORE_SOURCES, k_bytes)
     step_gbs = ab["step"] / (total_ms / steps / 1e3) / 1e9
 
     # ---- end to end: each step's inputs from pinned host memory, its
     # outputs back to pinned host memory, two steps per graph, double-buffered
     e2e_out = None
     if e2e:
-        pio = PipelinedIO(w, x, fused)
+        pio = PipelinedIO(w, x, mode)
         s_cp, s_out = torch.cuda.Stream(), torch.cuda.Stream()
         for _ in range(2):
             pio.record(s_csa, s_hca, s_cp, s_out)
@@ -721,8 +750,10 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
                    "indexer_heads": w.HI, "indexer": w.indexer, "o_dtype": "bf16",
                    "parallelism": f"replicas x{world}",
                    "l2": "flushed before every timed step: a 512 MiB write, then a 256 MiB read",
-                   "schedule": "fused" if fused else "split",
-                   "graph": ("one CUDA graph per step, the CSA layer as one csa_decode launch "
+                   "schedule": mode,
+                   "graph": ("one CUDA graph per step: a counter memset and one "
+                             "sa_decode_step launch for both layers" if mode == "step" else
+                             "one CUDA graph per step, the CSA layer as one csa_decode launch "
                              "and the HCA layer on two streams, both from the start" if fused
                              else "one CUDA graph per step, CSA and HCA on two streams, HCA "
                                   "after the CSA scores")},
@@ -748,9 +779,10 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--schedule", default="auto", choices=["auto", "fused", "split"],
-                    help="the CSA layer as one csa_decode launch (fused), as its separate calls "
-                         "(split), or fused where csa_decode applies (auto)")
+    ap.add_argument("--schedule", default="auto", choices=["auto", "step", "fused", "split"],
+                    help="both layers as one sa_decode_step launch (step), the CSA layer as one "
+                         "csa_decode launch (fused) or as its separate calls (split); auto: "
+                         "fused where csa_decode fills the GPU, else split")
     ap.add_argument("--no-extra", action="store_true",
                     help="time only the headline workload (no 1M decode and 64K prefill objects)")
     ap.add_argument("--prefill-calls", action="store_true",

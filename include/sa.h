@@ -251,6 +251,51 @@ int csa_decode(int B, int H, int d, int HI, int dI, int m, int k, int W, float s
                float* lse, int32_t* err, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * sa_decode_step -- the whole decode step of both layers for one new token
+ * per sequence, in one launch ([P2] "압축 희소 어텐션(CSA)과 극압축 어텐션(HCA)";
+ * [P3] CSA steps 1-4, HCA and "KV Cache 관리"; [P1] IDEAS: the mega-kernel
+ * direction): what csa_compress, csa_index_topk, csa_attend and
+ * hca_compress_attend compute for the same inputs, in one persistent kernel
+ * whose CTAs take work items (pooling, 2048-entry score slices, a row's
+ * top-k, shares of a row's key list) from a queue, so that one sequence's
+ * top-k and attention run while others are still scored.  The cache rows
+ * written and idx are bit-identical to the separate calls'; o, lse, ho and
+ * hlse differ only by the fp32 rounding of a different split of the key
+ * list.  One query per sequence (T = 1) at position q_pos[b].
+ *  q, q_hca [B,H,128] bf16 (H <= 64): the CSA and the HCA layer's queries
+ *  q_idx [B,64,64] bf16; w [B,64] f32: indexer queries and head weights
+ *  k_raw, v_raw, hk_raw, hv_raw [B,R,128] bf16; ik_raw [B,R,64] bf16;
+ *  z, hz [B,R] f32: each layer's ring of raw rows and pooling logits
+ *  (R >= W, R >= m, R >= m2)
+ *  blk_lo, blk_hi / hblk_lo, hblk_hi [B] int32 device: the CSA / HCA blocks
+ *  this step closes; max_blocks / max_blocks2 host bounds on their lengths
+ *  k_c, v_c [B,N_cap,128], ik_c [B,N_cap,64]; hk_c, hv_c [B,N2_cap,128]
+ *  bf16: the caches (read; the closed blocks written); m, m2 <= 128;
+ *  N_cap <= 32768 (a row's scores fit one CTA's shared memory), else
+ *  SA_ERR_UNSUPPORTED -- longer rows take the separate calls or csa_decode
+ *  idx [B,k] int32; o, ho [B,H,128] in o_dtype (SA_F32 or SA_BF16);
+ *  lse, hlse [B,H] f32: outputs
+ *  ws: sa_decode_step_workspace_bytes(B, H, N_cap, k, W, N2_cap) bytes,
+ *  16-byte aligned, owned by the caller; the call zeroes its counters on
+ *  `stream` first, so calls sharing a workspace must not overlap.  Too
+ *  small -> SA_ERR_INVALID_ARG; 0 from the query means the shape is not
+ *  taken (SA_ERR_UNSUPPORTED).
+ * Device errors as the separate calls; a bounded wait that gives up raises
+ * SA_ERR_DEVICE_TIMEOUT and every CTA stops taking work.
+ */
+size_t sa_decode_step_workspace_bytes(int B, int H, int N_cap, int k, int W, int N2_cap);
+int sa_decode_step(int B, int H, int d, int HI, int dI, int m, int k, int W, int m2,
+                   float sm_scale, const void* q, const void* q_idx, const float* w,
+                   const void* q_hca, const int32_t* q_pos, const void* k_raw, const void* v_raw,
+                   const void* ik_raw, const float* z, const void* hk_raw, const void* hv_raw,
+                   const float* hz, int R, const int32_t* blk_lo, const int32_t* blk_hi,
+                   int max_blocks, const int32_t* hblk_lo, const int32_t* hblk_hi,
+                   int max_blocks2, void* k_c, void* v_c, void* ik_c, int N_cap, void* hk_c,
+                   void* hv_c, int N2_cap, int32_t* idx, int o_dtype, void* o, float* lse,
+                   void* ho, float* hlse, void* ws, size_t ws_bytes, int32_t* err,
+                   void* stream);
+
+/* ---------------------------------------------------------------------------
  * Backward pass.  The top-k selection is not differentiable ([P1] IDEAS), so
  * it is a constant mask: the gradient of a loss with dL/dO given reaches the
  * queries, the attended cache rows and window rows, and -- through the

@@ -28,7 +28,7 @@ EXPORTS = (
     "csa_attend", "csa_attend_workspace_bytes", "hca_compress_attend",
     "hca_compress_attend_workspace_bytes", "attn_merge", "csa_index_topk_noalloc",
     "sa_mxfp4_quantize", "csa_decode", "csa_attend_backward", "hca_attend_backward",
-    "sa_compress_backward",
+    "sa_compress_backward", "sa_decode_step", "sa_decode_step_workspace_bytes",
 )
 
 
@@ -65,6 +65,11 @@ _lib.sa_compress_backward.argtypes = [_i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _v
 _lib.csa_decode.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                             _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp,
                             _vp]
+_lib.sa_decode_step.argtypes = ([_i] * 9 + [_f] + [_vp] * 12 + [_i] + [_vp] * 2 + [_i] +
+                                 [_vp] * 2 + [_i] + [_vp] * 3 + [_i] + [_vp] * 2 + [_i] +
+                                 [_vp, _i] + [_vp] * 5 + [_sz, _vp, _vp])
+_lib.sa_decode_step_workspace_bytes.argtypes = [_i] * 6
+_lib.sa_decode_step_workspace_bytes.restype = _sz
 _lib.csa_attend.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _i, _vp, _vp,
                             _vp, _i, _vp, _i, _vp, _vp, _sz, _vp, _vp]
 _lib.csa_attend_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
@@ -185,6 +190,30 @@ def csa_decode(B, H, d, HI, dI, m, k, W, sm_scale, q, q_idx, w, q_pos, k_raw, v_
                            _p(q_pos), _p(k_raw), _p(v_raw), _p(ik_raw), _p(z), R, _p(blk_lo),
                            _p(blk_hi), max_blocks, _p(k_c), _p(v_c), _p(ik_c), N_cap, _p(idx),
                            _p(o), _out_code(o), _p(lse), _p(err), _stream(stream)), "csa_decode")
+
+
+def sa_decode_step_workspace_bytes(B, H, N_cap, k, W, N2_cap) -> int:
+    """Workspace bytes of sa_decode_step (0: the shape is not taken)."""
+    return int(_lib.sa_decode_step_workspace_bytes(B, H, N_cap, k, W, N2_cap))
+
+
+def sa_decode_step(B, H, d, HI, dI, m, k, W, m2, sm_scale, q, q_idx, w, q_hca, q_pos, k_raw,
+                   v_raw, ik_raw, z, hk_raw, hv_raw, hz, R, blk_lo, blk_hi, max_blocks, hblk_lo,
+                   hblk_hi, max_blocks2, k_c, v_c, ik_c, N_cap, hk_c, hv_c, N2_cap, idx, o, lse,
+                   ho, hlse, ws, ws_bytes=None, err=None, stream=None):
+    """Both layers of one decode step in one launch; o and ho: f32 or bf16
+    tensors [B,H,d] of the same dtype (it selects the output type)."""
+    if _out_code(o) != _out_code(ho):
+        raise SaError(SA_ERR_INVALID_ARG, "sa_decode_step")
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(_lib.sa_decode_step(B, H, d, HI, dI, m, k, W, m2, sm_scale, _p(q), _p(q_idx), _p(w),
+                               _p(q_hca), _p(q_pos), _p(k_raw), _p(v_raw), _p(ik_raw), _p(z),
+                               _p(hk_raw), _p(hv_raw), _p(hz), R, _p(blk_lo), _p(blk_hi),
+                               max_blocks, _p(hblk_lo), _p(hblk_hi), max_blocks2, _p(k_c),
+                               _p(v_c), _p(ik_c), N_cap, _p(hk_c), _p(hv_c), N2_cap, _p(idx),
+                               _out_code(o), _p(o), _p(lse), _p(ho), _p(hlse), _p(ws), ws_bytes,
+                               _p(err), _stream(stream)), "sa_decode_step")
 
 
 def csa_attend_backward(dtype, B, T, H, d, m, k, W, sm_scale, q, q_pos, k_c, v_c, N_cap, idx,

@@ -304,6 +304,84 @@ int csa_decode(int B, int H, int d, int HI, int dI, int m, int k, int W, float s
 }
 
 namespace {
+// Workspace of sa_decode_step: counters, histograms and row info (zeroed by
+// each call) | score keys [B, N_cap] | CSA partials | HCA partials | top-k
+// candidate lists, each part 256-byte aligned.  Returns false when the step
+// kernel does not take the shape.
+bool step_layout(StepArgs& a, size_t* offs /* [7] */, size_t* total) {
+  if (!decode_step_plan(a, device_sms())) return false;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  size_t o = 0;
+  offs[0] = o; o += up(decode_step_counter_bytes(a.B));
+  offs[1] = o; o += up(4 * (size_t)a.B * ((a.N_cap + 3) / 4 * 4));
+  offs[2] = o; o += up(4 * (size_t)a.B * a.na * 64 * 128);
+  offs[3] = o; o += up(4 * (size_t)a.B * a.na * 64);
+  offs[4] = o; o += up(4 * (size_t)a.B * a.nh * 64 * 128);
+  offs[5] = o; o += up(4 * (size_t)a.B * a.nh * 64);
+  offs[6] = o; o += up(4 * (size_t)a.B * 4 * 4096);
+  *total = o;
+  return true;
+}
+}  // namespace
+
+size_t sa_decode_step_workspace_bytes(int B, int H, int N_cap, int k, int W, int N2_cap) {
+  if (B < 1 || H < 1 || N_cap < 0 || k < 0 || W < 0 || N2_cap < 0) return 0;
+  StepArgs a{};
+  a.B = B; a.H = H; a.N_cap = N_cap; a.k = k; a.W = W; a.N2_cap = N2_cap; a.m = 1; a.m2 = 1;
+  size_t offs[7], total = 0;
+  return step_layout(a, offs, &total) ? total : 0;
+}
+
+int sa_decode_step(int B, int H, int d, int HI, int dI, int m, int k, int W, int m2,
+                   float sm_scale, const void* q, const void* q_idx, const float* w,
+                   const void* q_hca, const int32_t* q_pos, const void* k_raw, const void* v_raw,
+                   const void* ik_raw, const float* z, const void* hk_raw, const void* hv_raw,
+                   const float* hz, int R, const int32_t* blk_lo, const int32_t* blk_hi,
+                   int max_blocks, const int32_t* hblk_lo, const int32_t* hblk_hi,
+                   int max_blocks2, void* k_c, void* v_c, void* ik_c, int N_cap, void* hk_c,
+                   void* hv_c, int N2_cap, int32_t* idx, int o_dtype, void* o, float* lse,
+                   void* ho, float* hlse, void* ws, size_t ws_bytes, int32_t* err,
+                   void* stream) {
+  if (B < 0 || H < 1 || m < 1 || m2 < 1 || k < 0 || W < 0 || R < 1 || R < W || R < m ||
+      R < m2 || N_cap < 0 || N2_cap < 0 || max_blocks < 0 || max_blocks2 < 0 ||
+      !plain_dtype(o_dtype))
+    return SA_ERR_INVALID_ARG;
+  if (d != 128 || HI != 64 || dI != 64 || H > 64 || m > 128 || m2 > 128)
+    return SA_ERR_UNSUPPORTED;
+  if (!q || !q_idx || !w || !q_hca || !q_pos || !k_raw || !v_raw || !ik_raw || !z || !hk_raw ||
+      !hv_raw || !hz || !blk_lo || !blk_hi || !hblk_lo || !hblk_hi || !k_c || !v_c || !ik_c ||
+      !hk_c || !hv_c || !o || !lse || !ho || !hlse || (k > 0 && !idx))
+    return SA_ERR_INVALID_ARG;
+  if (!al16(q) || !al16(q_idx) || !al16(w) || !al16(q_hca) || !al16(k_raw) || !al16(v_raw) ||
+      !al16(ik_raw) || !al16(hk_raw) || !al16(hv_raw) || !al16(k_c) || !al16(v_c) ||
+      !al16(ik_c) || !al16(hk_c) || !al16(hv_c) || !al16(o) || !al16(ho) || !al16(ws))
+    return SA_ERR_INVALID_ARG;
+  if (B == 0) return SA_OK;
+  StepArgs a{};
+  a.B = B; a.H = H; a.m = m; a.k = k; a.W = W; a.m2 = m2; a.sm_scale = sm_scale;
+  a.q = q; a.q_idx = q_idx; a.w = w; a.q_hca = q_hca; a.q_pos = q_pos;
+  a.k_raw = k_raw; a.v_raw = v_raw; a.ik_raw = ik_raw; a.z = z;
+  a.hk_raw = hk_raw; a.hv_raw = hv_raw; a.hz = hz; a.R = R;
+  a.blk_lo = blk_lo; a.blk_hi = blk_hi; a.max_blocks = max_blocks;
+  a.hblk_lo = hblk_lo; a.hblk_hi = hblk_hi; a.max_blocks2 = max_blocks2;
+  a.k_c = k_c; a.v_c = v_c; a.ik_c = ik_c; a.N_cap = N_cap;
+  a.hk_c = hk_c; a.hv_c = hv_c; a.N2_cap = N2_cap;
+  a.idx = idx; a.o_dtype = o_dtype; a.o = o; a.lse = lse; a.ho = ho; a.hlse = hlse; a.err = err;
+  size_t offs[7], total = 0;
+  if (!step_layout(a, offs, &total)) return SA_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < total) return SA_ERR_INVALID_ARG;
+  char* base = static_cast<char*>(ws);
+  a.ctr = reinterpret_cast<int*>(base + offs[0]);
+  a.keys = reinterpret_cast<uint32_t*>(base + offs[1]);
+  a.part_o = reinterpret_cast<float*>(base + offs[2]);
+  a.part_lse = reinterpret_cast<float*>(base + offs[3]);
+  a.hpart_o = reinterpret_cast<float*>(base + offs[4]);
+  a.hpart_lse = reinterpret_cast<float*>(base + offs[5]);
+  a.tk_cand = reinterpret_cast<uint32_t*>(base + offs[6]);
+  return status_of(launch_decode_step(a, static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
 // Shared checks and launch of the two attention backward calls.
 int attention_backward(AttnBwdArgs& a, int64_t n_keys_max, cudaStream_t st) {
   if (!plain_dtype(a.dtype) || a.B < 0 || a.T < 0 || a.H <= 0 || a.d <= 0 || a.d > 256 ||

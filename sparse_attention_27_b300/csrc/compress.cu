@@ -108,7 +108,8 @@ __global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressArgs
     const char* src; char* dst; int width, off;
     chunk_of(c, src, dst, width, off);
     float acc[kVec];
-    pool_partial<DT>(src, (int64_t)width * S::kBytes, off * S::kBytes, p0, m, R, s_w, g, RG, acc);
+    pool_partial<DT, 8>(src, (int64_t)width * S::kBytes, off * S::kBytes, p0, m, R, s_w, g, RG,
+                          acc);
 #pragma unroll
     for (int e = 0; e < kVec; ++e) s_part[(g * nchunks + c) * kVec + e] = acc[e];
   }

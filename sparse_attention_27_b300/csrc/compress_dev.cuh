@@ -30,10 +30,23 @@ __device__ __forceinline__ void pool_weights_warp(const float* z_b, int64_t p0, 
                                                   float* w) {
   const int lane = threadIdx.x & 31;
   float mu = -INFINITY;
-  for (int i = lane; i < m; i += 32) {
-    const float zi = __ldg(z_b + (p0 + i) % R);
-    w[i] = zi;
-    mu = fmaxf(mu, zi);
+  // a lane's logits are loaded four at a time (one memory round trip for
+  // blocks of up to 128 rows), then kept and maxed in order
+  for (int i0 = lane; i0 < m; i0 += 4 * 32) {
+    float zi[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + 32 * u;
+      zi[u] = i < m ? __ldg(z_b + (p0 + i) % R) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + 32 * u;
+      if (i < m) {
+        w[i] = zi[u];
+        mu = fmaxf(mu, zi[u]);
+      }
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, o));
@@ -58,22 +71,44 @@ __device__ __forceinline__ void load_chunk(const char* p, float* f) {
   }
 }
 
-// Partial g (of RG) of one 16-byte output chunk: rows i = g, g+RG, ... < m of
-// the raw array `base` (one sequence, rows of `row_bytes`, chunk at byte
-// `off`), block start p0, ring of R rows.
-template <int DT>
+// Partial g (of RG) of one 16-byte output chunk, rows i = g, g+RG, ... < m,
+// with load(i, f) giving row i's chunk as floats.  kBatch rows' loads are
+// issued before their multiply-adds (which stay in increasing i), so that
+// many memory latencies overlap instead of adding up; the result does not
+// depend on it.
+template <int kVec, int kBatch, class Load>
+__device__ __forceinline__ void pool_partial_by(Load load, int m, const float* w, int g, int RG,
+                                                float* acc) {
+#pragma unroll
+  for (int e = 0; e < kVec; ++e) acc[e] = 0.f;
+  for (int i0 = g; i0 < m; i0 += kBatch * RG) {
+    float f[kBatch][kVec];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = i0 + u * RG;
+      if (i < m) load(i, f[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = i0 + u * RG;
+      if (i < m) {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) acc[e] = fmaf(w[i], f[u][e], acc[e]);
+      }
+    }
+  }
+}
+
+// pool_partial_by over the raw array `base` in global memory (one sequence,
+// rows of `row_bytes`, chunk at byte `off`), block start p0, ring of R rows.
+template <int DT, int kBatch = 1>
 __device__ __forceinline__ void pool_partial(const char* base, int64_t row_bytes, int off,
                                              int64_t p0, int m, int R, const float* w, int g,
                                              int RG, float* acc) {
   constexpr int kVec = 16 / Store<DT>::kBytes;
-#pragma unroll
-  for (int e = 0; e < kVec; ++e) acc[e] = 0.f;
-  for (int i = g; i < m; i += RG) {
-    float f[kVec];
-    load_chunk<DT>(base + ((p0 + i) % R) * row_bytes + off, f);
-#pragma unroll
-    for (int e = 0; e < kVec; ++e) acc[e] = fmaf(w[i], f[e], acc[e]);
-  }
+  pool_partial_by<kVec, kBatch>(
+      [&](int i, float* f) { load_chunk<DT>(base + ((p0 + i) % R) * row_bytes + off, f); }, m, w,
+      g, RG, acc);
 }
 
 // Store one pooled 16-byte chunk (fp32 values) in the storage type.

@@ -90,10 +90,11 @@ struct Ctl {
   uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2];
   uint32_t tmem;
   int abort;
-  float w[kHI];                                // indexer head weights of the row
+  __align__(16) float w[kHI];                  // indexer head weights of the row
   float pw[kMaxPool];                          // pooling weights of one block
   float lse[kHeads];                           // this CTA's partial LSE
 };
+static_assert(offsetof(Ctl, w) % 16 == 0, "the epilogue reads w as float4");
 
 struct TMaps {
   CUtensorMap ik;                              // [B*N_cap, 64] bf16, box 64 x 256
@@ -159,7 +160,7 @@ __device__ __forceinline__ int pool_owner(const RowPlan& P, int64_t j, int C) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     csa_decode_kernel(const __grid_constant__ TMaps tm, FusedDecodeArgs a) {
-  extern __shared__ unsigned char smem_raw[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
   Ctl& C = *reinterpret_cast<Ctl*>(smem_raw);
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + sizeof(Ctl) + 1023) & ~uintptr_t(1023));

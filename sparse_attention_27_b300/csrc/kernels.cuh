@@ -130,6 +130,64 @@ struct FusedDecodeArgs {
 bool fused_decode_plan(FusedDecodeArgs& a, int num_sms);
 cudaError_t launch_fused_decode(const FusedDecodeArgs& a, cudaStream_t st);
 
+// Whole hybrid decode step (sa_decode_step): both layers of one decode token
+// per sequence in one persistent launch over a queue of work items.  All
+// tensors bf16 unless stated.
+constexpr int kStepMaxTilesPerPart = 32;   // key tiles per attention share at most
+struct StepArgs {
+  int B, H, m, k, W, m2;
+  float sm_scale;
+  const void* q;        // [B, H, 128] CSA queries
+  const void* q_idx;    // [B, 64, 64]
+  const float* w;       // [B, 64] f32
+  const void* q_hca;    // [B, H, 128] HCA queries
+  const int32_t* q_pos; // [B]
+  const void* k_raw;    // [B, R, 128]
+  const void* v_raw;
+  const void* ik_raw;   // [B, R, 64]
+  const float* z;       // [B, R] f32
+  const void* hk_raw;   // [B, R, 128]
+  const void* hv_raw;
+  const float* hz;      // [B, R] f32
+  int R;
+  const int32_t* blk_lo;
+  const int32_t* blk_hi;
+  int max_blocks;
+  const int32_t* hblk_lo;
+  const int32_t* hblk_hi;
+  int max_blocks2;
+  void* k_c;            // [B, N_cap, 128]
+  void* v_c;
+  void* ik_c;           // [B, N_cap, 64]
+  int N_cap;
+  void* hk_c;           // [B, N2_cap, 128]
+  void* hv_c;
+  int N2_cap;
+  int32_t* idx;         // [B, k]
+  int o_dtype;
+  void* o;              // [B, H, 128] in o_dtype
+  float* lse;           // [B, H]
+  void* ho;
+  float* hlse;
+  int32_t* err;
+  // workspace (laid out by the caller)
+  int* ctr;             // counters, zeroed by the launch (decode_step_counter_bytes)
+  uint32_t* keys;       // [B, N_cap] score keys
+  float* part_o;        // [B, na, 64, 128] CSA partials
+  float* part_lse;      // [B, na, 64]
+  float* hpart_o;       // [B, nh, 64, 128] HCA partials
+  float* hpart_lse;     // [B, nh, 64]
+  uint32_t* tk_cand;    // [B, 4, 4096] top-k candidate lists
+  // plan (decode_step_plan)
+  int tps, ns;          // score tiles per item, score items per sequence
+  int tpa, na;          // CSA key tiles per share, shares per sequence
+  int tph, nh;          // HCA
+  int grid;
+};
+bool decode_step_plan(StepArgs& a, int num_sms);
+size_t decode_step_counter_bytes(int B);
+cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t st);
+
 // Backward of the attention branches (the key list as in AttnArgs, fixed)
 // and of the block pooling; every gradient is added (fp32 atomics) into the
 // caller's buffers.

@@ -27,6 +27,8 @@
 //  C. emission in index order: out[#(> T) before i + min(#(== T) before i, take)],
 //     the counts of lower-ranked CTAs included.
 #pragma once
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace sa {
@@ -53,7 +55,8 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   return m;
 }
 
-constexpr int kKplMax = 32;                                // keys per thread, at most
+constexpr int kKplMax = 32;                                // keys per thread of the top-k kernels
+                                                           // (topk_select itself takes up to 64)
 constexpr int kTopkSmemBytes = (sizeof(TopkSmem) + 15) & ~15;
 constexpr int kFineShift = 19;                             // bin = key >> 19
 constexpr int kFineBins = 1 << (32 - kFineShift);          // 8192
@@ -228,6 +231,59 @@ __device__ __forceinline__ void find_bin_cluster(const int* h, const int* gsum, 
   __syncthreads();
 }
 
+// find_bin over one CTA's own 8192-bin histogram h (shared memory) in two
+// steps: the 64 group sums of 128 bins (each warp sums whole groups with
+// 16-byte loads), then one warp finds the group holding the krem-th largest
+// key and the bin inside it.  S.sel_bin, S.above as find_bin; synchronises
+// the CTA.
+template <int NT>
+__device__ void find_bin_groups(const int* h, int krem, TopkSmem& S) {
+  constexpr int NW = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  for (int g = w; g < 64; g += NW) {
+    const int4 v = reinterpret_cast<const int4*>(h + g * 128)[lane];
+    int s = v.x + v.y + v.z + v.w;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) S.gsum[g] = s;
+  }
+  __syncthreads();
+  if (w == 0) {
+    const int g0 = S.gsum[63 - 2 * lane], g1 = S.gsum[62 - 2 * lane];   // descending groups
+    int x = g0 + g1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    const int base = x - g0 - g1;
+    int G = -1, aboveG = 0;
+    if (base < krem && base + g0 >= krem) { G = 63 - 2 * lane; aboveG = base; }
+    else if (base + g0 < krem && base + g0 + g1 >= krem) { G = 62 - 2 * lane; aboveG = base + g0; }
+    const int src = __ffs(__ballot_sync(0xffffffffu, G >= 0)) - 1;
+    G = __shfl_sync(0xffffffffu, G, src);
+    aboveG = __shfl_sync(0xffffffffu, aboveG, src);
+    // bins G*128 + 127 - 4l - q (q < 4): one 16-byte load per lane
+    const int4 v = *reinterpret_cast<const int4*>(h + G * 128 + 124 - 4 * lane);
+    const int c4[4] = {v.w, v.z, v.y, v.x};
+    const int s2 = c4[0] + c4[1] + c4[2] + c4[3];
+    int x2 = s2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x2, o);
+      if (lane >= o) x2 += y;
+    }
+    int b2 = aboveG + x2 - s2, bin = -1, above = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (bin < 0 && b2 < krem && b2 + c4[q] >= krem) { bin = G * 128 + 127 - 4 * lane - q; above = b2; }
+      b2 += c4[q];
+    }
+    if (bin >= 0) { S.sel_bin = bin; S.above = above; }
+  }
+  __syncthreads();
+}
+
 // The kk-th largest of those keys[0..m) whose top `top` bits equal prefix0's
 // (1 <= kk <= their count over the cluster), by radix passes of up to 11 bits
 // over the bits below, the per-pass histograms summed over the cluster's C
@@ -312,7 +368,8 @@ __device__ void topk_select(TopkSmem& S, const uint32_t* keys, int cnt, int lo, 
   const uint32_t* wkeys = keys + w * 32 * KPL + lane;   // this lane's keys, stride 32
   const int i0 = w * 32 * KPL + lane;
   int above_w = 0, in_w = 0;
-  uint32_t mine = 0;                             // bit j: this lane's slot j is in bin sel
+  using Mask = typename std::conditional<(KPL > 32), uint64_t, uint32_t>::type;
+  Mask mine = 0;                                 // bit j: this lane's slot j is in bin sel
 #pragma unroll 4
   for (int j = 0; j < KPL; ++j) {
     const uint32_t key = wkeys[32 * j];
@@ -320,7 +377,7 @@ __device__ void topk_select(TopkSmem& S, const uint32_t* keys, int cnt, int lo, 
     above_w += __popc(__ballot_sync(0xffffffffu, hb > sel));
     const bool in = key != 0u && hb == sel;
     in_w += __popc(__ballot_sync(0xffffffffu, in));
-    mine |= (uint32_t)in << j;
+    mine |= (Mask)in << j;
   }
   if (lane == 0) { S.wg[w] = above_w; S.we[w] = 0; S.wc[w] = in_w; }
   __syncthreads();
@@ -336,7 +393,7 @@ __device__ void topk_select(TopkSmem& S, const uint32_t* keys, int cnt, int lo, 
   const int a_mine = __shfl_sync(0xffffffffu, aw, 31);
   if (tid == 0) { S.cnt[0] = a_mine; S.cnt[1] = c_mine; }
   int pos = w > 0 ? __shfl_sync(0xffffffffu, cw, w - 1) : 0;
-  for (int j = 0; j < KPL && __any_sync(0xffffffffu, mine >> j); ++j) {
+  for (int j = 0; j < KPL && __any_sync(0xffffffffu, (mine >> j) != 0); ++j) {
     const bool in = (mine >> j) & 1u;
     const unsigned b = __ballot_sync(0xffffffffu, in);
     const int at = pos + __popc(b & lt);

@@ -36,7 +36,8 @@ import torch
 from . import (SA_BF16, SA_F32, SA_MXFP4, csa_attend, csa_attend_backward,
                csa_attend_workspace_bytes, csa_compress, csa_decode, csa_index_topk,
                csa_index_topk_workspace_bytes, hca_attend_backward, hca_compress_attend,
-               hca_compress_attend_workspace_bytes, sa_compress_backward, sa_mxfp4_quantize)
+               hca_compress_attend_workspace_bytes, sa_compress_backward, sa_decode_step,
+               sa_decode_step_workspace_bytes, sa_mxfp4_quantize)
 
 _CODES = {"f32": SA_F32, "bf16": SA_BF16, "mxfp4": SA_MXFP4}
 
@@ -85,6 +86,7 @@ class HybridStep:
         self.ws_b = torch.empty(max(self.ws_attend, 256), dtype=torch.uint8, device=dev)
         self.ws_c = torch.empty(max(self.ws_hca, 256), dtype=torch.uint8, device=dev)
         self.scores = None
+        self.ws_step = None
         if D.indexer == "mxfp4":
             self.q_codes = torch.empty((D.B, D.T, D.HI, D.dI // 2), dtype=torch.uint8, device=dev)
             self.q_scales = torch.empty((D.B, D.T, D.HI, D.dI // 32), dtype=torch.uint8,
@@ -164,6 +166,27 @@ class HybridStep:
                    x["w_idx"], x["q_pos"], x["k_raw"], x["v_raw"], x["ik_raw"], x["z"], D.R,
                    x["blk_lo"], x["blk_hi"], D.max_blocks, x["k_c"], x["v_c"], x["ik_c"], D.ncap,
                    self.idx, self.o, self.lse, err=self.err, stream=stream)
+
+    def step_ok(self) -> bool:
+        """Whether sa_decode_step takes this pass: csa_decode's shapes, rows
+        of at most 32768 compressed entries, blocks of at most 128 rows."""
+        D = self.D
+        return (self.fused_ok() and D.m <= 128 and D.m2 <= 128 and
+                sa_decode_step_workspace_bytes(D.B, D.H, D.ncap, D.k, D.W, D.ncap2) > 0)
+
+    def decode_step(self, stream=None):
+        """Both layers of the pass in one launch (sa_decode_step)."""
+        D, x = self.D, self.x
+        if self.ws_step is None:
+            n = sa_decode_step_workspace_bytes(D.B, D.H, D.ncap, D.k, D.W, D.ncap2)
+            self.ws_step = torch.empty(max(n, 256), dtype=torch.uint8, device=self.o.device)
+        sa_decode_step(D.B, D.H, D.d, D.HI, D.dI, D.m, D.k, D.W, D.m2, D.sm_scale, x["q"],
+                       x["q_idx"], x["w_idx"], x["q_hca"], x["q_pos"], x["k_raw"], x["v_raw"],
+                       x["ik_raw"], x["z"], x["hk_raw"], x["hv_raw"], x["hz"], D.R, x["blk_lo"],
+                       x["blk_hi"], D.max_blocks, x["hblk_lo"], x["hblk_hi"], D.max_blocks2,
+                       x["k_c"], x["v_c"], x["ik_c"], D.ncap, x["hk_c"], x["hv_c"], D.ncap2,
+                       self.idx, self.o, self.lse, self.ho, self.hlse, self.ws_step,
+                       err=self.err, stream=stream)
 
     def run(self, stream=None):
         """The whole pass on one stream."""

@@ -121,3 +121,23 @@ def test_noalloc_limit_matches_the_header():
     got = re.search(r"#define\s+SA_NOALLOC_MAX_SCORES\s+(\d+)", src)
     assert got is not None
     assert int(got.group(1)) == m.NOALLOC_MAX_SCORES
+
+
+def test_decode_step_workspace_follows_its_layout():
+    """sa_decode_step's workspace, worked by hand from its layout for the 128K
+    decode (B=32, N_cap=32768, k=2048, W=128, N2_cap=1024; every part rounded
+    up to 256 bytes):
+      counters 32 + 7 per row (rounded up to 64 ints), then per row a 8192-bin
+      histogram and 16 ints of top-k info:  4 * (256 + 32 * 8208)   = 1051648
+      score keys, rows of 32768:            4 * 32 * 32768          = 4194304
+      CSA shares: 34 key tiles -> 4 shares  4 * 32 * 4 * 64 * 128   = 4194304
+        and their LSEs                      4 * 32 * 4 * 64         =   32768
+      HCA shares: 18 key tiles -> 2 shares  4 * 32 * 2 * 64 * 128   = 2097152
+        and their LSEs                      4 * 32 * 2 * 64         =   16384
+      top-k candidate lists, 4 x 4096/row   4 * 32 * 4 * 4096       = 2097152
+    Rows longer than 32768 entries (the 1M decode) are not taken: 0."""
+    m = pytest.importorskip("sparse_attention_27_b300")
+    assert m.sa_decode_step_workspace_bytes(32, 64, 32768, 2048, 128, 1024) == (
+        1051648 + 4194304 + 4194304 + 32768 + 2097152 + 16384 + 2097152)
+    assert m.sa_decode_step_workspace_bytes(4, 64, 262144, 2048, 128, 8192) == 0
+    assert m.sa_decode_step_workspace_bytes(0, 64, 100, 64, 16, 4) == 0

@@ -3,7 +3,8 @@
 변경" -- compressed caches, a sliding-window ring, and a tail of tokens not
 yet compressed -- kept up to date by the library's own calls, step after step.
 
-* Decode, many steps in a row: each step writes its token into ring row
+* Decode, many steps in a row (the separate calls, csa_decode, and
+  sa_decode_step): each step writes its token into ring row
   t mod R of every layer's per-token arrays, compresses the CSA block the
   token closes (every m = 4 steps) and the HCA block (every m' = 128 steps),
   and attends.  The float64 oracle keeps its own caches, compressed from the
@@ -70,10 +71,12 @@ def block_range(t: int, m: int, B: int):
     return np.full(B, lo, dtype=np.int32), np.full(B, hi, dtype=np.int32)
 
 
-@pytest.mark.parametrize("fused", [True, False])
-def test_decode_steps_advance_the_rings_and_close_blocks(fused):
+@pytest.mark.parametrize("mode", ["fused", "split", "step"])
+def test_decode_steps_advance_the_rings_and_close_blocks(mode):
     """260 consecutive decode steps of 4 sequences from position 15875: 65
-    CSA blocks and 2 HCA blocks close on the way (at t = 15999 and 16127)."""
+    CSA blocks and 2 HCA blocks close on the way (at t = 15999 and 16127).
+    The step runs as csa_decode + hca_compress_attend (fused), as the
+    separate calls (split) or as one sa_decode_step (step)."""
     S, t0 = 260, 15875
     w = synth.Workload("steps", "decode", B=4, L=t0 + S + 1, T=1, R=256, k=256, W=128)
     x = exact_scores(w, synth.make_inputs(w))
@@ -103,11 +106,14 @@ def test_decode_steps_advance_the_rings_and_close_blocks(fused):
         for n in ("q_pos", "blk_lo", "blk_hi", "hblk_lo", "hblk_hi"):
             step.x[n].copy_(dev(x[n]))
         # the GPU step
-        if fused:
-            step.csa_fused()
+        if mode == "step":
+            step.decode_step()
         else:
-            step.csa()
-        step.hca()
+            if mode == "fused":
+                step.csa_fused()
+            else:
+                step.csa()
+            step.hca()
         torch.cuda.synchronize()
         assert step.device_errors() == 0, (s, step.device_errors())
         # the oracle's step on its own caches
