@@ -363,6 +363,26 @@ int sa_compress_backward(int dtype, int B, int d, int m, const void* k_raw, cons
 int sa_mxfp4_quantize(const void* x, int64_t nblk, void* codes, void* scales, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * sa_ring_write -- writes each sequence's new token into the sliding-window
+ * rings ([P3] "KV Cache 관리: 저장 구조까지 변경": the raw rows of a layer's
+ * last tokens are kept per sequence in a ring of R rows, token t in row
+ * t mod R, from which the window is attended and the next blocks pooled):
+ *     ring_i[b, pos[b] mod R, :] = rows_i[b, :]   for each array i < n
+ * One launch for all arrays (e.g. a step's K, V, indexer key and pooling
+ * logit of both layers).
+ *  n          number of arrays, 1..8
+ *  rings      HOST array of n device pointers: ring i [B, R, row_bytes[i]]
+ *  rows       HOST array of n device pointers: rows i [B, row_bytes[i]]
+ *  row_bytes  HOST array of n sizes, each a positive multiple of 4
+ *  pos        [B] int32 device: each sequence's new position
+ * Errors: n outside 1..8, a size not a positive multiple of 4, a null or
+ * misaligned (4-byte) pointer -> SA_ERR_INVALID_ARG.  Device errors:
+ * pos[b] < 0 -> SA_ERR_BOUNDS (that sequence's rows are skipped).
+ */
+int sa_ring_write(int B, int R, const int32_t* pos, int n, void* const* rings,
+                  const void* const* rows, const int* row_bytes, int32_t* err, void* stream);
+
+/* ---------------------------------------------------------------------------
  * attn_merge -- exact log-sum-exp merge of attention partials computed over
  * disjoint key sets (the branches of the multi-branch design, [P2] and [P1]
  * IDEAS; also split-K partials):

@@ -28,7 +28,7 @@ EXPORTS = (
     "csa_attend", "csa_attend_workspace_bytes", "hca_compress_attend",
     "hca_compress_attend_workspace_bytes", "attn_merge", "csa_index_topk_noalloc",
     "sa_mxfp4_quantize", "csa_decode", "csa_attend_backward", "hca_attend_backward",
-    "sa_compress_backward", "sa_decode_step", "sa_decode_step_workspace_bytes",
+    "sa_compress_backward", "sa_decode_step", "sa_decode_step_workspace_bytes", "sa_ring_write",
 )
 
 
@@ -69,6 +69,7 @@ _lib.sa_decode_step.argtypes = ([_i] * 9 + [_f] + [_vp] * 12 + [_i] + [_vp] * 2 
                                  [_vp] * 2 + [_i] + [_vp] * 3 + [_i] + [_vp] * 2 + [_i] +
                                  [_vp, _i] + [_vp] * 5 + [_sz, _vp, _vp])
 _lib.sa_decode_step_workspace_bytes.argtypes = [_i] * 6
+_lib.sa_ring_write.argtypes = [_i, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp]
 _lib.sa_decode_step_workspace_bytes.restype = _sz
 _lib.csa_attend.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _i, _vp, _vp,
                             _vp, _i, _vp, _i, _vp, _vp, _sz, _vp, _vp]
@@ -190,6 +191,20 @@ def csa_decode(B, H, d, HI, dI, m, k, W, sm_scale, q, q_idx, w, q_pos, k_raw, v_
                            _p(q_pos), _p(k_raw), _p(v_raw), _p(ik_raw), _p(z), R, _p(blk_lo),
                            _p(blk_hi), max_blocks, _p(k_c), _p(v_c), _p(ik_c), N_cap, _p(idx),
                            _p(o), _out_code(o), _p(lse), _p(err), _stream(stream)), "csa_decode")
+
+
+def sa_ring_write(B, R, pos, rings, rows, err=None, stream=None):
+    """Each sequence's new token into the rings: rings[i][b, pos[b] % R] =
+    rows[i][b] for every pair (ring [B,R,...], rows [B,...], same dtype)."""
+    n = len(rings)
+    if n != len(rows) or not 1 <= n <= 8:
+        raise SaError(SA_ERR_INVALID_ARG, "sa_ring_write")
+    ring_p = (C.c_void_p * n)(*[_p(t) for t in rings])
+    row_p = (C.c_void_p * n)(*[_p(t) for t in rows])
+    nbytes = (C.c_int * n)(*[t[0].numel() * t.element_size() if t.dim() > 1 else t.element_size()
+                             for t in rows])
+    _check(_lib.sa_ring_write(B, R, _p(pos), n, ring_p, row_p, nbytes, _p(err), _stream(stream)),
+           "sa_ring_write")
 
 
 def sa_decode_step_workspace_bytes(B, H, N_cap, k, W, N2_cap) -> int:

@@ -303,6 +303,23 @@ int csa_decode(int B, int H, int d, int HI, int dI, int m, int k, int W, float s
   return status_of(launch_fused_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
+int sa_ring_write(int B, int R, const int32_t* pos, int n, void* const* rings,
+                  const void* const* rows, const int* row_bytes, int32_t* err, void* stream) {
+  if (B < 0 || R < 1 || n < 1 || n > kRingMaxArrays || !pos || !rings || !rows || !row_bytes)
+    return SA_ERR_INVALID_ARG;
+  RingWriteArgs a{};
+  a.B = B; a.R = R; a.n = n; a.pos = pos; a.err = err;
+  for (int i = 0; i < n; ++i) {
+    if (!rings[i] || !rows[i] || row_bytes[i] <= 0 || row_bytes[i] % 4 ||
+        reinterpret_cast<uintptr_t>(rings[i]) % 4 || reinterpret_cast<uintptr_t>(rows[i]) % 4)
+      return SA_ERR_INVALID_ARG;
+    a.rings[i] = rings[i];
+    a.rows[i] = rows[i];
+    a.row_bytes[i] = row_bytes[i];
+  }
+  return status_of(launch_ring_write(a, static_cast<cudaStream_t>(stream)));
+}
+
 namespace {
 // Workspace of sa_decode_step: counters, histograms and row info (zeroed by
 // each call) | score keys [B, N_cap] | CSA partials | HCA partials | top-k

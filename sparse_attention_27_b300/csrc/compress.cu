@@ -192,4 +192,27 @@ cudaError_t launch_mxfp4_quantize(const void* x_bf16, int64_t nblk, void* codes,
   return cudaGetLastError();
 }
 
+
+// ---------------------------------------------------------------- ring write
+// One CTA per (sequence, array): row b of array i into ring row pos[b] mod R,
+// 4 bytes per thread and step.
+__global__ void ring_write_kernel(RingWriteArgs a) {
+  const int b = blockIdx.x, i = blockIdx.y;
+  const int p = __ldg(a.pos + b);
+  if (p < 0) {
+    if (threadIdx.x == 0 && i == 0) set_err(a.err, SA_ERR_BOUNDS);
+    return;
+  }
+  const int words = a.row_bytes[i] / 4;
+  const uint32_t* src = static_cast<const uint32_t*>(a.rows[i]) + (int64_t)b * words;
+  uint32_t* dst = static_cast<uint32_t*>(a.rings[i]) + ((int64_t)b * a.R + p % a.R) * words;
+  for (int w = threadIdx.x; w < words; w += blockDim.x) dst[w] = __ldg(src + w);
+}
+
+cudaError_t launch_ring_write(const RingWriteArgs& a, cudaStream_t st) {
+  if (a.B == 0) return cudaSuccess;
+  ring_write_kernel<<<dim3((unsigned)a.B, (unsigned)a.n), 128, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace sa

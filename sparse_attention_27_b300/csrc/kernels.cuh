@@ -130,6 +130,18 @@ struct FusedDecodeArgs {
 bool fused_decode_plan(FusedDecodeArgs& a, int num_sms);
 cudaError_t launch_fused_decode(const FusedDecodeArgs& a, cudaStream_t st);
 
+// sa_ring_write: row b of array i into ring i's row pos[b] mod R.
+constexpr int kRingMaxArrays = 8;
+struct RingWriteArgs {
+  int B, R, n;
+  const int32_t* pos;
+  void* rings[kRingMaxArrays];
+  const void* rows[kRingMaxArrays];
+  int row_bytes[kRingMaxArrays];
+  int32_t* err;
+};
+cudaError_t launch_ring_write(const RingWriteArgs& a, cudaStream_t st);
+
 // Whole hybrid decode step (sa_decode_step): both layers of one decode token
 // per sequence in one persistent launch over a queue of work items.  All
 // tensors bf16 unless stated.

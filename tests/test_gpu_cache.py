@@ -35,6 +35,11 @@ from test_gpu_parity import TOL_ATT, check_cache, exact_bf16_bits, pool_bound
 pytestmark = pytest.mark.gpu
 
 RING = {"k_raw": "k_c", "v_raw": "v_c", "ik_raw": "ik_c"}
+
+
+def sa_lib():
+    import sparse_attention_27_b300 as m
+    return m
 PER_TOKEN = ("k_raw", "v_raw", "ik_raw", "z", "hk_raw", "hv_raw", "hz")
 PER_STEP = ("q", "q_hca", "q_idx", "w_idx")
 
@@ -94,13 +99,16 @@ def test_decode_steps_advance_the_rings_and_close_blocks(mode):
         t = t0 + s
         tok, qs = draw_token(w, s), draw_queries(w, s)
         slot = t % w.R
-        for n in PER_TOKEN:                      # the token into ring row t mod R
+        for n in PER_TOKEN:                      # the oracle's rings: row t mod R
             x[n][:, slot] = tok[n]
-            step.x[n][:, slot].copy_(dev(tok[n]))
+        x["q_pos"] = np.full((w.B, 1), t, dtype=np.int32)
+        step.x["q_pos"].copy_(dev(x["q_pos"]))
+        # the library's rings: one sa_ring_write for every per-token array
+        sa_lib().sa_ring_write(w.B, w.R, step.x["q_pos"], [step.x[n] for n in PER_TOKEN],
+                               [dev(tok[n]) for n in PER_TOKEN], err=step.err)
         for n in PER_STEP:
             x[n] = qs[n]
             step.x[n].copy_(dev(qs[n]))
-        x["q_pos"] = np.full((w.B, 1), t, dtype=np.int32)
         x["blk_lo"], x["blk_hi"] = block_range(t, w.m, w.B)
         x["hblk_lo"], x["hblk_hi"] = block_range(t, w.m2, w.B)
         for n in ("q_pos", "blk_lo", "blk_hi", "hblk_lo", "hblk_hi"):
@@ -191,3 +199,34 @@ def test_prefill_second_chunk_on_the_first_chunks_caches(L, t0):
         nb = L // m
         check_cache(host(s2.x[n][0, :nb]), ref[n][0, :nb], "bf16", n,
                     pool_bound(x[raw][0], m, 0, nb))
+
+
+def test_ring_write_puts_each_token_in_row_t_mod_R():
+    """sa_ring_write: row b of each array lands in ring row pos[b] mod R of
+    its ring, bit for bit; every other ring row is untouched; a negative
+    position is reported (SA_ERR_BOUNDS) and its rows are skipped."""
+    m = sa_lib()
+    B, R = 5, 12
+    g = torch.Generator(device="cuda").manual_seed(3)
+    rings = [torch.randn(B, R, 128, device="cuda", generator=g).to(torch.bfloat16),
+             torch.randn(B, R, 64, device="cuda", generator=g).to(torch.bfloat16),
+             torch.randn(B, R, device="cuda", generator=g)]
+    rows = [torch.randn(B, 128, device="cuda", generator=g).to(torch.bfloat16),
+            torch.randn(B, 64, device="cuda", generator=g).to(torch.bfloat16),
+            torch.randn(B, device="cuda", generator=g)]
+    pos = torch.tensor([0, 11, 12, 37, -1], dtype=torch.int32, device="cuda")
+    before = [r.clone() for r in rings]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m.sa_ring_write(B, R, pos, rings, rows, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 1 << m.SA_ERR_BOUNDS
+    for ring, row, old in zip(rings, rows, before):
+        want = old.clone()
+        for b, p_ in enumerate(pos.tolist()):
+            if p_ >= 0:
+                want[b, p_ % R] = row[b]
+        assert torch.equal(ring.view(torch.uint8) if ring.dtype != torch.float32 else ring.view(torch.int32),
+                           want.view(torch.uint8) if want.dtype != torch.float32 else want.view(torch.int32))
+    with pytest.raises(m.SaError) as e:       # a row size that is not a multiple of 4 bytes
+        m.sa_ring_write(B, R, pos, [rings[0][..., :1]], [rows[0][:, :1]])
+    assert e.value.status == m.SA_ERR_INVALID_ARG
