@@ -59,6 +59,8 @@ def lib():
             L.orc_round_bf16.argtypes = [C.c_double]
             L.orc_round_bf16.restype = C.c_double
             L.orc_compress.argtypes = [C.c_int64, C.c_int, C.c_int, _dp, _dp, C.c_int, _dp]
+            L.orc_compress_channels.argtypes = [C.c_int64, C.c_int, C.c_int, _dp, _dp, C.c_int,
+                                                _dp]
             L.orc_index_scores.argtypes = [C.c_int64, C.c_int, C.c_int, _dp, _dp, _dp, C.c_int64,
                                            _ip, _ip, _dp]
             L.orc_topk.argtypes = [C.c_int64, C.c_int64, _dp, _ip, C.c_int, _i32p]
@@ -120,6 +122,25 @@ def compress(x_ring: np.ndarray, z_ring: np.ndarray, m: int, blk_lo: int, blk_hi
     out = np.empty((nb, d))
     mode = {"f64": 0, "f32": 1, "bf16": 2}[store]
     lib().orc_compress(nb, m, d, X, Z, mode, out)
+    return out
+
+
+def compress_channels(x_ring: np.ndarray, z_ring: np.ndarray, m: int, blk_lo: int,
+                      blk_hi: int, store: str) -> np.ndarray:
+    """Per-channel softmax-pooled blocks [blk_lo, blk_hi) of one sequence:
+    x_ring and z_ring [R, d] (one logit per raw token and channel).  Block j
+    covers raw positions j*m .. j*m+m-1, found in ring rows p mod R.  Returns
+    doubles rounded to ``store`` ("f32", "bf16" or "f64")."""
+    R, d = x_ring.shape
+    nb = blk_hi - blk_lo
+    if nb <= 0:
+        return np.zeros((0, d))
+    pos = (np.arange(blk_lo * m, blk_hi * m) % R)
+    X = _c(to_f64(x_ring)[pos])
+    Z = _c(np.asarray(z_ring, dtype=np.float64)[pos])
+    out = np.empty((nb, d))
+    mode = {"f64": 0, "f32": 1, "bf16": 2}[store]
+    lib().orc_compress_channels(nb, m, d, X, Z, mode, out)
     return out
 
 

@@ -91,6 +91,39 @@ void orc_compress(int64_t nblk, int m, int d, const double *X, const double *z,
 
 /* ---------------------------------------------------- a2: indexer scores */
 
+/* Per-channel softmax pooling: the compressor variant with one logit per raw
+ * token AND channel ([P3] "Compressed Sparse Attention (CSA)" step 1, m
+ * consecutive entries merged into one; the pages do not say whether the
+ * merge weights are shared by all channels -- this is the variant where they
+ * are not).  For block b and channel c, with the block's m logits of that
+ * channel,
+ *   Xc[b, c] = sum_i softmax_i(z[b*m+i, c]) * X[b*m+i, c].
+ * Layouts: X, z [nblk*m, d] (row = raw position, column = channel);
+ * Xc [nblk, d].  round_mode as orc_compress. */
+void orc_compress_channels(int64_t nblk, int m, int d, const double *X, const double *z,
+                           int round_mode, double *Xc)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < nblk; ++b) {
+        for (int c = 0; c < d; ++c) {
+            double mu = z[(b * m) * (int64_t)d + c];
+            for (int i = 1; i < m; ++i) {
+                const double zi = z[(b * m + i) * (int64_t)d + c];
+                if (zi > mu) mu = zi;
+            }
+            double den = 0.0;
+            for (int i = 0; i < m; ++i) den += exp(z[(b * m + i) * (int64_t)d + c] - mu);
+            double acc = 0.0;
+            for (int i = 0; i < m; ++i)
+                acc += (exp(z[(b * m + i) * (int64_t)d + c] - mu) / den) *
+                       X[(b * m + i) * (int64_t)d + c];
+            if (round_mode == 1) acc = orc_round_f32(acc);
+            else if (round_mode == 2) acc = orc_round_bf16(acc);
+            Xc[b * (int64_t)d + c] = acc;
+        }
+    }
+}
+
 /* Lightning-indexer score of every visible compressed entry for each query row
  * ([P3] step 2, [P1] IDEAS):
  *     s[r, j] = sum_h w[r,h] * max(0, q_I[r,h,:] . Ik_c[seq[r], j, :])
