@@ -363,6 +363,27 @@ int sa_compress_backward(int dtype, int B, int d, int m, const void* k_raw, cons
 int sa_mxfp4_quantize(const void* x, int64_t nblk, void* codes, void* scales, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * sa_compress_channels -- the compressor variant with one pooling logit per
+ * raw token AND channel ([P3] "Compressed Sparse Attention (CSA)" step 1: m
+ * consecutive entries merged into one; here every channel has its own merge
+ * weights):
+ *     x_c[b, j, c] = sum_i softmax_i(z[b, p_i, c]) * x_raw[b, p_i, c],
+ * p_i = (j*m + i) mod R, i < m, for the blocks [blk_lo[b], blk_hi[b]).  Pools
+ * one array (K, V or the indexer key, each with its own logits); rounds to
+ * the storage type.
+ *  dtype      SA_F32 or SA_BF16: x_raw and x_c
+ *  x_raw [B,R,d]; z [B,R,d] f32; x_c [B,N_cap,d]
+ *  blk_lo, blk_hi [B] int32 device; max_blocks host bound on their lengths
+ * fp32 evaluation, per channel in ascending i: the max logit, the sum of
+ * exp(z_i - max), then sum_i (exp(z_i - max) / sum) * x_i by fused
+ * multiply-adds.  Device errors: a block outside [0, N_cap) or a range
+ * longer than max_blocks -> SA_ERR_BOUNDS (block skipped).
+ */
+int sa_compress_channels(int dtype, int B, int d, int m, const void* x_raw, const float* z, int R,
+                         const int32_t* blk_lo, const int32_t* blk_hi, int max_blocks, void* x_c,
+                         int N_cap, int32_t* err, void* stream);
+
+/* ---------------------------------------------------------------------------
  * sa_ring_write -- writes each sequence's new token into the sliding-window
  * rings ([P3] "KV Cache 관리: 저장 구조까지 변경": the raw rows of a layer's
  * last tokens are kept per sequence in a ring of R rows, token t in row

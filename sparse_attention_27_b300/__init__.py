@@ -29,6 +29,7 @@ EXPORTS = (
     "hca_compress_attend_workspace_bytes", "attn_merge", "csa_index_topk_noalloc",
     "sa_mxfp4_quantize", "csa_decode", "csa_attend_backward", "hca_attend_backward",
     "sa_compress_backward", "sa_decode_step", "sa_decode_step_workspace_bytes", "sa_ring_write",
+    "sa_compress_channels",
 )
 
 
@@ -70,6 +71,8 @@ _lib.sa_decode_step.argtypes = ([_i] * 9 + [_f] + [_vp] * 12 + [_i] + [_vp] * 2 
                                  [_vp, _i] + [_vp] * 5 + [_sz, _vp, _vp])
 _lib.sa_decode_step_workspace_bytes.argtypes = [_i] * 6
 _lib.sa_ring_write.argtypes = [_i, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp]
+_lib.sa_compress_channels.argtypes = [_i, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _vp, _i, _vp,
+                                      _vp]
 _lib.sa_decode_step_workspace_bytes.restype = _sz
 _lib.csa_attend.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _i, _vp, _vp,
                             _vp, _i, _vp, _i, _vp, _vp, _sz, _vp, _vp]
@@ -191,6 +194,14 @@ def csa_decode(B, H, d, HI, dI, m, k, W, sm_scale, q, q_idx, w, q_pos, k_raw, v_
                            _p(q_pos), _p(k_raw), _p(v_raw), _p(ik_raw), _p(z), R, _p(blk_lo),
                            _p(blk_hi), max_blocks, _p(k_c), _p(v_c), _p(ik_c), N_cap, _p(idx),
                            _p(o), _out_code(o), _p(lse), _p(err), _stream(stream)), "csa_decode")
+
+
+def sa_compress_channels(dtype, B, d, m, x_raw, z, R, blk_lo, blk_hi, max_blocks, x_c, N_cap,
+                         err=None, stream=None):
+    """Per-channel softmax pooling of one array: z [B,R,d] f32 logits."""
+    _check(_lib.sa_compress_channels(dtype, B, d, m, _p(x_raw), _p(z), R, _p(blk_lo), _p(blk_hi),
+                                     max_blocks, _p(x_c), N_cap, _p(err), _stream(stream)),
+           "sa_compress_channels")
 
 
 def sa_ring_write(B, R, pos, rings, rows, err=None, stream=None):

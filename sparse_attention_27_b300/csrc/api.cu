@@ -303,6 +303,18 @@ int csa_decode(int B, int H, int d, int HI, int dI, int m, int k, int W, float s
   return status_of(launch_fused_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
+int sa_compress_channels(int dtype, int B, int d, int m, const void* x_raw, const float* z, int R,
+                         const int32_t* blk_lo, const int32_t* blk_hi, int max_blocks, void* x_c,
+                         int N_cap, int32_t* err, void* stream) {
+  if (!plain_dtype(dtype) || B < 0 || d < 1 || m < 1 || R < m || max_blocks < 0 || N_cap < 0)
+    return SA_ERR_INVALID_ARG;
+  if (!x_raw || !z || !blk_lo || !blk_hi || !x_c) return SA_ERR_INVALID_ARG;
+  CompressChArgs a{};
+  a.dtype = dtype; a.B = B; a.d = d; a.m = m; a.R = R; a.max_blocks = max_blocks; a.N_cap = N_cap;
+  a.x_raw = x_raw; a.z = z; a.blk_lo = blk_lo; a.blk_hi = blk_hi; a.x_c = x_c; a.err = err;
+  return status_of(launch_compress_channels(a, static_cast<cudaStream_t>(stream)));
+}
+
 int sa_ring_write(int B, int R, const int32_t* pos, int n, void* const* rings,
                   const void* const* rows, const int* row_bytes, int32_t* err, void* stream) {
   if (B < 0 || R < 1 || n < 1 || n > kRingMaxArrays || !pos || !rings || !rows || !row_bytes)

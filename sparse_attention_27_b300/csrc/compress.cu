@@ -215,4 +215,47 @@ cudaError_t launch_ring_write(const RingWriteArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+
+// ------------------------------------------------ per-channel pooling
+// One CTA per (sequence, block); thread c pools channel c (and c + blockDim,
+// ...).  fp32 order, per channel: mu = max_i z_i (i ascending); den =
+// sum_i exp(z_i - mu) in ascending i; x_c = sum_i (exp(z_i - mu) / den) * x_i
+// by fused multiply-adds in ascending i; rounded to the storage type.
+template <int DT>
+__global__ void compress_channels_kernel(CompressChArgs a) {
+  const int b = blockIdx.y;
+  const int lo = __ldg(a.blk_lo + b), hi = __ldg(a.blk_hi + b);
+  const int64_t j = (int64_t)lo + blockIdx.x;
+  if (j >= hi) return;
+  if (hi - lo > a.max_blocks || j < 0 || j >= a.N_cap) {
+    if (threadIdx.x == 0) set_err(a.err, SA_ERR_BOUNDS);
+    return;
+  }
+  const int m = a.m, R = a.R, d = a.d;
+  const int64_t p0 = j * m;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    const float* zc = a.z + (int64_t)b * R * d + c;
+    auto row = [&](int i) -> int64_t { return ((p0 + i) % R) * d; };
+    float mu = -INFINITY;
+    for (int i = 0; i < m; ++i) mu = fmaxf(mu, __ldg(zc + row(i)));
+    float den = 0.f;
+    for (int i = 0; i < m; ++i) den += expf(__ldg(zc + row(i)) - mu);
+    float acc = 0.f;
+    for (int i = 0; i < m; ++i) {
+      const float wi = expf(__ldg(zc + row(i)) - mu) / den;
+      acc = fmaf(wi, Store<DT>::ld(a.x_raw, (int64_t)b * R * d + row(i) + c), acc);
+    }
+    Store<DT>::st(a.x_c, ((int64_t)b * a.N_cap + j) * d + c, acc);
+  }
+}
+
+cudaError_t launch_compress_channels(const CompressChArgs& a, cudaStream_t st) {
+  if (a.B == 0 || a.max_blocks == 0) return cudaSuccess;
+  const dim3 grid((unsigned)a.max_blocks, (unsigned)a.B);
+  const int threads = a.d < 128 ? ((a.d + 31) / 32) * 32 : 128;
+  if (a.dtype == SA_BF16) compress_channels_kernel<SA_BF16><<<grid, threads, 0, st>>>(a);
+  else compress_channels_kernel<SA_F32><<<grid, threads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace sa

@@ -130,6 +130,18 @@ struct FusedDecodeArgs {
 bool fused_decode_plan(FusedDecodeArgs& a, int num_sms);
 cudaError_t launch_fused_decode(const FusedDecodeArgs& a, cudaStream_t st);
 
+// sa_compress_channels: per-channel softmax pooling of one array.
+struct CompressChArgs {
+  int dtype, B, d, m, R, max_blocks, N_cap;
+  const void* x_raw;    // [B, R, d]
+  const float* z;       // [B, R, d] f32
+  const int32_t* blk_lo;
+  const int32_t* blk_hi;
+  void* x_c;            // [B, N_cap, d]
+  int32_t* err;
+};
+cudaError_t launch_compress_channels(const CompressChArgs& a, cudaStream_t st);
+
 // sa_ring_write: row b of array i into ring i's row pos[b] mod R.
 constexpr int kRingMaxArrays = 8;
 struct RingWriteArgs {
