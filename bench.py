@@ -485,10 +485,13 @@ class PipelinedIO:
 
     def record(self, s_csa, s_hca, s_cp, s_out, n: int = 4):
         """n consecutive steps over the two buffer sets (step k uses set k
-        mod 2): a step's inputs were copied in while the step before it ran;
-        its outputs go out while the next one runs; its set is refilled from
-        pinned memory for step k + 2 (or the next replay) once it is done, and
-        step k + 2 writes the set's outputs only after they have gone out."""
+        mod 2).  The compute streams wait on each other directly: step k's
+        CSA stream (its ring write, then the CSA layer) after step k - 1's HCA
+        layer, step k's HCA stream after step k's ring write.  A step's inputs
+        were copied in while the step before it ran; its outputs go out while
+        the next one runs; its set is refilled from pinned memory for step
+        k + 2 (or the next replay) once it is done, and step k + 2 writes the
+        set's outputs only after they have gone out."""
         import torch
         cur = torch.cuda.current_stream()
         start = torch.cuda.Event()
@@ -497,36 +500,35 @@ class PipelinedIO:
             s_.wait_event(start)
         in_ev = [None, None]                      # inputs of set p in place
         out_ev = [None, None]                     # outputs of set p copied out
-        prev = None
+        hca_done = None                           # the previous step's HCA layer
         for k in range(n):
             p = k % 2
-            for s_ in (s_csa, s_hca):
-                for e in (in_ev[p], out_ev[p], prev):
-                    if e is not None:
-                        s_.wait_event(e)
+            for e in (in_ev[p], out_ev[p], hca_done):
+                if e is not None:
+                    s_csa.wait_event(e)
             self._compute(p, s_csa, s_hca)
             e1, e2 = torch.cuda.Event(), torch.cuda.Event()
             e1.record(s_csa)
             e2.record(s_hca)
+            hca_done = e2
             s_out.wait_event(e1)
             s_out.wait_event(e2)
-            done = torch.cuda.Event()
-            done.record(s_out)
-            prev = done
             with torch.cuda.stream(s_out):        # this step's outputs while the next runs
                 self.h_out[p].copy_(self.d_out[p], non_blocking=True)
             out_ev[p] = torch.cuda.Event()
             out_ev[p].record(s_out)
-            s_cp.wait_event(done)
+            s_cp.wait_event(e1)
+            s_cp.wait_event(e2)
             with torch.cuda.stream(s_cp):         # refill this set for step k + 2
                 self.d_in[p].copy_(self.h_in[p], non_blocking=True)
             in_ev[p] = torch.cuda.Event()
             in_ev[p].record(s_cp)
-        j1, j2 = torch.cuda.Event(), torch.cuda.Event()
+        j1, j2, j3 = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
         j1.record(s_out)
         j2.record(s_cp)
-        cur.wait_event(j1)
-        cur.wait_event(j2)
+        j3.record(s_csa)
+        for e in (j1, j2, j3):
+            cur.wait_event(e)
 
 
 def cpu_baseline(w, x, seqs: int) -> dict:
