@@ -9,35 +9,42 @@
 // "EP 95. DeepSeek-V4 논문 읽기 — 노정석", section IDEAS (one shared KV head).
 //
 // Work: an item is (query row, split of the row's key list); a persistent grid
-// of at most two CTAs per SM takes items as they come free.  Two resident CTAs give
-// each SM two independent pipelines (each CTA: two K/V stages, one Q tile,
-// 256 TMEM columns).  A row's key list is the
+// takes items as they come free.  Two shapes of the same pipeline:
+//  * shallow (decode): two CTAs per SM, each with two K/V stages, one Q tile
+//    and 256 TMEM columns -- two independent pipelines per SM hide the
+//    set-up and drain of the short items of a decode step;
+//  * deep (long key lists, prefill): one CTA per SM with six K/V stages and
+//    four producer warps, so that up to four tiles are gathered while the
+//    tensor core works on two.
+// A row's key list is the
 // compressed part (rows idx[r, i] for CSA, rows 0.. for HCA), padded to a
 // multiple of 4 keys, then the window rows (ring slot u mod R); it is
 // processed in tiles of 64 keys.
 //
-// Warp roles (288 threads):
-//  * warp 3, fetcher: takes the CTA's items one by one from a counter shared
+// Warp roles (P producer warps; 32 * (P + 6) threads):
+//  * warp P, fetcher: takes the CTA's items one by one from a counter shared
 //    by the grid (zeroed by the call before the launch) and passes them to
 //    the other roles through a two-slot ring in shared memory.  CTAs that
 //    start late -- behind another kernel that holds most SMs -- find the
 //    work already taken, so the grid never waits for them.  Without a
 //    counter it hands out items c, c+G, ...
-//  * warps 0-1, producers: warp w issues the tiles with ordinal n = w (mod
-//    kProducers).
+//  * warps 0..P-1, producers: warp w issues the tiles with ordinal n = w (mod P).
 //    Lane l finds the source rows of keys 2l and 2l+1; then each cp.async
 //    instruction of the warp copies two whole 256-byte rows (half-warp per
 //    key, one 16-byte chunk per lane) straight into the 128B-swizzled layout
 //    the tensor core reads (keys past the list are zero-filled); the warp
 //    waits for its copies, fences them to the async proxy and arrives on the
-//    stage's mbarrier, so two tiles are in flight per CTA (four per SM).
+//    stage's mbarrier, so P tiles are in flight per CTA.  In dense mode
+//    (HCA) a tile of 64 consecutive compressed rows comes instead by four TMA
+//    boxes, the copy engine applying the same swizzle.
 //    Warp 0 also brings the item's 64 query heads by one TMA tiled load per
 //    64-column half into the Q tile.
-//  * warp 4, MMA: S(n) = Q . K(n)^T (M = 64 heads, N = 64 keys, K = 128) into
+//  * warp P+1, MMA: S(n) = Q . K(n)^T (M = 64 heads, N = 64 keys, K = 128) into
 //    one of two TMEM S buffers, issued before PV(n-1) so that the softmax of
 //    tile n overlaps the tensor core; O += P(n) . V(n) (M = 64, N = 128,
 //    K = 64) into the TMEM O accumulator (freed by the softmax after each item).
-//  * warps 5-8, softmax: the M = 64 accumulator puts rows 16q..16q+15 in
+//  * warps P+2..P+5, softmax (TMEM lane quarter = warp mod 4): the M = 64
+//    accumulator puts rows 16q..16q+15 in
 //    TMEM lanes 32q..32q+15; the 16x256b load shape spreads those 16 rows
 //    over all 32 lanes (two heads and a quarter of the keys per lane), fp32
 //    exp2 of the scaled logits, P to shared memory in bf16; the running max
@@ -57,20 +64,30 @@ namespace sa {
 
 namespace {
 
-constexpr int kThreads = 288;
+// One shape of the pipeline: CTAs per SM, K/V stages per CTA, producer warps.
+// A producer's wait for stage n % S is sound by parity only while that
+// barrier is at most one phase behind: the warp's own previous tile n - P
+// waited for the release of tile n - P - S, which covers tile n - 2S as long
+// as P <= S (releases come in tile order).
+template <int kCtas, int kStg, int kProd>
+struct AttnShape {
+  static constexpr int kCtasPerSm = kCtas;
+  static constexpr int kStages = kStg;
+  static constexpr int kProducers = kProd;
+  static constexpr int kFetchWarp = kProd;       // fills the item ring
+  static constexpr int kMmaWarp = kProd + 1;     // MMA issuer and TMEM owner; softmax after it
+  static constexpr int kThreads = 32 * (kProd + 6);
+  // warps that read every item: the producers, the MMA warp, the 4 softmax warps
+  static constexpr int kItemReaders = kProd + 1 + 4;
+  static_assert(kProd <= kStg, "parity waits of the producers");
+};
+using ShallowShape = AttnShape<2, 2, 2>;         // decode: two pipelines per SM
+using DeepShape = AttnShape<1, 6, 4>;            // long key lists: one deep pipeline
+// items per SM from which a launch takes the deep shape
+constexpr int kAttnDeepItemsPerSm = 8;
+
 constexpr int kKeys = 64;                      // keys per tile
-constexpr int kCtasPerSm = 2;                  // two independent pipelines per SM
-constexpr int kStages = 2;                     // K/V tiles in flight per CTA
-// Producer warps 0 .. kProducers-1 issue tile n in warp n % kProducers.  A
-// producer's wait for stage n % kStages is sound by parity only while that
-// barrier is at most one phase behind: the warp's own previous tile n -
-// kProducers waited for the release of tile n - kProducers - kStages, which
-// covers tile n - 2 * kStages as long as kProducers <= kStages.
-constexpr int kProducers = kStages;
-constexpr int kFetchWarp = 3;                  // fills the item ring (a warp no producer uses)
-// warps that read every item: the producers, the MMA warp, the 4 softmax warps
-constexpr int kItemReaders = kProducers + 1 + 4;
-static_assert(kProducers < kFetchWarp, "the fetcher is not a producer");
+constexpr int kMaxStages = 6;
 constexpr int kQBufs = 1;                      // query tiles per CTA
 constexpr int kOBufs = 1;                      // TMEM O accumulators per CTA
 constexpr int kD = 128;                        // head dim
@@ -83,12 +100,12 @@ constexpr int kTmemCols = 256;                 // S: 2 x 64 at 0; O: 128 at 128 
 constexpr float kRescaleThreshold = 32.f;      // log2 units: P <= 2^32, far inside fp32 and bf16
 
 struct Ctl {
-  uint64_t full[kStages], empty[kStages];
+  uint64_t full[kMaxStages], empty[kMaxStages];
   uint64_t q_full[kQBufs], q_empty[kQBufs];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2], p_empty[2];
   uint64_t o_empty[kOBufs];
-  uint64_t it_full[2], it_empty[2];   // ring of the CTA's next items (fetched by warp 3)
+  uint64_t it_full[2], it_empty[2];   // ring of the CTA's next items (fetched by the fetcher)
   int64_t it_slot[2];
   uint32_t tmem;
   int abort;
@@ -96,6 +113,8 @@ struct Ctl {
 
 struct TMaps {
   CUtensorMap q;
+  CUtensorMap k, v;        // dense mode: the compressed caches [B*N_cap, 128], box 64 x 64
+  int dense_tma;           // 1: tiles wholly inside a row's compressed rows come by TMA
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -144,8 +163,11 @@ __device__ __forceinline__ Item make_item(const AttnArgs& a, int64_t it) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+template <class Sh>
+__global__ void __launch_bounds__(Sh::kThreads, Sh::kCtasPerSm)
     attend_tc_kernel(const __grid_constant__ TMaps tm, AttnArgs a) {
+  constexpr int kStages = Sh::kStages, kProducers = Sh::kProducers;
+  constexpr int kFetchWarp = Sh::kFetchWarp, kMmaWarp = Sh::kMmaWarp;
   extern __shared__ unsigned char smem_raw[];
   Ctl& C = *reinterpret_cast<Ctl*>(smem_raw);
   unsigned char* base = reinterpret_cast<unsigned char*>(
@@ -176,18 +198,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int s = 0; s < kOBufs; ++s) mbar_init(&C.o_empty[s], 128);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&C.it_full[s], 1);
-      mbar_init(&C.it_empty[s], kItemReaders);
+      mbar_init(&C.it_empty[s], Sh::kItemReaders);
     }
     C.abort = 0;
     mbar_fence_init();
   }
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&tm.q);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm.q);
+    if (tm.dense_tma) {
+      tma_prefetch_desc(&tm.k);
+      tma_prefetch_desc(&tm.v);
+    }
+  }
   // the fetcher claims its first item now, so the round trip to the counter
   // overlaps the set-up
   int64_t first_item = -1;
   if (warp == kFetchWarp && lane == 0)
     first_item = a.item_counter ? (int64_t)atomicAdd(a.item_counter, 1u) : (int64_t)blockIdx.x;
-  if (warp == 4) tmem_alloc(&C.tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(&C.tmem, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -265,6 +293,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           break;
         }
         unsigned char* stage = sKV + st * kStageBytes;
+        if (tm.dense_tma && (I.t_begin + t + 1) * kKeys <= I.n_comp) {
+          // 64 consecutive compressed rows (dense mode): four TMA boxes; the
+          // stage completes by byte count plus the warp's 32 arrivals
+          if (lane == 0) {
+            const int32_t y = (int32_t)((int64_t)I.b * a.N_cap + (I.t_begin + t) * kKeys);
+            mbar_arrive_expect_tx(&C.full[st], kStageBytes);
+            tma_load_2d(&tm.k, &C.full[st], stage, 0, y);
+            tma_load_2d(&tm.k, &C.full[st], stage + kHalf, 64, y);
+            tma_load_2d(&tm.v, &C.full[st], stage + 2 * kHalf, 0, y);
+            tma_load_2d(&tm.v, &C.full[st], stage + 3 * kHalf, 64, y);
+          } else {
+            mbar_arrive(&C.full[st]);
+          }
+          continue;
+        }
         // lane l resolves the source rows of keys 2l and 2l+1 as (row << 1 | raw),
         // -1 for a key with no row (masked: zero-filled)
         int64_t src2[2];
@@ -311,9 +354,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     if (!ok) *abort_flag = 1;
-  } else if (warp < 4) {
-    // warps between the producers and the fetcher have no role
-  } else if (warp == 4) {
+  } else if (warp == kMmaWarp) {
     // ================================================================= MMA
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(kHeads, kKeys, 0, 0);
@@ -580,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -622,8 +663,27 @@ bool attend_tc_supported(const AttnArgs& a) {
 
 int attend_tc_items_per_sm() { return 2; }
 
+template <class Sh>
 static size_t attend_tc_smem() {
-  return sizeof(Ctl) + 1024 + kQBufs * kQBytes + kStages * kStageBytes + 2 * kPBytes;
+  return sizeof(Ctl) + 1024 + kQBufs * kQBytes + Sh::kStages * kStageBytes + 2 * kPBytes;
+}
+static_assert(sizeof(Ctl) + 1024 + kQBufs * kQBytes + DeepShape::kStages * kStageBytes +
+                      2 * kPBytes <= 232448,
+              "the deep pipeline fits the 227 KB of shared memory a block may have");
+static_assert(2 * (sizeof(Ctl) + 1024 + kQBufs * kQBytes + ShallowShape::kStages * kStageBytes +
+                   2 * kPBytes) <= 233472,
+              "two shallow pipelines fit one SM");
+
+template <class Sh>
+static cudaError_t launch_shape(const TMaps& tm, const AttnArgs& a, int64_t items, int num_sms,
+                                cudaStream_t st) {
+  const size_t smem = attend_tc_smem<Sh>();
+  cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<Sh>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)min64((int64_t)Sh::kCtasPerSm * num_sms, items);
+  attend_tc_kernel<Sh><<<grid, Sh::kThreads, smem, st>>>(tm, a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_attend_tc(const AttnArgs& a, int num_sms, cudaStream_t st) {
@@ -632,13 +692,16 @@ cudaError_t launch_attend_tc(const AttnArgs& a, int num_sms, cudaStream_t st) {
   if (a.split_tiles > kAttnTcMaxSplitTiles) return cudaErrorInvalidValue;
   TMaps tm;
   if (!tmap_rows128(&tm.q, a.q, (uint64_t)a.B * a.T * a.H, kHeads)) return cudaErrorInvalidValue;
-  const size_t smem = attend_tc_smem();
-  cudaError_t e =
-      cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  const int grid = (int)min64((int64_t)kCtasPerSm * num_sms, items);
-  attend_tc_kernel<<<grid, kThreads, smem, st>>>(tm, a);
-  return cudaGetLastError();
+  // dense mode reads runs of consecutive compressed rows: by TMA where the
+  // caches admit a tensor map (16-byte aligned base)
+  const uint64_t crow = (uint64_t)a.B * a.N_cap;
+  tm.dense_tma = !a.gather && crow > 0 && tmap_rows128(&tm.k, a.kc, crow, kKeys) &&
+                 tmap_rows128(&tm.v, a.vc, crow, kKeys);
+  // many items (a prefill chunk): one deep pipeline per SM; a decode step's
+  // few short items: two shallow ones
+  return items >= kAttnDeepItemsPerSm * (int64_t)num_sms
+             ? launch_shape<DeepShape>(tm, a, items, num_sms, st)
+             : launch_shape<ShallowShape>(tm, a, items, num_sms, st);
 }
 
 }  // namespace sa

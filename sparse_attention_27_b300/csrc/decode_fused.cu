@@ -170,14 +170,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* sel = reinterpret_cast<int32_t*>(keys + a.cap);         // [a.selcap]
   unsigned char* X = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(sel + a.selcap) + 1023) & ~uintptr_t(1023));
-  // region X, by phase: score stages | top-k scratch | K/V stages + P tiles | partial O
+  // region X, by phase: score stages | top-k scratch | K/V stages | partial O
   unsigned char* sA = X;
   int* hist = reinterpret_cast<int*>(X);                           // [kFineBins]
   uint32_t* ck = reinterpret_cast<uint32_t*>(X + 4 * kFineBins);   // [kCandMax]
   int32_t* ci = reinterpret_cast<int32_t*>(ck + kCandMax);         // [kCandMax]
   TopkSmem& TS = *reinterpret_cast<TopkSmem*>(ci + kCandMax);
   unsigned char* sKV = X;                                          // [stages_kv][kKVBytes]
-  unsigned char* sP = X + a.stages_kv * kKVBytes;                  // [2][kPBytes]
+  // the P tiles of the attention take the score keys' space, dead once the
+  // top-k has passed its last cluster barrier
+  unsigned char* sP = reinterpret_cast<unsigned char*>(keys);      // [2][kPBytes]
   float* sO = reinterpret_cast<float*>(X);                         // [64][128]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -806,12 +808,13 @@ static size_t fused_smem(int cap, int selcap, int stages_a, int stages_kv) {
                        4 * (size_t)cap + 4 * (size_t)selcap;
   const size_t topk = 4 * (size_t)kFineBins + 8 * (size_t)kCandMax + sizeof(TopkSmem);
   const size_t x = std::max(std::max((size_t)stages_a * kABytes, topk),
-                            std::max((size_t)stages_kv * kKVBytes + 2 * kPBytes,
-                                     (size_t)kHeads * kD * 4));
+                            std::max((size_t)stages_kv * kKVBytes, (size_t)kHeads * kD * 4));
   return fixed + 1024 + x;
 }
 
 constexpr size_t kSmemMax = 232448;              // 227 KB per block on sm_100-class parts
+static_assert(4 * 8192 >= 2 * kPBytes, "the P tiles fit the smallest key array");
+static_assert((kBBytes + kQBytes) % 1024 == 0, "the P tiles start on a 1024-byte boundary");
 
 bool fused_decode_plan(FusedDecodeArgs& a, int num_sms) {
   if (a.B <= 0) return false;

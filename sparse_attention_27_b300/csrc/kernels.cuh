@@ -86,7 +86,9 @@ struct AttnArgs {
   int32_t* err;
 };
 constexpr int kAttnTile = 64;     // keys per attention tile (split granularity)
-constexpr int kAttnTcMaxSplitTiles = 32;   // tensor-core kernel: key tiles per split at most
+// tensor-core kernel: key tiles per split at most (a loop bound only: the
+// running sums stay below 2^32 per key, far inside fp32, at any length)
+constexpr int kAttnTcMaxSplitTiles = 1 << 16;
 cudaError_t launch_attend_simt(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_attend_tc(const AttnArgs& a, int num_sms, cudaStream_t st);
 bool attend_tc_supported(const AttnArgs& a);

@@ -87,7 +87,7 @@ def _sms_148():
 def test_attention_workspace_queries_follow_the_split_rule():
     """Workspace sizes of the attention calls, worked out by hand from the split
     rule: key lists of 64-key tiles; the tensor-core kernel aims at 2 (row,
-    split) items per SM and at most 32 tiles per split; split s has
+    split) items per SM, with no cap on a split's length; split s has
     ceil(tiles / ns) tiles; partials are rows*nsplit*H*d f32 for O plus
     rows*nsplit*H f32 for LSE, each rounded up to 256 B, then 256 B for the
     tensor-core kernel's item counter.  148 SMs (the count the library
@@ -107,8 +107,8 @@ def test_attention_workspace_queries_follow_the_split_rule():
     assert m.csa_attend_workspace_bytes(m.SA_BF16, 4, 1, 64, 128, 2048, 128) == ws(4, 34)
     # 1M decode HCA: 8192/64 + 2 = 130 tiles; 74 wanted -> 2 tiles each -> 65 splits
     assert m.hca_compress_attend_workspace_bytes(m.SA_BF16, 4, 1, 64, 128, 8192, 128) == ws(4, 65)
-    # 64K prefill CSA: one split wanted, but at most 32 tiles per split -> 2 splits of 17
-    assert m.csa_attend_workspace_bytes(m.SA_BF16, 1, 65536, 64, 128, 2048, 128) == ws(65536, 2)
+    # 64K prefill CSA: 65536 rows fill the SMs, one split of 34 tiles, no partials
+    assert m.csa_attend_workspace_bytes(m.SA_BF16, 1, 65536, 64, 128, 2048, 128) == ws(65536, 1)
     # fp32 (CUDA-core kernel, one item per CTA): 256 rows fill the SMs, no split
     assert m.csa_attend_workspace_bytes(m.SA_F32, 1, 256, 16, 128, 64, 128) == ws(256, 1)
 

@@ -199,6 +199,23 @@ def test_prefill_bf16_small(L, k, W):
     assert r["recall"] >= 0.98, r
 
 
+def test_prefill_bf16_deep_pipeline():
+    """A prefill chunk with enough query rows (3000 items a launch) for the
+    attention kernel's deep shape (one CTA per SM, six K/V stages, four
+    producer warps); raw key rows scaled by 2^band over 8 bands of position,
+    so that the pooled key rows and the window rows of later queries carry
+    larger logits and key lists cross rescale bands mid-item.  Every row is
+    compared with the oracle."""
+    w = synth.Workload("preD", "prefill", B=1, L=3000, T=3000, k=256, W=128, x8=True)
+    x = synth.make_inputs(w)
+    R = x["k_raw"].shape[1]
+    for band in range(1, 8):
+        rows = np.arange(band * R // 8, (band + 1) * R // 8)
+        synth.scale_rows(x["k_raw"][0], rows, float(2 ** band), w.dtype)
+    r = run_staged(w, x)
+    assert r["recall"] >= 0.98, r
+
+
 @pytest.mark.parametrize("H", [1, 16, 40])
 def test_decode_bf16_fewer_heads(H):
     w = synth.Workload("decH", "decode", B=3, L=3000, T=1, R=128, H=H, k=300, W=100, m2=16)
