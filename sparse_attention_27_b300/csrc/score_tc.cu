@@ -51,7 +51,9 @@ struct ScoreTcCfg {
   static constexpr int kTileBytes = kTileEntries * kDI * 2;   // 16 KB
   static constexpr int kABytes = kStageTiles * kTileBytes;    // 32 KB
   static constexpr int kBBytes = QG * kHI * kDI * 2;          // 8 KB per query
-  static constexpr size_t kSmem = 1024 /*align slack*/ + kStages * kABytes + 2 * kBBytes + 512 +
+  static constexpr int kWBytes = QG * kHI * 4;                // a group's head weights, f32
+  static constexpr size_t kSmem = 1024 /*align slack*/ + kStages * kABytes + 2 * kBBytes +
+                                  2 * kWBytes + 512 +
                                   kMaxJobsPerCta * sizeof(JobRec<QG>);
 };
 
@@ -65,7 +67,9 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* sA = smem;
   unsigned char* sB = sA + Cfg::kStages * Cfg::kABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + 2 * Cfg::kBBytes);
+  // the head weights of each epilogue warpgroup's current query group
+  float* sW = reinterpret_cast<float*>(sB + 2 * Cfg::kBBytes);         // [2][QG*64]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + 2 * Cfg::kBBytes + 2 * Cfg::kWBytes);
   uint64_t* full = bars;
   uint64_t* empty = full + Cfg::kStages;
   uint64_t* bfull = empty + Cfg::kStages;
@@ -176,15 +180,26 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     // Two warpgroups take alternate tiles (ordinal o of this CTA's tiles:
-    // group o % 2, accumulator o % kAccBufs).
+    // group o % 2, accumulator o % kAccBufs).  Each warpgroup copies the head
+    // weights of a job's query group into its own shared-memory slot when the
+    // group changes; the tile loop then reads them as broadcast float4s.
     const int grp = (warp - 2) >> 2;
     const int quad = warp & 3;
     const int row_in_tile = quad * 32 + lane;
+    const int gtid = (warp - 2 - 4 * grp) * 32 + lane;        // 0..127 in the warpgroup
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    int64_t o = 0;
+    float* wg = sW + grp * QG * kHI;
+    int64_t o = 0, prev_g = -1;
     for (int ji = 0; ji < n_my && !*s_abort; ++ji) {
       const JobRec<QG>& J = jobs[ji];
       if (J.t_lo >= J.t_hi) continue;
+      if (J.g != prev_g) {
+        named_bar_sync(1 + grp, 128);                         // the previous weights are read
+        const float* wsrc = p.w + ((int64_t)J.b * p.T + J.t0) * kHI;
+        for (int i = gtid; i < J.nq * kHI; i += 128) wg[i] = __ldg(wsrc + i);
+        named_bar_sync(1 + grp, 128);
+        prev_g = J.g;
+      }
       bool stop = false;
       for (int t = J.t_lo; t < J.t_hi; ++t, ++o) {
         if ((int)(o & 1) != grp) continue;
@@ -193,25 +208,24 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
         if (!mbar_wait(&tfull[acc], acc_ph, p.err)) { *s_abort = 1; stop = true; break; }
         tc_fence_after();
         const int64_t j = (int64_t)t * kTileEntries + row_in_tile;
+        const uint32_t tacc = tmem + lane_base + acc * Cfg::kAccCols;
 #pragma unroll 1
         for (int q = 0; q < J.nq; ++q) {
-          const int64_t r = (int64_t)J.b * p.T + J.t0 + q;
-          const float4* w4 = reinterpret_cast<const float4*>(p.w + r * kHI);
-          float4 wv[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) wv[i] = __ldg(w4 + i);
           uint32_t v[64];
-          tmem_ld32_async(tmem + lane_base + acc * Cfg::kAccCols + q * kHI, v);
-          tmem_ld32_async(tmem + lane_base + acc * Cfg::kAccCols + q * kHI + 32, v + 32);
+          tmem_ld32_async(tacc + q * kHI, v);
+          tmem_ld32_async(tacc + q * kHI + 32, v + 32);
           tmem_wait_ld();
+          const float4* w4 = reinterpret_cast<const float4*>(wg + q * kHI);
           float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            s0 = fmaf(wv[i].x, fmaxf(__uint_as_float(v[4 * i + 0]), 0.f), s0);
-            s1 = fmaf(wv[i].y, fmaxf(__uint_as_float(v[4 * i + 1]), 0.f), s1);
-            s2 = fmaf(wv[i].z, fmaxf(__uint_as_float(v[4 * i + 2]), 0.f), s2);
-            s3 = fmaf(wv[i].w, fmaxf(__uint_as_float(v[4 * i + 3]), 0.f), s3);
+            const float4 wv = w4[i];
+            s0 = fmaf(wv.x, fmaxf(__uint_as_float(v[4 * i + 0]), 0.f), s0);
+            s1 = fmaf(wv.y, fmaxf(__uint_as_float(v[4 * i + 1]), 0.f), s1);
+            s2 = fmaf(wv.z, fmaxf(__uint_as_float(v[4 * i + 2]), 0.f), s2);
+            s3 = fmaf(wv.w, fmaxf(__uint_as_float(v[4 * i + 3]), 0.f), s3);
           }
+          const int64_t r = (int64_t)J.b * p.T + J.t0 + q;
           if (j < J.n[q]) p.scores[r * p.ld + j] = (s0 + s1) + (s2 + s3);
         }
         tc_fence_before();
