@@ -90,6 +90,8 @@ struct Ctl {
   uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2];
   uint32_t tmem;
   int abort;
+  uint32_t smax;                               // largest key of this CTA's first score tile
+  uint32_t bin_lo;                             // the row's relative first-level bins (FineBins::lo)
   __align__(16) float w[kHI];                  // indexer head weights of the row
   float pw[kMaxPool];                          // pooling weights of one block
   float lse[kHeads];                           // this CTA's partial LSE
@@ -225,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&C.p_empty[s], 1);
     }
     C.abort = 0;
+    C.smax = 0u;
     if (rank == 0) {
       if (P.p >= 0 && ((int64_t)P.p + 1) / a.m > a.N_cap) set_err(a.err, SA_ERR_BOUNDS);
       if (!fresh_ok || fb_lo < 0) set_err(a.err, SA_ERR_BOUNDS);
@@ -239,6 +242,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = C.tmem;
+  // The top-k bins its keys relative to the row's largest sampled key: the
+  // first score tile of every CTA, published by the warpgroup that scores it.
+  // The cluster exchanges the samples through one barrier whose arrive comes
+  // early (the sampling warps right after their first tile, every other
+  // thread now) and whose wait comes only before the histogram.
+  const bool sample_x = Cn > 1 && !P.all;
+  const bool sampler = warp >= kWarpEpi && warp < kWarpEpi + 4;   // epilogue group 0: tile 0
+  if (sample_x && !sampler) cluster_arrive_release();
 
   if (warp == kWarpTma && lane == 0) {
     tma_prefetch_desc(&tm.ik);
@@ -309,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const float4* w4 = reinterpret_cast<const float4*>(C.w);
+    bool arrived = false;                        // the sampling warps' cluster arrive
     for (int o = grp; o < nt_score; o += kEpiGroups) {
       const int acc = o % kAcc;
       if (*abort_flag || !mbar_wait(&C.t_full[acc], (uint32_t)((o / kAcc) & 1), a.err)) {
@@ -336,7 +348,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool real = lo + jl < P.n;
       nan_local |= real && is_nan_bits(s);
       keys[jl] = real ? score_key(s) : 0u;
+      if (o == 0) {                                         // the sample: tile 0, group 0
+        if (real) atomicMax(&C.smax, score_key(s));
+        if (sample_x) cluster_arrive_release();
+        arrived = true;
+      }
     }
+    // no tile 0 here, or stopped before it: the arrive all the same, so that
+    // every thread of the cluster passes the barrier
+    if (grp == 0 && sample_x && !arrived) cluster_arrive_release();
   };
   if (warp >= kWarpEpi && warp < kWarpEpi + 8) {
     score_epilogue((warp - kWarpEpi) >> 2);
@@ -392,17 +412,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* out_idx = a.idx + (int64_t)b * k;
   const int sel_lo = at_lo * kKeys;              // first list position this CTA attends
   if (!P.all) {
+    if (sample_x) cluster_wait_acquire();         // every CTA's sample is in place
+    if (tid == 0) {
+      uint32_t mx = C.smax;
+      for (int r = 0; r < Cn; ++r) mx = max(mx, Cn > 1 ? *peer(&C.smax, r) : mx);
+      // 1024 bins per octave from 6 octaves below the sample's largest key to
+      // 2 above it (no sample: the absolute bins)
+      const uint32_t v = mx >> 13;
+      C.bin_lo = mx == 0u ? 0xFFFFFFFFu : (v > 6u * 1024u ? v - 6u * 1024u : 0u);
+    }
     for (int i = tid; i < kFineBins; i += kThreads) hist[i] = 0;
     __syncthreads();
-    for (int i = tid; i < cnt; i += kThreads) atomicAdd(&hist[keys[i] >> kFineShift], 1);
+    const FineBins fb = C.bin_lo == 0xFFFFFFFFu ? kAbsoluteBins : FineBins{13, C.bin_lo};
+    for (int i = tid; i < cnt; i += kThreads) atomicAdd(&hist[fb.bin(keys[i])], 1);
     __syncthreads();
     auto emit = [&](int pos, int j) { out_idx[pos] = j; };
     if (a.cap == 8192)
       topk_select<kThreads, 16>(TS, keys, cnt, lo, hist, ck, ci, nan_local, k, Cn, rank, a.err,
-                                emit);
+                                emit, fb);
     else
       topk_select<kThreads, 32>(TS, keys, cnt, lo, hist, ck, ci, nan_local, k, Cn, rank, a.err,
-                                emit);
+                                emit, fb);
     // the selection is complete in global memory (topk_select ends with a
     // cluster barrier after the emission): this CTA's share of the key list,
     // read through L2 (other CTAs wrote it), padding slots -1

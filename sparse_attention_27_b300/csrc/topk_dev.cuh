@@ -16,8 +16,9 @@
 // in lane l, bank-conflict free), so a ballot over one j lists keys in index
 // order.  Three steps over the CTA's keys:
 //  A. a histogram of their top 13 bits (sign, exponent, 4 mantissa bits: 8192
-//     bins, one atomic per key), summed over the cluster through distributed
-//     shared memory, gives the bin holding the row's k-th largest key;
+//     bins, one atomic per key; or a relative map of 1024 bins per octave, see
+//     FineBins), summed over the cluster through distributed shared memory,
+//     gives the bin holding the row's k-th largest key;
 //  B. each CTA lists its keys in that bin with their indices and counts, per
 //     warp, its keys in higher bins; every CTA then copies all the cluster's
 //     lists into one and finds the exact k-th largest T in it (rank counting
@@ -63,6 +64,30 @@ constexpr int kFineBins = 1 << (32 - kFineShift);          // 8192
 constexpr int kCandMax = 4096;                             // listed keys of one bin
 constexpr int kRankMax = 256;
 constexpr int kRowsMaxCluster = 16;
+
+// The first-level bins of a row's keys, kFineBins of them, monotone in the
+// key.  Absolute (shift 19, lo 0): bin = the key's top 13 bits.  Relative
+// (shift 13): bin = (key >> 13) - lo, the values at or below lo in bin 0 and
+// those at or above lo + kFineBins - 1 in the last bin -- 1024 bins per octave
+// of the score over a window of 8 octaves placed by the caller.  A bin's keys
+// share their top `top` bits (prefix), which the exact select then leaves
+// alone; the two end bins of the relative map share none.
+struct FineBins {
+  int shift;
+  uint32_t lo;
+  __device__ __forceinline__ uint32_t bin(uint32_t key) const {
+    const uint32_t v = key >> shift;
+    return v <= lo ? 0u : min(v - lo, (uint32_t)(kFineBins - 1));
+  }
+  __device__ __forceinline__ bool clamped(uint32_t b) const {
+    return shift != kFineShift && (b == 0 || b == (uint32_t)(kFineBins - 1));
+  }
+  __device__ __forceinline__ int top(uint32_t b) const { return clamped(b) ? 0 : 32 - shift; }
+  __device__ __forceinline__ uint32_t prefix(uint32_t b) const {
+    return clamped(b) ? 0u : (lo + b) << shift;
+  }
+};
+constexpr FineBins kAbsoluteBins{kFineShift, 0u};
 
 // Sum of v over the CTA, returned to every thread.
 template <int NT>
@@ -333,7 +358,7 @@ __device__ uint32_t radix_select(const uint32_t* keys, int m, int kk, TopkSmem& 
 template <int NT, int KPL, class Emit>
 __device__ void topk_select(TopkSmem& S, const uint32_t* keys, int cnt, int lo, int* hist,
                             uint32_t* ck, int32_t* ci, int nan_local, int k, int C, int rank,
-                            int32_t* err, Emit emit) {
+                            int32_t* err, Emit emit, const FineBins fb = kAbsoluteBins) {
   constexpr int NW = NT / 32;
   constexpr int CAP = NT * KPL;                  // key slots of this CTA
   uint32_t* uk = reinterpret_cast<uint32_t*>(hist);                 // [kCandMax] union keys
@@ -373,7 +398,7 @@ __device__ void topk_select(TopkSmem& S, const uint32_t* keys, int cnt, int lo, 
 #pragma unroll 4
   for (int j = 0; j < KPL; ++j) {
     const uint32_t key = wkeys[32 * j];
-    const uint32_t hb = key >> kFineShift;       // empty slots: key 0, never above sel
+    const uint32_t hb = fb.bin(key);             // empty slots: key 0, never above sel
     above_w += __popc(__ballot_sync(0xffffffffu, hb > sel));
     const bool in = key != 0u && hb == sel;
     in_w += __popc(__ballot_sync(0xffffffffu, in));
@@ -451,7 +476,7 @@ __device__ void topk_select(TopkSmem& S, const uint32_t* keys, int cnt, int lo, 
       T = S.T;
       take = S.take;
     } else {
-      T = radix_select<NT>(uk, c_all, r1, S, &take, 32 - kFineShift, sel << kFineShift, 1);
+      T = radix_select<NT>(uk, c_all, r1, S, &take, fb.top(sel), fb.prefix(sel), 1);
     }
     // the union's share of the counts: per warp of this CTA, and before it
     int gb = 0, eb = 0;
@@ -472,7 +497,10 @@ __device__ void topk_select(TopkSmem& S, const uint32_t* keys, int cnt, int lo, 
     eq_before += both & 0xFFFF;
     __syncthreads();
   } else {                                       // heavily tied: cluster-wide radix passes
-    T = radix_select<NT>(keys, CAP, r1, S, &take, 32 - kFineShift, sel << kFineShift, C);
+    // over every key of the row: within an end bin of a relative map (no
+    // shared prefix) the bin's r1-th largest is the row's k-th largest
+    T = radix_select<NT>(keys, CAP, fb.clamped(sel) ? k : r1, S, &take, fb.top(sel),
+                         fb.prefix(sel), C);
     int g = 0, e = 0;
 #pragma unroll 4
     for (int j = 0; j < KPL; ++j) {

@@ -15,8 +15,9 @@ csa_index_topk, csa_attend) on the same inputs:
 Shapes cover several tiles per CTA with a ragged last tile, rows whose
 visible entries are all selected (n <= k), rows where no block closes, very
 early positions (no compressed entry, a short window), k = 0 (window only),
-fewer heads than the MMA's 64, a NaN row, and the full 128K and 1M decode
-workloads.
+fewer heads than the MMA's 64, a NaN row, rows whose k-th largest score
+falls outside the top-k's relative bin window, and the full 128K and 1M
+decode workloads.
 """
 from __future__ import annotations
 
@@ -131,6 +132,33 @@ def test_fused_decode_nan_row_rejected_like_the_three_calls():
     x["w_idx"][1, 0, 5] = np.nan
     r = check_fused(w, x, expect_err=1 << sa().SA_ERR_NAN)
     assert np.all(r["idx"][1] == -1) and np.all(r["idx"][[0, 2]] >= 0)
+
+
+@pytest.mark.parametrize("case", ["sample_far_above", "top_bin_lists", "top_bin_overflow"])
+def test_fused_topk_relative_bins_end_bins(case):
+    """The fused top-k bins keys relative to the largest key of each CTA's
+    first score tile (1024 bins per octave, 6 octaves below that sample to 2
+    above); keys outside the window share an end bin, which the exact select
+    handles without the bins' shared prefix.  Indexer key rows scaled by 2^10
+    put the k-th largest key there: in the bottom bin (a few huge rows in the
+    sampled tiles, k past them: the bin overflows the lists, cluster-wide
+    radix passes), in the top bin with ~3000 keys (listed, exact select over
+    the union) and with ~5000 (overflow).  idx must stay bit-identical to
+    csa_index_topk's and a valid top-k of the oracle's scores."""
+    w = synth.Workload("frel", "decode", B=4, L=65536, T=1, R=128,
+                       k=256 if case == "sample_far_above" else 2048, x8=True)
+    x = synth.make_inputs(w)
+    g = np.random.default_rng(5)
+    tiles = w.ncap // 128
+    for b in range(w.B):
+        if case == "sample_far_above":          # 4 rows in every 8th tile (each CTA's first)
+            rows = np.concatenate([t * 128 + g.choice(128, 4, replace=False)
+                                   for t in range(0, tiles, 8)])
+        else:                                   # rows outside every 8th tile
+            cand = np.array([j for j in range(w.ncap - 8) if (j // 128) % 8 != 0])
+            rows = g.choice(cand, 3000 if case == "top_bin_lists" else 5000, replace=False)
+        synth.scale_rows(x["ik_c"][b], np.sort(rows), 1024.0, "bf16")
+    check_fused(w, x)
 
 
 @pytest.mark.parametrize("name", ["decode128k", "decode1m"])
