@@ -17,7 +17,9 @@
 namespace sa {
 
 // topk_rows_kernel: step A's input -- the row's fp32 scores, turned into
-// keys and the 13-bit histogram with 16-byte loads -- then topk_select.
+// keys with 16-byte loads, the row's largest key (over the cluster), and the
+// histogram of the keys binned relative to it (FineBins: 1024 bins per
+// octave from 6 octaves below the largest key) -- then topk_select.
 template <int NT, int KPL>
 __global__ void __launch_bounds__(NT, 1) topk_rows_kernel(TopkArgs a, int C, int chunk) {
   constexpr int CAP = NT * KPL;                  // keys one CTA holds
@@ -61,13 +63,16 @@ __global__ void __launch_bounds__(NT, 1) topk_rows_kernel(TopkArgs a, int C, int
     }
   }
   for (int i = tid; i < kFineBins; i += NT) hist[i] = 0;      // while the loads fly
+  if (tid == 0) S.kmax = 0u;
   __syncthreads();
   int nan_local = 0;
+  uint32_t kmax = 0u;
   auto put = [&](int i, float v) -> uint32_t {
     if (i >= cnt) return 0u;
-    nan_local |= is_nan_bits(v);
+    const bool nan = is_nan_bits(v);
+    nan_local |= nan;
     const uint32_t key = score_key(v);
-    atomicAdd(&hist[key >> kFineShift], 1);
+    if (!nan) kmax = max(kmax, key);
     return key;
   };
 #pragma unroll
@@ -77,9 +82,22 @@ __global__ void __launch_bounds__(NT, 1) topk_rows_kernel(TopkArgs a, int C, int
         make_uint4(put(4 * g, f[q].x), put(4 * g + 1, f[q].y), put(4 * g + 2, f[q].z),
                    put(4 * g + 3, f[q].w));
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  if ((tid & 31) == 0 && kmax > 0u) atomicMax(&S.kmax, kmax);
+  if (C > 1) cluster_sync(); else __syncthreads();   // every CTA's largest key is in place
+  uint32_t mx = S.kmax;
+  for (int r = 0; r < C; ++r) mx = max(mx, C > 1 ? *peer(&S.kmax, r) : mx);
+  const uint32_t v = mx >> 13;
+  const FineBins fb = mx == 0u ? kAbsoluteBins
+                               : FineBins{13, v > 6u * 1024u ? v - 6u * 1024u : 0u};
+  for (int i = tid; i < CAP; i += NT) {
+    const uint32_t key = keys[i];
+    if (key != 0u) atomicAdd(&hist[fb.bin(key)], 1);
+  }
   nan_local = __syncthreads_or(nan_local);
   topk_select<NT, KPL>(S, keys, cnt, lo, hist, ck, ci, nan_local, k, C, rank, a.err,
-                       [&](int pos, int j) { out[pos] = j; });
+                       [&](int pos, int j) { out[pos] = j; }, fb);
 }
 
 static size_t rows_smem(int nt, int kpl) {

@@ -48,6 +48,7 @@ struct TopkSmem {
   int sel_bin, above;
   int take;                               // keys equal to T that are kept
   uint32_t T;                             // the k-th largest key
+  uint32_t kmax;                          // this CTA's largest key (relative bins)
 };
 
 __device__ __forceinline__ unsigned lanemask_lt() {
