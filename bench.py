@@ -385,15 +385,16 @@ def load_cudart():
 
 
 class PipelinedIO:
-    """End-to-end decode steps from pinned host memory, double-buffered.
+    """End-to-end decode steps from pinned host memory, over three buffer sets.
 
-    Two HybridSteps (buffer sets 0 and 1) share the caches and rings; each has
+    Three HybridSteps (buffer sets 0, 1, 2) share the caches and rings; each has
     its own per-step inputs -- q, q_hca, q_idx, w_idx, q_pos and the new
     token's ring rows (staged) -- in one device buffer filled by one copy from
     one pinned host buffer, and its own outputs (o, lse, ho, hlse) in one
     device buffer read back by one copy.  ``record`` captures n consecutive
     steps: while step k computes, step k + 1's inputs are already in place and
-    step k - 1's outputs go out on a copy stream.  Each step first writes its
+    step k - 1's outputs go out on a copy stream; a set's refill and readout
+    have two steps' time before the set is used again.  Each step first writes its
     token into ring row t mod R of every layer's per-token arrays
     (sa_ring_write, one launch) on the CSA stream, before either layer runs.
     Every step's copies are inside the timed region."""
@@ -401,6 +402,8 @@ class PipelinedIO:
     IN = ["q", "q_hca", "q_idx", "w_idx", "q_pos"]
     RING = {"csa": ["k_raw", "v_raw", "ik_raw", "z"], "hca": ["hk_raw", "hv_raw", "hz"]}
     OUT = ["o", "lse", "ho", "hlse"]
+
+    SETS = 3
 
     def __init__(self, w, x, mode: str):
         import numpy as np
@@ -412,7 +415,7 @@ class PipelinedIO:
         slot = (w.L - 1) % w.ring
         ring_names = self.RING["csa"] + self.RING["hca"]
         self.steps, self.d_in, self.h_in, self.d_out, self.h_out, self.staged = [], [], [], [], [], []
-        for p in range(2):
+        for p in range(self.SETS):
             xs = dict(base.x)
             tens = [base.x[n] for n in self.IN] + [base.x[n][:, slot] for n in ring_names]
             buf, views = self._carve(tens, dev)
@@ -484,25 +487,25 @@ class PipelinedIO:
             st.hca(s_hca)
 
     def record(self, s_csa, s_hca, s_cp, s_out, n: int = 4):
-        """n consecutive steps over the two buffer sets (step k uses set k
-        mod 2).  The compute streams wait on each other directly: step k's
+        """n consecutive steps over the buffer sets (step k uses set k mod
+        SETS).  The compute streams wait on each other directly: step k's
         CSA stream (its ring write, then the CSA layer) after step k - 1's HCA
         layer, step k's HCA stream after step k's ring write.  A step's inputs
         were copied in while the step before it ran; its outputs go out while
         the next one runs; its set is refilled from pinned memory for step
-        k + 2 (or the next replay) once it is done, and step k + 2 writes the
-        set's outputs only after they have gone out."""
+        k + SETS (or the next replay) once it is done, and step k + SETS writes
+        the set's outputs only after they have gone out."""
         import torch
         cur = torch.cuda.current_stream()
         start = torch.cuda.Event()
         start.record(cur)
         for s_ in (s_csa, s_hca, s_cp, s_out):
             s_.wait_event(start)
-        in_ev = [None, None]                      # inputs of set p in place
-        out_ev = [None, None]                     # outputs of set p copied out
+        in_ev = [None] * self.SETS                # inputs of set p in place
+        out_ev = [None] * self.SETS               # outputs of set p copied out
         hca_done = None                           # the previous step's HCA layer
         for k in range(n):
-            p = k % 2
+            p = k % self.SETS
             for e in (in_ev[p], out_ev[p], hca_done):
                 if e is not None:
                     s_csa.wait_event(e)
@@ -519,7 +522,7 @@ class PipelinedIO:
             out_ev[p].record(s_out)
             s_cp.wait_event(e1)
             s_cp.wait_event(e2)
-            with torch.cuda.stream(s_cp):         # refill this set for step k + 2
+            with torch.cuda.stream(s_cp):         # refill this set for step k + SETS
                 self.d_in[p].copy_(self.h_in[p], non_blocking=True)
             in_ev[p] = torch.cuda.Event()
             in_ev[p].record(s_cp)
@@ -721,16 +724,16 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
     step_gbs = ab["step"] / (total_ms / steps / 1e3) / 1e9
 
     # ---- end to end: each step's inputs from pinned host memory, its
-    # outputs back to pinned host memory, two steps per graph, double-buffered
+    # outputs back to pinned host memory, sixteen steps per graph, three buffer sets
     e2e_out = None
     if e2e:
         pio = PipelinedIO(w, x, mode)
         s_cp, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-        # eight steps per graph: the L2 flush before each timed replay leaves
+        # sixteen steps per graph: the L2 flush before each timed replay leaves
         # the first host-to-device copy after it several times slower than the
         # rest (measured 106-118 against 29 us for 1.36 MB), a cost a decode
         # loop pays once, not every step
-        per_graph = 8
+        per_graph = 16
         for _ in range(2):
             pio.record(s_csa, s_hca, s_cp, s_out, per_graph)
         torch.cuda.synchronize()
@@ -748,8 +751,10 @@ def decode_measure(w, steps: int, warmup: int, rank: int, world: int, local: int
                    "note": "pinned host buffers; each step one copy of its inputs in (q, q_hca, "
                            "q_idx, w, positions, the new ring rows) and one of its outputs (O in "
                            "bf16, LSE) out, and one sa_ring_write of its token into the rings; "
-                           "double-buffered, eight steps per graph: a step's inputs arrive while "
-                           "the step before it runs, its outputs leave while the next one runs"}
+                           "three buffer sets, sixteen steps per graph (L2 flushed before each "
+                           "graph): a step's inputs arrive "
+                           "while the step before it runs, its outputs leave while the next one "
+                           "runs, and a set is reused two steps after it was freed"}
         del pio
     out = {
         "value": value, "ms_per_step": total_ms / steps,
