@@ -64,6 +64,8 @@ namespace sa {
 
 namespace {
 
+constexpr int kMaxStages = 6;                  // K/V stages of the deepest shape
+
 // One shape of the pipeline: CTAs per SM, K/V stages per CTA, producer warps.
 // A producer's wait for stage n % S is sound by parity only while that
 // barrier is at most one phase behind: the warp's own previous tile n - P
@@ -80,6 +82,7 @@ struct AttnShape {
   // warps that read every item: the producers, the MMA warp, the 4 softmax warps
   static constexpr int kItemReaders = kProd + 1 + 4;
   static_assert(kProd <= kStg, "parity waits of the producers");
+  static_assert(kStg <= kMaxStages, "stage barriers in Ctl");
 };
 using ShallowShape = AttnShape<2, 2, 2>;         // decode: two pipelines per SM
 using DeepShape = AttnShape<1, 6, 4>;            // long key lists: one deep pipeline
@@ -87,7 +90,6 @@ using DeepShape = AttnShape<1, 6, 4>;            // long key lists: one deep pip
 constexpr int kAttnDeepItemsPerSm = 8;
 
 constexpr int kKeys = 64;                      // keys per tile
-constexpr int kMaxStages = 6;
 constexpr int kQBufs = 1;                      // query tiles per CTA
 constexpr int kOBufs = 1;                      // TMEM O accumulators per CTA
 constexpr int kD = 128;                        // head dim

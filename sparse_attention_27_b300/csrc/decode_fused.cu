@@ -323,7 +323,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool arrived = false;                        // the sampling warps' cluster arrive
     for (int o = grp; o < nt_score; o += kEpiGroups) {
       const int acc = o % kAcc;
-      if (*abort_flag || !mbar_wait(&C.t_full[acc], (uint32_t)((o / kAcc) & 1), a.err)) {
+      // warp-uniform: the TMEM loads below are warp-collective
+      if (!__all_sync(0xffffffffu, !*abort_flag &&
+                                       mbar_wait(&C.t_full[acc], (uint32_t)((o / kAcc) & 1), a.err))) {
         *abort_flag = 1;
         break;
       }

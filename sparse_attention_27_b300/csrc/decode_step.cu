@@ -1267,7 +1267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int first = (grp - K.tiles % kEpiGroups + kEpiGroups) % kEpiGroups;
         for (int o = first; o < nt && live; o += kEpiGroups) {
           const int og = K.tiles + o, acc = og % kAcc;
-          if (*abort_flag || !mbar_wait(&C.t_full[acc], (uint32_t)((og / kAcc) & 1), a.err)) {
+          // warp-uniform: the TMEM loads below are warp-collective
+          if (!__all_sync(0xffffffffu,
+                          !*abort_flag &&
+                              mbar_wait(&C.t_full[acc], (uint32_t)((og / kAcc) & 1), a.err))) {
             fail();
             break;
           }

@@ -348,7 +348,10 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
         // the query group's B tile: QG*64 rows (query q, head h), two blocks
         // each, zero past nq
         const int slot = nsw & 1;
-        if (!mbar_wait(&b_empty[slot], ((nsw >> 1) & 1) ^ 1, p.err)) { *s_abort = 1; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&b_empty[slot], ((nsw >> 1) & 1) ^ 1, p.err))) {
+          *s_abort = 1;
+          break;
+        }
         unsigned char* tile = sB + slot * Cfg::kBBytes;
         for (int it = tc; it < QG * kIdxHeads * 2; it += kConvThreads) {
           const int rr = it >> 1, hh = it & 1;
@@ -374,7 +377,11 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
         const int nsub = min(kS, J.t_hi - t);
         const int rstage = (int)(k % kRawStages), astage = (int)(k % kAStages);
         const uint32_t rph = (uint32_t)((k / kRawStages) & 1), aph = (uint32_t)((k / kAStages) & 1);
-        if (!mbar_wait(&raw_full[rstage], rph, p.err)) { *s_abort = 1; stop = true; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&raw_full[rstage], rph, p.err))) {
+          *s_abort = 1;
+          stop = true;
+          break;
+        }
         // all of the step's loads first, then the stage is released
         const unsigned char* raw = sRaw + rstage * Cfg::kRawBytes;
         uint4 cw[kS][kHalves];
@@ -391,7 +398,11 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
           }
         }
         mbar_arrive(&raw_empty[rstage]);
-        if (!mbar_wait(&a_empty[astage], aph ^ 1, p.err)) { *s_abort = 1; stop = true; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&a_empty[astage], aph ^ 1, p.err))) {
+          *s_abort = 1;
+          stop = true;
+          break;
+        }
         unsigned char* a = sA + astage * Cfg::kAStepBytes;
         float* ksd = s_ks + (int)(k % kKsSlots) * Cfg::kStepEntries;
 #pragma unroll
@@ -435,14 +446,15 @@ __global__ void __launch_bounds__(kMxThreads, 1) score_mx_kernel(ScoreJobs p, Mx
       for (int t = J.t_lo; t < J.t_hi; t += kS, ++k) {
         const int nsub = min(kS, J.t_hi - t);
         const int acc = (int)(k % kAccBufs);
-        if (!mbar_wait(&t_full[acc], (uint32_t)((k / kAccBufs) & 1), p.err)) {
+        // warp-uniform waits: the TMEM loads below are warp-collective
+        if (!__all_sync(0xffffffffu, mbar_wait(&t_full[acc], (uint32_t)((k / kAccBufs) & 1), p.err))) {
           *s_abort = 1;
           stop = true;
           break;
         }
         // this thread's entry rows' factors 2^(e_row), from the converters' ring
         const int ks = (int)(k % kKsSlots);
-        if (!mbar_wait(&ks_full[ks], (uint32_t)((k / kKsSlots) & 1), p.err)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&ks_full[ks], (uint32_t)((k / kKsSlots) & 1), p.err))) {
           *s_abort = 1;
           stop = true;
           break;

@@ -189,8 +189,11 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
     const int gtid = (warp - 2 - 4 * grp) * 32 + lane;        // 0..127 in the warpgroup
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     float* wg = sW + grp * QG * kHI;
+    // Every thread walks every job, so that all 128 reach each named barrier;
+    // once a wait gives up or the CTA aborts, the warp only skips its tiles.
     int64_t o = 0, prev_g = -1;
-    for (int ji = 0; ji < n_my && !*s_abort; ++ji) {
+    bool stop = false;
+    for (int ji = 0; ji < n_my; ++ji) {
       const JobRec<QG>& J = jobs[ji];
       if (J.t_lo >= J.t_hi) continue;
       if (J.g != prev_g) {
@@ -200,12 +203,17 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
         named_bar_sync(1 + grp, 128);
         prev_g = J.g;
       }
-      bool stop = false;
       for (int t = J.t_lo; t < J.t_hi; ++t, ++o) {
         if ((int)(o & 1) != grp) continue;
+        stop = __any_sync(0xffffffffu, stop || *s_abort);
+        if (stop) continue;
         const int acc = (int)(o % Cfg::kAccBufs);
         const uint32_t acc_ph = (uint32_t)((o / Cfg::kAccBufs) & 1);
-        if (!mbar_wait(&tfull[acc], acc_ph, p.err)) { *s_abort = 1; stop = true; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_ph, p.err))) {
+          *s_abort = 1;
+          stop = true;
+          continue;
+        }
         tc_fence_after();
         const int64_t j = (int64_t)t * kTileEntries + row_in_tile;
         const uint32_t tacc = tmem + lane_base + acc * Cfg::kAccCols;
@@ -231,7 +239,6 @@ __global__ void __launch_bounds__(kScoreTcThreads, 1)
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
       }
-      if (stop) break;
     }
   }
   tc_fence_before();
